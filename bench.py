@@ -1,0 +1,378 @@
+"""Benchmark of the FP32 GEMM C = A x B on the 8192^3 N(0,1) workload.
+
+One step = one product through the C ABI (split pre-pass + GEMM kernel [+
+split-K reduce]) with A, B and C resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--path auto|tf32x3|ffma] [--split-k S]
+
+--impl reference times the CPU oracle (the plain fp64 triple loop) on a
+bounded row sample of the same workload.  Under torchrun every rank runs the
+same product on its own GPU (independent replicas: the product has no
+exchange step), and the value is the aggregate over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from shared_memory_tiled_fp32_gb300.workloads import WORKLOADS, make_inputs, row_order  # noqa: E402
+
+METRIC = "FP32 GEMM TFLOP/s at M=N=K=4096/8192 and % of roofline; max rel error"
+DEFAULT_WORKLOAD = "sq8192_normal"
+# nominal dense tensor rates (PFLOP/s): tf32 1.1, bf16 2.25 -> ratio for scaling
+# the measured bf16 peak to tf32
+TF32_OVER_BF16 = 1.1 / 2.25
+# GB300 CUDA cores: 152 SMs x 128 fp32 FMA lanes x 2 FLOP per clock
+FFMA_FLOP_PER_CLK = 152 * 128 * 2
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+                  "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--path", default="auto", choices=["auto", "tf32x3", "ffma"])
+    ap.add_argument("--split-k", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline (profiling runs)")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples taken between wall times t0 and t1 (the
+        timed region; the nearest sample after t0 if none fell inside)."""
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        chosen = self.lines
+        if t0 is not None:
+            inside = [x for x in self.lines if t0 <= x[0] <= t1 + 0.12]
+            after = [x for x in self.lines if x[0] >= t0]
+            chosen = inside or after[:1] or self.lines[-1:]
+        for _, ln in chosen:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": float(np.median(sms)), "sm_max_mhz": max(maxs), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+def traffic_from_profiles(kernel_tag: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    src = os.path.join(ROOT, "shared_memory_tiled_fp32_gb300", "csrc", "tg_kernels.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    prof = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    if not os.path.exists(prof):
+        return None
+    text = open(prof).read()
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_b) or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+def oracle_rows_timed(A_np, B_np, rows):
+    import oracle
+
+    t0 = time.perf_counter()
+    ref = oracle.sgemm_rows(A_np, B_np, rows)
+    return ref, time.perf_counter() - t0
+
+
+def cpu_baseline(w, A_np, B_np, target_s):
+    """Time the oracle on a seeded row sample sized to ~target_s seconds."""
+    import oracle
+
+    rows_all = row_order(w).numpy()  # seeded random order of the output rows
+    probe = rows_all[: max(oracle.threads(), 8)]
+    _, t_probe = oracle_rows_timed(A_np, B_np, probe)
+    per_row = t_probe / len(probe)
+    n = int(min(w.M, max(len(probe), target_s / max(per_row, 1e-9))))
+    n = max(oracle.threads(), n // oracle.threads() * oracle.threads())
+    rows = np.sort(rows_all[:n])
+    ref, t = oracle_rows_timed(A_np, B_np, rows)
+    value = 2.0 * len(rows) * w.N * w.K / t / 1e12
+    return rows, ref, {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                       "sample": f"{len(rows)} of {w.M} output rows (all {w.N} columns), seeded; "
+                                 f"{t:.1f} s of fp64 triple-loop work"}
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    A, B = make_inputs(w.M, w.N, w.K, w.dist, w.seed)
+    A_np, B_np = A.numpy(), B.numpy()
+    rows_all = row_order(w).numpy()
+    probe = rows_all[: max(oracle.threads(), 8)]
+    _, t_probe = oracle_rows_timed(A_np, B_np, probe)
+    per_row = t_probe / len(probe)
+    # each step: a bounded row sample sized so the whole run takes ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(oracle.threads(), min(w.M, budget / max(per_row, 1e-9))))
+    n = max(oracle.threads(), n // oracle.threads() * oracle.threads())
+    for s in range(args.warmup):
+        oracle_rows_timed(A_np, B_np, np.sort(rows_all[s * n % w.M:][:n]))
+    times = []
+    for s in range(args.steps):
+        _, t = oracle_rows_timed(A_np, B_np, np.sort(rows_all[(s + args.warmup) * n % w.M:][:n]))
+        times.append(t)
+    t_step = float(np.mean(times))
+    value = 2.0 * n * w.N * w.K / t_step / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dist": w.dist, "seed": w.seed,
+                   "step": f"oracle on {n} sampled output rows"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{n} of {w.M} output rows per step (all {w.N} columns)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    w = WORKLOADS[args.workload]
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    import shared_memory_tiled_fp32_gb300 as tg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tg.lib()
+    A, B = make_inputs(w.M, w.N, w.K, w.dist, w.seed)
+    Ad, Bd = A.to(dev), B.to(dev)
+    Cd = torch.empty(w.M, w.N, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plan = tg.plan(w.M, w.N, w.K, A=Ad.data_ptr(), B=Bd.data_ptr(), C=Cd.data_ptr(), path=args.path,
+                   split_k=args.split_k)
+    ws = torch.empty(max(1, plan["workspace_bytes"] // 4 + 64), device=dev)
+
+    def step(ev0=None, ev1=None):
+        tg.matmul(Ad, Bd, out=Cd, path=args.path, split_k=args.split_k, workspace=ws,
+                  main_begin=ev0, main_end=ev1, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if tg.sync_status() != 0:
+        raise RuntimeError("a kernel reported a timeout during warm-up")
+
+    # per-step events around the main GEMM kernel (recorded once to create them)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        e1.record(stream)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(*evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(wall0, wall1)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    main_ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+    if world > 1:
+        t = torch.tensor([elapsed_ms, main_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms, main_ms = float(t[0]), float(t[1])
+    status = tg.sync_status()
+    if status != 0:
+        raise RuntimeError(f"a kernel reported status {status} in the timed region")
+    ms_per_step = elapsed_ms / args.steps
+    value = w.flop * world / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the host-buffer entry point (pinned memory)
+    Ap, Bp = A.pin_memory(), B.pin_memory()
+    Cp = torch.empty(w.M, w.N).pin_memory()
+    tg.sgemm_host(Ap, Bp, Cp, path=args.path, split_k=args.split_k)
+    e2e_times = []
+    for _ in range(args.e2e_steps):
+        t0 = time.perf_counter()
+        tg.sgemm_host(Ap, Bp, Cp, path=args.path, split_k=args.split_k)
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = float(np.mean(e2e_times))
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    timed_region_s = elapsed_ms * 1e-3
+    sustained = timed_region_s >= 1.0
+    math_tflops = 2.0 * w.M * w.N * w.K / (main_ms * 1e-3) / 1e12
+    if plan["path"] == "tf32x3":
+        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        peak = bf16 * TF32_OVER_BF16 / 3.0
+        bound = "tensor"
+        peak_note = (f"tf32 dense = {'sustained' if sustained else 'burst'} bf16 of {peak_src} "
+                     f"({bf16} TFLOP/s) x 1.1/2.25; three tf32 products per useful FMA -> / 3")
+        kernel_tag = "tf32x3_gemm"
+    else:
+        peak = FFMA_FLOP_PER_CLK * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        bound = "alu"
+        peak_note = "152 SMs x 128 FMA lanes x 2 FLOP x max SM clock"
+        kernel_tag = "ffma_gemm"
+    traffic = traffic_from_profiles(kernel_tag, w.name)
+
+    # correctness and the CPU baseline on the same seeded row sample
+    cpu = None
+    max_rel = None
+    if not args.no_cpu:
+        rows, ref, cpu = cpu_baseline(w, A.numpy(), B.numpy(), args.cpu_seconds)
+        got = Cd[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
+        r64 = ref.astype(np.float64)
+        max_rel = float(np.linalg.norm(got - r64) / np.linalg.norm(r64))
+        elt = float(np.abs(got - r64).max() / np.abs(r64).max())
+        max_rel = {"normwise_rel": max_rel, "max_abs_over_max_ref": elt, "rows_checked": len(rows)}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dist": w.dist, "seed": w.seed,
+                   "path": plan["path"], "split_k": plan["split_k"], "grid": plan["grid"],
+                   "tile": [plan["block_m"], plan["block_n"], plan["block_k"]],
+                   "l2": "inputs larger than L2 (A+B = %d MiB, pre-pass copies %d MiB)"
+                         % (4 * (w.M * w.K + w.K * w.N) >> 20, plan["workspace_bytes"] >> 20),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": bound, "achieved": math_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": math_tflops / peak, "traffic": traffic, "peak_source": peak_note,
+                     "kernel": kernel_tag, "kernel_ms": main_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": w.flop / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 4 * w.M * w.N,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": plan["launches"] * args.steps,
+        "max_rel_error": max_rel,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * tg_sgemm.h -- C ABI of the GB300 (sm_103a) row-major FP32 matrix product.
+ *
+ * The operation is C = A x B:
+ *
+ *     C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j],   0 <= i < M, 0 <= j < N
+ *
+ * as defined in "03 CUDA Shared Memory: Tiling, Bank Conflicts, and
+ * Reduction" (section "Shared Memory와 Tiling": one row of A times one column
+ * of B, two FLOP per k) and in the PMPP ch. 5 notes ("메모리 계층과 데이터
+ * 지역성", §5.4 tiled kernel, §5.5 ghost elements: out-of-range tile entries
+ * are zeros, only the final store is range-checked).  The pages show square
+ * matrices; this library takes any M, N, K >= 0 with row strides.
+ *
+ * Layout: every matrix is row-major with a leading dimension (row stride, in
+ * elements): A[i*lda + k], B[k*ldb + j], C[i*ldc + j] (row-major linear index
+ * r*W + c, "PMPP 단권화" ch. 3).  Requirements: lda >= max(1,K),
+ * ldb >= max(1,N), ldc >= max(1,N).  No alignment is required of the
+ * pointers or strides.  C is overwritten (there is no alpha/beta); columns
+ * j >= N of a padded C row are never written.  K == 0 writes +0.0 to the
+ * whole M x N block of C.  C must not overlap A or B.
+ *
+ * Pointers are device pointers of the current CUDA device (except for
+ * tg_sgemm_host).  The caller owns A, B, C and any workspace; the library
+ * never frees or keeps them.
+ *
+ * Execution follows the CUDA host-program pattern of "PMPP 단권화" ch. 2
+ * (caller-owned buffers, cudaError_t-style return codes, streams): calls only
+ * enqueue work on `stream` and return without synchronising the host.  Errors
+ * found before launch (bad arguments, unsupported device, launch failure) are
+ * returned at once.  A kernel that gives up a bounded wait records a timeout
+ * in a per-device error word instead of trapping; tg_sgemm_sync_status
+ * reports it.
+ *
+ * Only GB300-class devices (compute capability 10.3) are supported; there is
+ * no CPU fallback and no other backend.
+ */
+#ifndef TG_SGEMM_H
+#define TG_SGEMM_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum tg_status {
+    TG_OK = 0,
+    TG_ERR_INVALID_VALUE = 1,      /* bad size, stride, null or overlapping pointer, bad option */
+    TG_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+    TG_ERR_OUT_OF_MEMORY = 3,      /* workspace allocation failed */
+    TG_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed (sticky errors stay set) */
+    TG_ERR_TIMEOUT = 5,            /* a kernel gave up a bounded wait (reported by tg_sgemm_sync_status) */
+    TG_ERR_WORKSPACE_TOO_SMALL = 6 /* caller workspace smaller than tg_sgemm_plan's workspace_bytes */
+} tg_status;
+
+/* Math paths.  Both are hand-written sm_103a kernels fed by TMA through an
+ * mbarrier pipeline with warp-specialised producer and consumer warps.
+ *  - TG_PATH_TF32X3: tensor cores (tcgen05.mma kind::tf32, accumulator in
+ *    tensor memory).  Each float is split into hi = tf32(x) and
+ *    lo = tf32(x - hi); the product is lo*hi + hi*lo + hi*hi.  A pre-pass
+ *    writes hi/lo copies of A and of B transposed.
+ *  - TG_PATH_FFMA: register-blocked fused multiply-add on the CUDA cores, fp32
+ *    throughout.
+ *  - TG_PATH_AUTO: TG_PATH_TF32X3. */
+typedef enum tg_path { TG_PATH_AUTO = 0, TG_PATH_FFMA = 1, TG_PATH_TF32X3 = 2 } tg_path;
+
+/* Options for tg_sgemm_ex.  Zero-initialise and set what you need.
+ *  path            tg_path value.
+ *  split_k         0 = automatic; S >= 1 = split K into S slices whose fp32
+ *                  partial products are summed in fixed slice order by a
+ *                  reduce kernel (deterministic: no float atomics).  S is
+ *                  capped at the number of K blocks.
+ *  workspace       optional device buffer of at least workspace_bytes (as
+ *                  reported by tg_sgemm_plan), 256-byte aligned.  NULL = the
+ *                  library allocates it stream-ordered on `stream` from its
+ *                  own per-device memory pool and frees it stream-ordered.
+ *  main_begin/end  optional events, recorded on `stream` immediately before
+ *                  and after the main GEMM kernel (for timing it alone). */
+typedef struct tg_sgemm_opts {
+    int path;
+    int split_k;
+    void* workspace;
+    size_t workspace_bytes;
+    cudaEvent_t main_begin;
+    cudaEvent_t main_end;
+} tg_sgemm_opts;
+
+/* What one call would launch (filled by tg_sgemm_plan). */
+typedef struct tg_plan_info {
+    int path;          /* TG_PATH_FFMA or TG_PATH_TF32X3 */
+    int split_k;       /* K slices */
+    int block_m, block_n, block_k, stages; /* CTA tile and pipeline depth */
+    int tiles_m, tiles_n;
+    long long units;   /* tiles x split_k work units */
+    int grid;          /* persistent CTAs launched (<= SM count) */
+    int prepass;       /* 1 = an operand re-layout kernel runs first */
+    int launches;      /* kernels one call launches */
+    size_t workspace_bytes;
+} tg_plan_info;
+
+/* C = A x B with automatic path and split choice (see the file comment for
+ * layout, ownership and errors).  Returns TG_OK, TG_ERR_INVALID_VALUE,
+ * TG_ERR_UNSUPPORTED_DEVICE, TG_ERR_OUT_OF_MEMORY or TG_ERR_CUDA. */
+tg_status tg_sgemm(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                   float* C, int ldc, cudaStream_t stream);
+
+/* tg_sgemm with options (opts may be NULL = defaults).  Additionally returns
+ * TG_ERR_WORKSPACE_TOO_SMALL. */
+tg_status tg_sgemm_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                      float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts);
+
+/* Plan a call without launching anything: host arithmetic only.  Pointers
+ * may be NULL (then the most conservative alignment is assumed).  num_sms is
+ * the SM count to plan for; 0 = query the current device.  path/split_k as in
+ * tg_sgemm_opts.  Returns TG_OK or TG_ERR_INVALID_VALUE (bad sizes, strides,
+ * path, split_k < 0, out == NULL). */
+tg_status tg_sgemm_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
+                        const void* C, int ldc, int path, int split_k, int num_sms,
+                        tg_plan_info* out);
+
+/* Workspace bytes tg_sgemm_ex needs for these arguments on the current
+ * device (0 on invalid arguments).  Same as tg_sgemm_plan(...).workspace_bytes. */
+size_t tg_sgemm_workspace_bytes(int M, int N, int K, const void* A, int lda, const void* B,
+                                int ldb, const void* C, int ldc, int path, int split_k);
+
+/* Host-buffer convenience call: A, B and C are HOST pointers (pinned memory
+ * gives asynchronous copies).  Copies A and B to device memory allocated
+ * stream-ordered on `stream`, computes C = A x B there, copies C back and
+ * synchronises `stream` before returning, so C is ready on return.  Also
+ * returns TG_ERR_TIMEOUT if a kernel of this call gave up a wait. */
+tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                        float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts);
+
+/* Synchronise `stream`, then read and clear the current device's error word.
+ * Returns TG_ERR_TIMEOUT if any kernel of this library on this device gave up
+ * a bounded wait since the last check (the word is shared by all streams),
+ * TG_ERR_CUDA if the synchronisation failed, else TG_OK. */
+tg_status tg_sgemm_sync_status(cudaStream_t stream);
+
+/* Raw value of the current device's error word (0 = none; otherwise a site
+ * code of the wait that gave up) without clearing it.  Synchronises `stream`. */
+unsigned int tg_sgemm_error_site(cudaStream_t stream);
+
+/* Self-test of the bounded wait: launches one tiny kernel that waits on an
+ * mbarrier nothing will ever arrive on, with a limit of timeout_us
+ * microseconds (1..10,000,000).  The kernel records a timeout in the error
+ * word and returns; the context stays usable.  Returns the launch status;
+ * the caller then expects tg_sgemm_sync_status == TG_ERR_TIMEOUT. */
+tg_status tg_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* tg_status_string(tg_status status);
+
+/* Library ABI version (major*100 + minor). */
+int tg_sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_SGEMM_H */

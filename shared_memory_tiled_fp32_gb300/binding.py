@@ -1,0 +1,236 @@
+"""ctypes binding of libtg_sgemm.so (the C ABI in include/tg_sgemm.h).
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels.  There is no fallback of any kind; if the library is missing the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtg_sgemm.so")
+
+TG_OK = 0
+STATUS = {
+    0: "TG_OK",
+    1: "TG_ERR_INVALID_VALUE",
+    2: "TG_ERR_UNSUPPORTED_DEVICE",
+    3: "TG_ERR_OUT_OF_MEMORY",
+    4: "TG_ERR_CUDA",
+    5: "TG_ERR_TIMEOUT",
+    6: "TG_ERR_WORKSPACE_TOO_SMALL",
+}
+PATHS = {"auto": 0, "ffma": 1, "tf32x3": 2}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+
+# Every symbol include/tg_sgemm.h declares.
+EXPORTS = (
+    "tg_sgemm",
+    "tg_sgemm_ex",
+    "tg_sgemm_plan",
+    "tg_sgemm_workspace_bytes",
+    "tg_sgemm_host",
+    "tg_sgemm_sync_status",
+    "tg_sgemm_error_site",
+    "tg_selftest_wait_timeout",
+    "tg_status_string",
+    "tg_sgemm_version",
+)
+
+
+class TgError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int),
+        ("split_k", ctypes.c_int),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("main_begin", ctypes.c_void_p),
+        ("main_end", ctypes.c_void_p),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int),
+        ("split_k", ctypes.c_int),
+        ("block_m", ctypes.c_int),
+        ("block_n", ctypes.c_int),
+        ("block_k", ctypes.c_int),
+        ("stages", ctypes.c_int),
+        ("tiles_m", ctypes.c_int),
+        ("tiles_n", ctypes.c_int),
+        ("units", ctypes.c_longlong),
+        ("grid", ctypes.c_int),
+        ("prepass", ctypes.c_int),
+        ("launches", ctypes.c_int),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["path"] = PATH_NAMES.get(d["path"], d["path"])
+        return d
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing; build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+            )
+        L = ctypes.CDLL(LIB_PATH)
+        i, p, vp = ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+        gemm = [i, i, i, p, i, p, i, p, i, vp]
+        L.tg_sgemm.argtypes = gemm
+        L.tg_sgemm.restype = i
+        L.tg_sgemm_ex.argtypes = gemm + [ctypes.POINTER(Opts)]
+        L.tg_sgemm_ex.restype = i
+        L.tg_sgemm_host.argtypes = gemm + [ctypes.POINTER(Opts)]
+        L.tg_sgemm_host.restype = i
+        L.tg_sgemm_plan.argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
+        L.tg_sgemm_plan.restype = i
+        L.tg_sgemm_workspace_bytes.argtypes = [i, i, i, p, i, p, i, p, i, i, i]
+        L.tg_sgemm_workspace_bytes.restype = ctypes.c_size_t
+        L.tg_sgemm_sync_status.argtypes = [vp]
+        L.tg_sgemm_sync_status.restype = i
+        L.tg_sgemm_error_site.argtypes = [vp]
+        L.tg_sgemm_error_site.restype = ctypes.c_uint
+        L.tg_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        L.tg_selftest_wait_timeout.restype = i
+        L.tg_status_string.argtypes = [i]
+        L.tg_status_string.restype = ctypes.c_char_p
+        L.tg_sgemm_version.argtypes = []
+        L.tg_sgemm_version.restype = i
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != TG_OK:
+        raise TgError(status, what)
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _event_handle(ev):
+    if ev is None:
+        return None
+    h = getattr(ev, "cuda_event", 0)
+    if not h:
+        raise ValueError("pass torch.cuda.Event objects that have been recorded once (created)")
+    return h
+
+
+def _rowmajor_ld(t, name):
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    return max(t.stride(0) if t.shape[0] > 1 else t.shape[1], t.shape[1], 1)
+
+
+def make_opts(path="auto", split_k=0, workspace=None, main_begin=None, main_end=None) -> Opts:
+    o = Opts()
+    o.path = PATHS[path] if isinstance(path, str) else int(path)
+    o.split_k = int(split_k)
+    if workspace is not None:
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    o.main_begin = _event_handle(main_begin)
+    o.main_end = _event_handle(main_end)
+    return o
+
+
+def matmul(A, B, out=None, *, path="auto", split_k=0, workspace=None, main_begin=None,
+           main_end=None, stream=None):
+    """C = A @ B for float32 CUDA tensors (row-major, any row stride).
+
+    Enqueues on ``stream`` (default: the current stream) and returns ``out``.
+    """
+    import torch
+
+    for name, t in (("A", A), ("B", B)):
+        if t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a float32 CUDA tensor")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} x {tuple(B.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32 or not out.is_cuda or tuple(out.shape) != (M, N):
+        raise ValueError("out must be an (M, N) float32 CUDA tensor")
+    lda, ldb, ldc = _rowmajor_ld(A, "A"), _rowmajor_ld(B, "B"), _rowmajor_ld(out, "out")
+    o = make_opts(path, split_k, workspace, main_begin, main_end)
+    with torch.cuda.device(A.device):
+        st = lib().tg_sgemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                               _stream_handle(stream), ctypes.byref(o))
+    _check(st, "tg_sgemm_ex")
+    return out
+
+
+def sgemm_host(A, B, out, *, path="auto", split_k=0, stream=None):
+    """C = A @ B for float32 CPU tensors (pinned memory for async copies).
+
+    Copies in, computes on the current device, copies out and synchronises.
+    """
+    import torch
+
+    M, K = A.shape
+    _, N = B.shape
+    lda, ldb, ldc = _rowmajor_ld(A, "A"), _rowmajor_ld(B, "B"), _rowmajor_ld(out, "out")
+    o = make_opts(path, split_k)
+    st = lib().tg_sgemm_host(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                             _stream_handle(stream), ctypes.byref(o))
+    _check(st, "tg_sgemm_host")
+    return out
+
+
+def plan(M, N, K, lda=None, ldb=None, ldc=None, *, A=0, B=0, C=0, path="auto", split_k=0,
+         num_sms=0) -> dict:
+    """What one call would launch (host arithmetic; num_sms=0 queries the device)."""
+    info = PlanInfo()
+    lda = max(K, 1) if lda is None else lda
+    ldb = max(N, 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
+    st = lib().tg_sgemm_plan(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
+                             PATHS[path] if isinstance(path, str) else int(path), split_k, num_sms,
+                             ctypes.byref(info))
+    _check(st, "tg_sgemm_plan")
+    return info.as_dict()
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise and return (then clear) the device error status code."""
+    return int(lib().tg_sgemm_sync_status(_stream_handle(stream)))
+
+
+def error_site(stream=None) -> int:
+    return int(lib().tg_sgemm_error_site(_stream_handle(stream)))
+
+
+def selftest_wait_timeout(timeout_us: int, stream=None) -> int:
+    return int(lib().tg_selftest_wait_timeout(timeout_us, _stream_handle(stream)))
+
+
+def status_string(status: int) -> str:
+    return lib().tg_status_string(status).decode()

@@ -1,0 +1,67 @@
+// Internal declarations shared by the host planner, the C-ABI entry points
+// and the kernel launchers.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/tg_sgemm.h"
+
+namespace tg {
+
+// CTA tile shapes of the two math paths.
+//
+// TF32x3: a 128 x 256 output tile per CTA (tcgen05 M=128, N=256 accumulator,
+// 256 of the 512 tensor-memory columns, so two tiles are in flight), K staged
+// 16 floats (64 bytes, one 64-byte swizzle row) at a time, 4 stages of
+// 48 KiB.
+constexpr int kTf32BM = 128, kTf32BN = 256, kTf32BK = 16, kTf32Stages = 4;
+// FFMA: a 128 x 256 output tile, 256 math threads each holding an 8 x 16
+// register block, K staged 32 floats at a time, 4 stages of 48 KiB.
+constexpr int kFfmaBM = 128, kFfmaBN = 256, kFfmaBK = 32, kFfmaStages = 4;
+
+constexpr size_t kWsAlign = 256;
+
+struct Plan {
+    int M = 0, N = 0, K = 0;
+    long long lda = 0, ldb = 0, ldc = 0;
+    int path = TG_PATH_TF32X3;
+    int split = 1;
+    int bm = 0, bn = 0, bk = 0, stages = 0;
+    int tiles_m = 0, tiles_n = 0;
+    long long units = 0;
+    int grid = 0;
+    int nkb = 0;         // K blocks of bk
+    int k4 = 0, n4 = 0;  // K and N rounded up to a multiple of 4 (16-byte rows)
+    bool zero_fill = false;  // K == 0: C = 0, nothing else runs
+    bool pack_a = false, pack_b = false;  // FFMA: copy an operand to a 16-byte-pitched buffer
+    bool vec_c = false;  // C rows start on 16-byte boundaries
+    // workspace layout (byte offsets; a region absent from the plan has size 0)
+    size_t off_a0 = 0, off_a1 = 0, off_b0 = 0, off_b1 = 0, off_part = 0;
+    long long ldp = 0;           // partial-product row stride (elements)
+    long long part_stride = 0;   // elements between two K-slice partials
+    size_t ws_bytes = 0;
+    int launches = 0;
+};
+
+// Argument checks of the C ABI (pure host arithmetic).  With need_pointers
+// false (planning only) NULL pointers are accepted and skip the overlap check.
+tg_status validate(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
+                   const void* C, int ldc, int path, int split_k, bool need_pointers = true);
+
+// Fill `p` for the given call; num_sms > 0.  Assumes validate() passed.
+void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
+               const void* C, int ldc, int path, int split_k, int num_sms, Plan* p);
+
+// Enqueue every kernel of plan `p` on `stream` (defined in tg_kernels.cu).
+tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, void* ws,
+                      cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end);
+
+// Device-side error word (defined in tg_kernels.cu).
+tg_status read_error_word(cudaStream_t stream, bool clear, unsigned int* value);
+tg_status launch_wait_selftest(unsigned int timeout_us, cudaStream_t stream);
+
+// One-time per-device set-up of kernel attributes (tg_kernels.cu).
+tg_status prepare_device_kernels();
+
+}  // namespace tg

@@ -1,0 +1,809 @@
+// sm_103a kernels of the row-major FP32 GEMM C = A x B and their launchers.
+//
+// The method is the pages' shared-memory tiling ("03 CUDA Shared Memory:
+// Tiling, Bank Conflicts, and Reduction", "Shared Memory와 Tiling"; PMPP ch. 5
+// notes §5.3-§5.5), rebuilt for Blackwell:
+//  * a CTA owns one output tile and walks K in phases; the tiles of A and B of
+//    a phase are staged in shared memory by TMA instead of by the threads;
+//  * out-of-range parts of a tile are the pages' ghost elements: TMA fills
+//    them with zeros, and only the final store is range-checked;
+//  * the pages' two __syncthreads() per phase (one so the tile is complete
+//    before it is read, one so nobody overwrites a tile still being read)
+//    become two mbarriers per pipeline stage, "full" and "empty", so several
+//    phases are in flight at once;
+//  * the loading threads are one producer warp; the math warps never load
+//    from global memory (warp-uniform role split by warp index, as in the
+//    pages' divergence-free branching by warp number).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "tg_internal.h"
+#include "tg_ptx.cuh"
+
+namespace tg {
+
+// Per-device error word: 0, or the site code of the first bounded wait that
+// gave up.  Shared by every kernel and stream of this library on the device.
+__device__ unsigned int g_error_word;
+
+enum : uint32_t {
+    kSiteFfmaProducer = 0x101,
+    kSiteFfmaConsumer = 0x102,
+    kSiteTfProducer = 0x201,
+    kSiteTfMmaSmem = 0x202,
+    kSiteTfMmaTmem = 0x203,
+    kSiteTfEpilogue = 0x204,
+    kSiteSelftest = 0x301,
+};
+
+// ------------------------------------------------------------ shared bits
+
+struct GemmArgs {
+    int M, N, K;
+    int tiles_m, tiles_n;
+    int split, nkb;
+    long long units;
+    float* out;              // C (split == 1) or the first K-slice partial
+    long long ldo;           // row stride of `out`
+    long long slice_stride;  // elements between K-slice partials
+    int vec_out;             // rows of `out` start on 16-byte boundaries
+    uint64_t timeout_ns;
+};
+
+struct Unit {
+    int m0, n0, kb0, kb1;
+    float* out;
+};
+
+// Work unit u -> (K slice, output tile).  Tiles are visited in groups of
+// kGroupM tile rows, column by column inside a group, so CTAs running at the
+// same time share A rows and B columns in L2.
+constexpr int kGroupM = 8;
+
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int BM, int BN) {
+    const long long tiles = (long long)a.tiles_m * a.tiles_n;
+    const int s = (int)(u / tiles);
+    const int t = (int)(u - (long long)s * tiles);
+    const int per_group = kGroupM * a.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * kGroupM;
+    const int gm = min(a.tiles_m - first_m, kGroupM);
+    const int r = t - g * per_group;
+    Unit x;
+    x.m0 = (first_m + r % gm) * BM;
+    x.n0 = (r / gm) * BN;
+    x.kb0 = (int)((long long)s * a.nkb / a.split);
+    x.kb1 = (int)((long long)(s + 1) * a.nkb / a.split);
+    x.out = a.out + (long long)s * a.slice_stride;
+    return x;
+}
+
+// Store 4 consecutive values of one output row starting at column `col`,
+// range-checked against N (the pages' guarded final store).
+__device__ __forceinline__ void store_row4(float* row, int col, int N, float4 v, bool vec) {
+    if (vec && col + 3 < N) {
+        *reinterpret_cast<float4*>(row + col) = v;
+    } else {
+        if (col < N) row[col] = v.x;
+        if (col + 1 < N) row[col + 1] = v.y;
+        if (col + 2 < N) row[col + 2] = v.z;
+        if (col + 3 < N) row[col + 3] = v.w;
+    }
+}
+
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {
+    const uint32_t a = smem_addr(raw);
+    return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// ---------------------------------------------------------------- FFMA path
+//
+// CTA tile 128 x 256, K phase 32, 384 threads = 3 warpgroups.  Warpgroup 0
+// is the producer (one thread issues the TMA loads); warpgroups 1-2 (math
+// warps 0-7) do the math.  Each math thread keeps an 8 x 16 block of C in registers
+// (register tiling: "Occupancy와 Block 크기" and PMPP ch. 6 coarsening): per
+// k it reads 8 values of A and 16 of B from shared memory and issues 128 FMAs.
+//
+// Shared-memory layouts and banks ("Bank Conflict" section):
+//  * A tile [128 rows][32 k] arrives with the 128-byte TMA swizzle: the 16-byte
+//    chunk c of row r sits at chunk position c ^ (r % 8) -- the pages' XOR
+//    swizzle applied to 16-byte words.  A thread's 8 rows are r0 + 4i, so the
+//    4 lanes of a warp that read different rows in one instruction read 4
+//    consecutive rows -> 4 different chunk positions -> no bank conflict.
+//    Lanes sharing a row read the same address (broadcast).
+//  * B tile [32 k][256 columns], no swizzle: 8 lanes read 8 consecutive
+//    16-byte words of one row (conflict-free), the other lanes broadcast.
+
+// Register budget: launched at kFfmaLaunchRegs per thread (the most 384
+// threads may have), the producer warpgroup drops to kFfmaProducerRegs and the
+// math warpgroups rise to kFfmaMathRegs; the pool balances exactly:
+// 4*32*40 + 8*32*232 = 384*168.  The host refuses to launch a build whose
+// register count differs, since an unbalanced raise would wait for ever.
+constexpr int kFfmaThreads = 384;
+constexpr int kFfmaLaunchRegs = 168, kFfmaProducerRegs = 40, kFfmaMathRegs = 232;
+static_assert(4 * 32 * kFfmaProducerRegs + 8 * 32 * kFfmaMathRegs == kFfmaThreads * kFfmaLaunchRegs,
+              "setmaxnreg split must balance the launch allocation");
+constexpr uint32_t kFfmaAStage = kFfmaBM * kFfmaBK * 4;  // 16 KiB
+constexpr uint32_t kFfmaBStage = kFfmaBK * kFfmaBN * 4;  // 32 KiB
+constexpr uint32_t kFfmaStageBytes = kFfmaAStage + kFfmaBStage;
+constexpr size_t kFfmaSmemBytes = 1024 + (size_t)kFfmaStages * kFfmaStageBytes + 2 * kFfmaStages * 8;
+
+__device__ __forceinline__ float lanef(const float4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+__global__ void __launch_bounds__(kFfmaThreads, 1)
+    ffma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     GemmArgs args) {
+    constexpr int BM = kFfmaBM, BN = kFfmaBN, BK = kFfmaBK, ST = kFfmaStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_smem_1024(smem_raw);
+    float* sA = reinterpret_cast<float*>(smem);
+    float* sB = reinterpret_cast<float*>(smem + ST * kFfmaAStage);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * kFfmaStageBytes);
+    uint64_t* empty = full + ST;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitCtl wc{&g_error_word, args.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 8);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp < 4) {  // ---------------------------------------- producer
+        regs_dec<kFfmaProducerRegs>();
+        if (warp == 0 && lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+                const Unit t = decode_unit(args, u, BM, BN);
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteFfmaProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], kFfmaStageBytes);
+                    tma_load_2d(sA + stage * BM * BK, &tmA, &full[stage], kb * BK, t.m0);
+                    tma_load_2d(sB + stage * BK * BN, &tmB, &full[stage], t.n0, kb * BK);
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == ST) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every copy issued must land before the CTA may exit
+            for (int s = 0; s < ST; ++s)
+                if ((issued >> s) & 1u) mbar_drain(&full[s], (last_par >> s) & 1u, args.timeout_ns);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------- math
+    regs_inc<kFfmaMathRegs>();
+    const int mw = warp - 4;                  // math warp 0..7
+    const int wm = mw & 3, wn = mw >> 2;      // warp tile: rows 32*wm.., columns 128*wn..
+    const int lm = lane & 3, ln = lane >> 2;  // thread rows wm*32 + lm + 4i, columns 32j + 4ln + q
+    int stage = 0;
+    uint32_t phase = 0;
+    for (long long u = blockIdx.x; u < args.units; u += gridDim.x) {
+        const Unit t = decode_unit(args, u, BM, BN);
+        float acc[8][16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
+
+        bool ok = true;
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+            const bool got = mbar_wait(&full[stage], phase, wc, kSiteFfmaConsumer);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            const float* a = sA + stage * BM * BK;
+            const float* b = sB + stage * BK * BN + wn * 128 + 4 * ln;
+#pragma unroll 1
+            for (int kk = 0; kk < BK; kk += 4) {
+                float4 av[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = wm * 32 + lm + 4 * i;
+                    const int chunk = (kk >> 2) ^ (r & 7);
+                    av[i] = *reinterpret_cast<const float4*>(a + r * BK + chunk * 4);
+                }
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    float4 bv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        bv[j] = *reinterpret_cast<const float4*>(b + (kk + k4) * BN + 32 * j);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float x = lanef(av[i], k4);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc[i][4 * j + 0] = fmaf(x, bv[j].x, acc[i][4 * j + 0]);
+                            acc[i][4 * j + 1] = fmaf(x, bv[j].y, acc[i][4 * j + 1]);
+                            acc[i][4 * j + 2] = fmaf(x, bv[j].z, acc[i][4 * j + 2]);
+                            acc[i][4 * j + 3] = fmaf(x, bv[j].w, acc[i][4 * j + 3]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == ST) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+
+        // guarded store: 4 rows x 128 contiguous bytes per warp instruction
+        const bool vec = args.vec_out != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = t.m0 + wm * 32 + lm + 4 * i;
+            if (r < args.M) {
+                float* row = t.out + (long long)r * args.ldo;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = t.n0 + wn * 128 + 32 * j + 4 * ln;
+                    store_row4(row, c, args.N,
+                               make_float4(acc[i][4 * j], acc[i][4 * j + 1], acc[i][4 * j + 2],
+                                           acc[i][4 * j + 3]),
+                               vec);
+                }
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------------- 3xTF32 path
+//
+// Operands come from the split pre-pass: A_hi, A_lo as [M][k4] and B_hi, B_lo
+// as B transposed, [N][k4] -- both K-major, so every tile row is 16 values of
+// K (64 bytes) and TMA writes it with the 64-byte swizzle the tensor core's
+// K-major layout expects.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
+// owner and MMA issuer (one thread), warps 2-5 = epilogue.  The accumulator
+// is a 128 x 256 fp32 tile in tensor memory (lane = row, column = column);
+// two of them (512 columns) let the epilogue of one tile overlap the MMAs of
+// the next.  Per 8-wide K slice the MMA thread issues
+//     D += A_lo B_hi;  D += A_hi B_lo;  D += A_hi B_hi
+// (the small terms first; A_lo B_lo, of relative size 2^-22, is dropped).
+
+constexpr int kTfThreads = 192;
+constexpr uint32_t kTfAStage = kTf32BM * kTf32BK * 4;              // 8 KiB
+constexpr uint32_t kTfBStage = kTf32BN * kTf32BK * 4;              // 16 KiB
+constexpr uint32_t kTfStageBytes = 2 * (kTfAStage + kTfBStage);     // 48 KiB
+constexpr int kEpiPitch = 36;  // floats per staged row: 16-byte aligned, conflict-free
+constexpr uint32_t kTfEpiBytes = 4 * 32 * kEpiPitch * 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSw64RowGroupBytes = 8 * 64;  // 8 rows of one 64-byte swizzle row
+constexpr uint32_t kDescSwizzle64 = 4;
+constexpr int kTfBars = 2 * kTf32Stages + 5;
+constexpr size_t kTfSmemBytes =
+    1024 + (size_t)kTf32Stages * kTfStageBytes + kTfEpiBytes + kTfBars * 8 + 16;
+
+__global__ void __launch_bounds__(kTfThreads, 1)
+    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi,
+                       const __grid_constant__ CUtensorMap tmAlo,
+                       const __grid_constant__ CUtensorMap tmBhi,
+                       const __grid_constant__ CUtensorMap tmBlo, GemmArgs args) {
+    constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK, ST = kTf32Stages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_smem_1024(smem_raw);
+    float* epi = reinterpret_cast<float*>(smem + ST * kTfStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * kTfStageBytes + kTfEpiBytes);
+    uint64_t* empty = full + ST;
+    uint64_t* tfull = empty + ST;  // [2] accumulator ready
+    uint64_t* tempty = tfull + 2;  // [2] accumulator drained by the epilogue
+    uint64_t* drain = tempty + 2;  // every MMA of this CTA completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitCtl wc{&g_error_word, args.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {  // ---------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmAhi);
+            tma_prefetch_desc(&tmAlo);
+            tma_prefetch_desc(&tmBhi);
+            tma_prefetch_desc(&tmBlo);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+                const Unit t = decode_unit(args, u, BM, BN);
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteTfProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * kTfStageBytes;
+                    mbar_arrive_expect_tx(&full[stage], kTfStageBytes);
+                    tma_load_2d(st, &tmAhi, &full[stage], kb * BK, t.m0);
+                    tma_load_2d(st + kTfAStage, &tmAlo, &full[stage], kb * BK, t.m0);
+                    tma_load_2d(st + 2 * kTfAStage, &tmBhi, &full[stage], kb * BK, t.n0);
+                    tma_load_2d(st + 2 * kTfAStage + kTfBStage, &tmBlo, &full[stage], kb * BK, t.n0);
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == ST) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < ST; ++s)
+                if ((issued >> s) & 1u) mbar_drain(&full[s], (last_par >> s) & 1u, args.timeout_ns);
+        }
+    } else if (warp == 1) {  // --------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_tf32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0, iter = 0;
+            bool ok = true;
+            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x, ++iter) {
+                const Unit t = decode_unit(args, u, BM, BN);
+                const uint32_t buf = iter & 1u, par = (iter >> 1) & 1u;
+                if (!mbar_wait(&tempty[buf], par ^ 1u, wc, kSiteTfMmaTmem)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, wc, kSiteTfMmaSmem)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_hi = smem_addr(smem + stage * kTfStageBytes);
+                    const uint32_t a_lo = a_hi + kTfAStage;
+                    const uint32_t b_hi = a_hi + 2 * kTfAStage;
+                    const uint32_t b_lo = b_hi + kTfBStage;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 8; ++ks) {
+                        const uint32_t ko = ks * 32;  // 8 tf32 values along K
+                        const uint64_t dahi = smem_desc_kmajor(a_hi + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                        const uint64_t dalo = smem_desc_kmajor(a_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                        const uint64_t dbhi = smem_desc_kmajor(b_hi + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                        const uint64_t dblo = smem_desc_kmajor(b_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                        mma_tf32_ss(d_tmem, dalo, dbhi, idesc, (kb > t.kb0 || ks > 0) ? 1u : 0u);
+                        mma_tf32_ss(d_tmem, dahi, dblo, idesc, 1u);
+                        mma_tf32_ss(d_tmem, dahi, dbhi, idesc, 1u);
+                    }
+                    mma_commit(&empty[stage]);  // frees the stage once these MMAs are done
+                    if (++stage == ST) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[buf]);
+            }
+            // no tensor-memory access may be in flight when the CTA frees it
+            mma_commit(drain);
+            mbar_drain(drain, 0, args.timeout_ns);
+        }
+    } else {  // ---------------------------------------------------- epilogue
+        const int q = warp & 3;  // this warp may access tensor-memory lanes 32q..32q+31
+        float* stg = epi + (warp - 2) * 32 * kEpiPitch;
+        const bool vec = args.vec_out != 0;
+        uint32_t iter = 0;
+        for (long long u = blockIdx.x; u < args.units; u += gridDim.x, ++iter) {
+            const Unit t = decode_unit(args, u, BM, BN);
+            const uint32_t buf = iter & 1u, par = (iter >> 1) & 1u;
+            const bool got = mbar_wait(&tfull[buf], par, wc, kSiteTfEpilogue);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after_sync();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+            const int row0 = t.m0 + q * 32;
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, r);
+                tmem_ld_wait(r);
+                if (c == BN / 32 - 1) {  // accumulator fully read: hand it back
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[buf]);
+                }
+                // lane i holds row row0+i, columns c*32..c*32+31; transpose
+                // through shared memory so each store covers whole row segments
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    *reinterpret_cast<float4*>(stg + lane * kEpiPitch + 4 * v) =
+                        make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                __syncwarp();
+                const int col = t.n0 + c * 32 + 4 * (lane & 7);
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int rr = it * 4 + (lane >> 3);
+                    const float4 v = *reinterpret_cast<const float4*>(stg + rr * kEpiPitch + 4 * (lane & 7));
+                    const int grow = row0 + rr;
+                    if (grow < args.M) store_row4(t.out + (long long)grow * args.ldo, col, args.N, v, vec);
+                }
+                __syncwarp();
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------ pre-pass
+//
+// SPLIT (3xTF32):  A -> A_hi, A_lo [M][k4];  B -> B_hi^T, B_lo^T [N][k4]
+//   hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32).
+// PACK (FFMA, operand not TMA-legal): A -> [M][k4], B -> [K][n4].
+// Padding columns (k >= K, n >= N) are written as zeros (ghost elements).
+// Work is cut into 32 x 32 tiles, one per 256-thread block iteration.  B's
+// transpose goes through a [32][33] shared tile: the padded row makes the
+// column read conflict-free ("Bank Conflict", padding: gcd(33, 32) = 1).
+
+struct PrepassArgs {
+    const float* A;
+    long long lda;
+    const float* B;
+    long long ldb;
+    int M, N, K, k4, n4;
+    float* a0;
+    float* a1;
+    float* b0;
+    float* b1;
+    long long a_tiles, b_tiles;
+    int a_tiles_inner, b_tiles_inner;
+};
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(256) prepass_kernel(PrepassArgs p) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const long long total = p.a_tiles + p.b_tiles;
+    for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+        if (t < p.a_tiles) {
+            const int tm = (int)(t / p.a_tiles_inner), tk = (int)(t % p.a_tiles_inner);
+            const int k = tk * 32 + tx;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int m = tm * 32 + ty + 8 * r;
+                if (m < p.M && k < p.k4) {
+                    const float x = (k < p.K) ? p.A[(long long)m * p.lda + k] : 0.0f;
+                    const long long o = (long long)m * p.k4 + k;
+                    if (SPLIT) {
+                        const float hi = to_tf32(x);
+                        p.a0[o] = hi;
+                        p.a1[o] = to_tf32(x - hi);
+                    } else {
+                        p.a0[o] = x;
+                    }
+                }
+            }
+        } else if (SPLIT) {
+            const long long tb = t - p.a_tiles;
+            const int tn = (int)(tb / p.b_tiles_inner), tk = (int)(tb % p.b_tiles_inner);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int k = tk * 32 + ty + 8 * r, n = tn * 32 + tx;
+                tile[ty + 8 * r][tx] = (k < p.K && n < p.N) ? p.B[(long long)k * p.ldb + n] : 0.0f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int n = tn * 32 + ty + 8 * r, k = tk * 32 + tx;
+                if (n < p.N && k < p.k4) {
+                    const float x = tile[tx][ty + 8 * r];
+                    const float hi = to_tf32(x);
+                    const long long o = (long long)n * p.k4 + k;
+                    p.b0[o] = hi;
+                    p.b1[o] = to_tf32(x - hi);
+                }
+            }
+            __syncthreads();
+        } else {
+            const long long tb = t - p.a_tiles;
+            const int tk = (int)(tb / p.b_tiles_inner), tn = (int)(tb % p.b_tiles_inner);
+            const int n = tn * 32 + tx;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int k = tk * 32 + ty + 8 * r;
+                if (k < p.K && n < p.n4)
+                    p.b0[(long long)k * p.n4 + n] = (n < p.N) ? p.B[(long long)k * p.ldb + n] : 0.0f;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------ split-K reduce
+// C = sum_{s=0}^{S-1} partial_s, always in slice order s = 0, 1, ... so the
+// result does not depend on scheduling (float atomics would: "Reduction",
+// the atomicAdd variant).  Memory-bound; float4 loads of the 16-byte-pitched
+// partials.
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ part, long long ldp, long long slice, int S,
+                         float* C, long long ldc, int M, int N, int vec_c) {
+    const int n4g = (N + 3) / 4;
+    const long long total = (long long)M * n4g;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int m = (int)(i / n4g), c = (int)(i % n4g) * 4;
+        const float* p = part + (long long)m * ldp + c;
+        float4 s = *reinterpret_cast<const float4*>(p);
+        for (int t = 1; t < S; ++t) {
+            const float4 v = *reinterpret_cast<const float4*>(p + t * slice);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        store_row4(C + (long long)m * ldc, c, N, s, vec_c != 0);
+    }
+}
+
+// K == 0: the empty sum.
+__global__ void __launch_bounds__(256) fill_zero_kernel(float* C, long long ldc, int M, int N) {
+    const long long total = (long long)M * N;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x)
+        C[(i / N) * ldc + (i % N)] = 0.0f;
+}
+
+// Waits on an mbarrier that nothing arrives on; the bounded wait gives up,
+// records kSiteSelftest and the kernel returns normally.
+__global__ void wait_selftest_kernel(uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtl wc{&g_error_word, timeout_ns};
+        (void)mbar_wait(&bar, 0, wc, kSiteSelftest);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+namespace {
+
+uint64_t default_timeout_ns() {
+    static uint64_t ns = [] {
+        const char* s = std::getenv("TG_WAIT_TIMEOUT_MS");
+        long long ms = s ? std::atoll(s) : 0;
+        if (ms <= 0) ms = 4000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return ns;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D fp32 tensor map: `inner` elements per row (the valid extent; anything
+// beyond reads as zero), `outer` rows, `row_bytes` between rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int elementwise_grid(long long work, int per_block) {
+    long long g = (work + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    if (g > 4096) g = 4096;
+    return (int)g;
+}
+
+tg_status last_launch_status() {
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+}  // namespace
+
+tg_status prepare_device_kernels() {
+    // The FFMA kernel's warpgroup register split is only balanced when it is
+    // launched with exactly kFfmaLaunchRegs registers per thread.
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, ffma_gemm_kernel) != cudaSuccess) return TG_ERR_CUDA;
+    if (fa.numRegs != kFfmaLaunchRegs) return TG_ERR_CUDA;
+    if (cudaFuncSetAttribute(ffma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFfmaSmemBytes) != cudaSuccess)
+        return TG_ERR_CUDA;
+    if (cudaFuncSetAttribute(tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kTfSmemBytes) != cudaSuccess)
+        return TG_ERR_CUDA;
+    return TG_OK;
+}
+
+tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, void* ws,
+                      cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+    if (p.M == 0 || p.N == 0) return TG_OK;
+    if (p.zero_fill) {
+        fill_zero_kernel<<<elementwise_grid((long long)p.M * p.N, 256), 256, 0, stream>>>(C, p.ldc, p.M, p.N);
+        return last_launch_status();
+    }
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    GemmArgs ga{};
+    ga.M = p.M;
+    ga.N = p.N;
+    ga.K = p.K;
+    ga.tiles_m = p.tiles_m;
+    ga.tiles_n = p.tiles_n;
+    ga.split = p.split;
+    ga.nkb = p.nkb;
+    ga.units = p.units;
+    ga.timeout_ns = default_timeout_ns();
+    if (p.split > 1) {
+        ga.out = reinterpret_cast<float*>(w + p.off_part);
+        ga.ldo = p.ldp;
+        ga.slice_stride = p.part_stride;
+        ga.vec_out = 1;
+    } else {
+        ga.out = C;
+        ga.ldo = p.ldc;
+        ga.slice_stride = 0;
+        ga.vec_out = p.vec_c ? 1 : 0;
+    }
+
+    PrepassArgs pa{};
+    pa.A = A;
+    pa.lda = p.lda;
+    pa.B = B;
+    pa.ldb = p.ldb;
+    pa.M = p.M;
+    pa.N = p.N;
+    pa.K = p.K;
+    pa.k4 = p.k4;
+    pa.n4 = p.n4;
+
+    if (p.path == TG_PATH_TF32X3) {
+        float* ahi = reinterpret_cast<float*>(w + p.off_a0);
+        float* alo = reinterpret_cast<float*>(w + p.off_a1);
+        float* bhi = reinterpret_cast<float*>(w + p.off_b0);
+        float* blo = reinterpret_cast<float*>(w + p.off_b1);
+        pa.a0 = ahi;
+        pa.a1 = alo;
+        pa.b0 = bhi;
+        pa.b1 = blo;
+        pa.a_tiles_inner = (p.k4 + 31) / 32;
+        pa.b_tiles_inner = (p.k4 + 31) / 32;
+        pa.a_tiles = (long long)((p.M + 31) / 32) * pa.a_tiles_inner;
+        pa.b_tiles = (long long)((p.N + 31) / 32) * pa.b_tiles_inner;
+        const long long tiles = pa.a_tiles + pa.b_tiles;
+        prepass_kernel<true><<<(int)(tiles < 8192 ? tiles : 8192), 256, 0, stream>>>(pa);
+        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+
+        CUtensorMap mAhi, mAlo, mBhi, mBlo;
+        const uint64_t row = 4ull * p.k4;
+        if (!make_map(&mAhi, ahi, p.K, p.M, row, kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !make_map(&mAlo, alo, p.K, p.M, row, kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !make_map(&mBhi, bhi, p.K, p.N, row, kTf32BK, kTf32BN, CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !make_map(&mBlo, blo, p.K, p.N, row, kTf32BK, kTf32BN, CU_TENSOR_MAP_SWIZZLE_64B))
+            return TG_ERR_CUDA;
+        if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
+        tf32x3_gemm_kernel<<<p.grid, kTfThreads, kTfSmemBytes, stream>>>(mAhi, mAlo, mBhi, mBlo, ga);
+        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+        if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
+    } else {
+        const float* a_src = A;
+        const float* b_src = B;
+        long long a_row = p.lda, b_row = p.ldb;
+        if (p.pack_a || p.pack_b) {
+            pa.a0 = p.pack_a ? reinterpret_cast<float*>(w + p.off_a0) : nullptr;
+            pa.b0 = p.pack_b ? reinterpret_cast<float*>(w + p.off_b0) : nullptr;
+            pa.a_tiles_inner = (p.k4 + 31) / 32;
+            pa.b_tiles_inner = (p.n4 + 31) / 32;
+            pa.a_tiles = p.pack_a ? (long long)((p.M + 31) / 32) * pa.a_tiles_inner : 0;
+            pa.b_tiles = p.pack_b ? (long long)((p.K + 31) / 32) * pa.b_tiles_inner : 0;
+            const long long tiles = pa.a_tiles + pa.b_tiles;
+            prepass_kernel<false><<<(int)(tiles < 8192 ? tiles : 8192), 256, 0, stream>>>(pa);
+            if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+            if (p.pack_a) {
+                a_src = pa.a0;
+                a_row = p.k4;
+            }
+            if (p.pack_b) {
+                b_src = pa.b0;
+                b_row = p.n4;
+            }
+        }
+        CUtensorMap mA, mB;
+        if (!make_map(&mA, a_src, p.K, p.M, 4ull * a_row, kFfmaBK, kFfmaBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&mB, b_src, p.N, p.K, 4ull * b_row, kFfmaBN, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return TG_ERR_CUDA;
+        if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
+        ffma_gemm_kernel<<<p.grid, kFfmaThreads, kFfmaSmemBytes, stream>>>(mA, mB, ga);
+        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+        if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
+    }
+
+    if (p.split > 1) {
+        const long long work = (long long)p.M * ((p.N + 3) / 4);
+        splitk_reduce_kernel<<<elementwise_grid(work, 256), 256, 0, stream>>>(
+            ga.out, p.ldp, p.part_stride, p.split, C, p.ldc, p.M, p.N, p.vec_c ? 1 : 0);
+        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+    }
+    return TG_OK;
+}
+
+tg_status read_error_word(cudaStream_t stream, bool clear, unsigned int* value) {
+    unsigned int v = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return TG_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return TG_ERR_CUDA;
+    if (clear && v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return TG_ERR_CUDA;
+    }
+    *value = v;
+    return TG_OK;
+}
+
+tg_status launch_wait_selftest(unsigned int timeout_us, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>((uint64_t)timeout_us * 1000ull);
+    return last_launch_status();
+}
+
+}  // namespace tg

@@ -1,0 +1,134 @@
+// Host planner of the FP32 GEMM: argument checks, path and tile choice,
+// split-K choice and workspace layout.  Pure host arithmetic; no CUDA calls.
+//
+// The tile decomposition follows the pages' tiling scheme ("03 CUDA Shared
+// Memory: Tiling, Bank Conflicts, and Reduction", section "Shared Memory와
+// Tiling"; PMPP ch. 5 notes §5.3-§5.4): every CTA owns one BM x BN block of C
+// and walks K in phases of BK, with ceil(K/BK) phases and zero-filled ghost
+// elements past the edges (§5.5).  What differs from the pages is the
+// scheduling: CTAs are persistent (one per SM, looping over tiles), because a
+// GB300 SM holds one such CTA at a time (the occupancy trade-off of "Occupancy와
+// Block 크기", taken at its extreme: few warps, each with much work).
+#include <algorithm>
+#include <cstdint>
+
+#include "tg_internal.h"
+
+namespace tg {
+
+namespace {
+
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
+    return a0 < b1 && b0 < a1;
+}
+
+}  // namespace
+
+tg_status validate(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
+                   const void* C, int ldc, int path, int split_k, bool need_pointers) {
+    if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_VALUE;
+    if (lda < std::max(1, K) || ldb < std::max(1, N) || ldc < std::max(1, N))
+        return TG_ERR_INVALID_VALUE;
+    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3)
+        return TG_ERR_INVALID_VALUE;
+    if (split_k < 0) return TG_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return TG_OK;  // nothing is read or written
+    if (!need_pointers && (A == nullptr || B == nullptr || C == nullptr)) return TG_OK;
+    if (C == nullptr) return TG_ERR_INVALID_VALUE;
+    if (K > 0 && (A == nullptr || B == nullptr)) return TG_ERR_INVALID_VALUE;
+    // C must not overlap the operands (checked on the address ranges spanned)
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(C);
+    const uintptr_t c1 = c0 + 4ull * ((unsigned long long)(M - 1) * ldc + N);
+    if (K > 0) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(A);
+        const uintptr_t a1 = a0 + 4ull * ((unsigned long long)(M - 1) * lda + K);
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(B);
+        const uintptr_t b1 = b0 + 4ull * ((unsigned long long)(K - 1) * ldb + N);
+        if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
+            return TG_ERR_INVALID_VALUE;
+    }
+    return TG_OK;
+}
+
+void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
+               const void* C, int ldc, int path, int split_k, int num_sms, Plan* p) {
+    *p = Plan{};
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->lda = lda;
+    p->ldb = ldb;
+    p->ldc = ldc;
+    p->path = (path == TG_PATH_FFMA) ? TG_PATH_FFMA : TG_PATH_TF32X3;
+    p->vec_c = C != nullptr && (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
+    if (p->path == TG_PATH_TF32X3) {
+        p->bm = kTf32BM; p->bn = kTf32BN; p->bk = kTf32BK; p->stages = kTf32Stages;
+    } else {
+        p->bm = kFfmaBM; p->bn = kFfmaBN; p->bk = kFfmaBK; p->stages = kFfmaStages;
+    }
+    p->k4 = (int)round_up((size_t)K, 4);
+    p->n4 = (int)round_up((size_t)N, 4);
+    if (M == 0 || N == 0) {
+        p->launches = 0;
+        return;
+    }
+    if (K == 0) {  // the empty sum: C = +0.0, one fill kernel
+        p->zero_fill = true;
+        p->split = 1;
+        p->launches = 1;
+        return;
+    }
+    p->tiles_m = (int)cdiv(M, p->bm);
+    p->tiles_n = (int)cdiv(N, p->bn);
+    p->nkb = (int)cdiv(K, p->bk);
+    const long long tiles = (long long)p->tiles_m * p->tiles_n;
+
+    // Split K when the tiles alone would leave most SMs idle.  Every slice
+    // keeps at least 4 K blocks, and there are at most 16 slices.
+    int S = 1;
+    if (split_k > 0) {
+        S = std::min(split_k, p->nkb);
+    } else if (tiles < num_sms / 2 && p->nkb >= 8) {
+        long long s = std::min<long long>({(long long)num_sms / tiles, (long long)p->nkb / 4, 16});
+        S = (int)std::max<long long>(1, s);
+    }
+    p->split = S;
+    p->units = tiles * S;
+    p->grid = (int)std::min<long long>(p->units, num_sms);
+
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = round_up(off + bytes, kWsAlign);
+        return at;
+    };
+    if (p->path == TG_PATH_TF32X3) {
+        // hi/lo copies: A as [M][k4], B transposed as [N][k4] (both K-major)
+        const size_t a_bytes = 4ull * M * p->k4, b_bytes = 4ull * N * p->k4;
+        p->off_a0 = take(a_bytes);
+        p->off_a1 = take(a_bytes);
+        p->off_b0 = take(b_bytes);
+        p->off_b1 = take(b_bytes);
+    } else {
+        // TMA reads the operands in place when their base is 16-byte aligned
+        // and their row pitch a multiple of 16 bytes; otherwise a pre-pass
+        // copies them to a padded buffer (A: [M][k4], B: [K][n4]).
+        p->pack_a = A == nullptr || (reinterpret_cast<uintptr_t>(A) % 16 != 0) || (lda % 4 != 0);
+        p->pack_b = B == nullptr || (reinterpret_cast<uintptr_t>(B) % 16 != 0) || (ldb % 4 != 0);
+        if (p->pack_a) p->off_a0 = take(4ull * M * p->k4);
+        if (p->pack_b) p->off_b0 = take(4ull * K * p->n4);
+    }
+    if (S > 1) {
+        p->ldp = p->n4;
+        p->part_stride = (long long)M * p->n4;
+        p->off_part = take(4ull * S * M * p->n4);
+    }
+    p->ws_bytes = off;
+    const bool prepass = p->path == TG_PATH_TF32X3 || p->pack_a || p->pack_b;
+    p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0);
+}
+
+}  // namespace tg

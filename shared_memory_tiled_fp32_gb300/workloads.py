@@ -78,10 +78,16 @@ def workload_inputs(name: str):
     return make_inputs(w.M, w.N, w.K, w.dist, w.seed)
 
 
+def row_order(w: Workload):
+    """A seeded random permutation of the output rows of ``w``."""
+    gen = torch.Generator().manual_seed(w.row_seed if w.row_seed is not None else 1000 + w.seed)
+    return torch.randperm(w.M, generator=gen)
+
+
 def sample_rows(w: Workload, count: int | None = None):
-    """Distinct output rows, uniformly without replacement, seeded."""
+    """``count`` distinct output rows (default: the workload's row sample),
+    uniformly without replacement, seeded, in ascending order."""
     count = w.row_sample if count is None else count
     if count is None or count >= w.M:
         return torch.arange(w.M, dtype=torch.int64)
-    gen = torch.Generator().manual_seed(w.row_seed if w.row_seed is not None else 1000 + w.seed)
-    return torch.randperm(w.M, generator=gen)[:count].sort().values
+    return row_order(w)[:count].sort().values

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol the header declares, rejects bad arguments before touching CUDA,
+and plans tiles, K splits and workspace as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import shared_memory_tiled_fp32_gb300 as tg
+from shared_memory_tiled_fp32_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tg_sgemm.h")
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:unsigned\s+)?[a-z_]+\s*\**\s*(tg_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_header_symbols():
+    L = tg.lib()
+    funcs = header_functions()
+    assert funcs, "no declarations parsed"
+    assert sorted(binding.EXPORTS) == funcs
+    for name in funcs:
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings():
+    assert tg.lib().tg_sgemm_version() == 100
+    for code, name in tg.STATUS.items():
+        assert tg.status_string(code).startswith(name)
+
+
+def _call(M, N, K, A, lda, B, ldb, C, ldc, path=0, split=0):
+    o = binding.Opts()
+    o.path, o.split_k = path, split
+    return tg.lib().tg_sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, None, ctypes.byref(o))
+
+
+def test_argument_errors_need_no_gpu():
+    p = 1 << 20  # never dereferenced: every case below fails validation first
+    bad = [
+        (-1, 4, 4, p, 4, p + 10**6, 4, p + 2 * 10**6, 4),
+        (4, -1, 4, p, 4, p + 10**6, 4, p + 2 * 10**6, 4),
+        (4, 4, -1, p, 4, p + 10**6, 4, p + 2 * 10**6, 4),
+        (4, 4, 8, p, 7, p + 10**6, 4, p + 2 * 10**6, 4),     # lda < K
+        (4, 8, 4, p, 4, p + 10**6, 7, p + 2 * 10**6, 8),     # ldb < N
+        (4, 8, 4, p, 4, p + 10**6, 8, p + 2 * 10**6, 7),     # ldc < N
+        (4, 4, 4, None, 4, p + 10**6, 4, p + 2 * 10**6, 4),  # null A
+        (4, 4, 4, p, 4, None, 4, p + 2 * 10**6, 4),          # null B
+        (4, 4, 4, p, 4, p + 10**6, 4, None, 4),              # null C
+        (4, 4, 4, p, 4, p + 10**6, 4, p + 8, 4),             # C overlaps A
+        (4, 4, 4, p, 4, p + 10**6, 4, p + 10**6 + 60, 4),    # C overlaps B
+    ]
+    for args in bad:
+        assert _call(*args) == 1, args
+    assert _call(4, 4, 4, p, 4, p + 10**6, 4, p + 2 * 10**6, 4, path=7) == 1
+    assert _call(4, 4, 4, p, 4, p + 10**6, 4, p + 2 * 10**6, 4, split=-2) == 1
+    # empty outputs are a valid no-op that never reaches the device
+    assert _call(0, 4, 4, None, 4, None, 4, None, 4) == 0
+    assert _call(4, 0, 4, None, 4, None, 1, None, 1) == 0
+
+
+def test_plan_tiles_split_and_workspace():
+    sms = 152
+    p = tg.plan(8192, 8192, 8192, num_sms=sms)
+    assert (p["path"], p["tiles_m"], p["tiles_n"], p["split_k"]) == ("tf32x3", 64, 32, 1)
+    assert p["grid"] == sms and p["units"] == 2048 and p["launches"] == 2
+    assert p["workspace_bytes"] == 4 * 8192 * 8192 * 4  # A_hi, A_lo, B_hi^T, B_lo^T
+    # ragged: ceil(777/128) x ceil(1029/256) tiles, split to fill the SMs
+    p = tg.plan(777, 1029, 513, num_sms=sms)
+    assert (p["tiles_m"], p["tiles_n"]) == (7, 5)
+    assert p["split_k"] == 4 and p["units"] == 140 and p["launches"] == 3
+    # an explicit split is capped by the K blocks
+    p = tg.plan(64, 64, 32, num_sms=sms, split_k=9)
+    assert p["split_k"] == 2  # ceil(32/16) K blocks
+    # FFMA reads aligned operands in place and packs misaligned ones
+    one = dict(num_sms=sms, path="ffma", split_k=1)
+    a = tg.plan(512, 512, 512, A=4096, B=1 << 20, C=1 << 24, **one)
+    assert a["prepass"] == 0 and a["workspace_bytes"] == 0 and a["launches"] == 1
+    b = tg.plan(512, 512, 512, A=4100, B=1 << 20, C=1 << 24, **one)
+    assert b["prepass"] == 1 and b["workspace_bytes"] == 512 * 512 * 4 and b["launches"] == 2
+    c = tg.plan(512, 513, 512, 512, 513, 513, A=4096, B=1 << 20, C=1 << 24, **one)
+    assert c["prepass"] == 1 and c["workspace_bytes"] == 512 * 516 * 4
+    # few tiles: K is split so the SMs fill, partials add 4 * S * M * roundup(N, 4) bytes
+    d = tg.plan(512, 512, 512, A=4096, B=1 << 20, C=1 << 24, num_sms=sms, path="ffma")
+    assert d["split_k"] == 4 and d["workspace_bytes"] == 4 * 4 * 512 * 512 and d["launches"] == 2
+    # K = 0 is one fill kernel
+    z = tg.plan(10, 10, 0, num_sms=sms)
+    assert z["launches"] == 1 and z["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (300, 7, 5000), (2048, 2048, 16384), (129, 257, 17)])
+def test_plan_split_ranges_cover_k(M, N, K):
+    """Each K slice gets a non-empty, contiguous run of K blocks."""
+    for path in ("tf32x3", "ffma"):
+        p = tg.plan(M, N, K, num_sms=152, path=path)
+        nkb = -(-K // p["block_k"])
+        S = p["split_k"]
+        bounds = [s * nkb // S for s in range(S + 1)]
+        assert bounds[0] == 0 and bounds[-1] == nkb
+        assert all(b1 > b0 for b0, b1 in zip(bounds, bounds[1:]))
