@@ -281,26 +281,41 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 // K (64 bytes) and TMA writes it with the 64-byte swizzle the tensor core's
 // K-major layout expects.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
-// owner and MMA issuer (one thread), warps 2-5 = epilogue.  The accumulator
-// is a 128 x 256 fp32 tile in tensor memory (lane = row, column = column);
-// two of them (512 columns) let the epilogue of one tile overlap the MMAs of
-// the next.  Per 8-wide K slice the MMA thread issues
+// Per 8-wide K slice the MMA thread issues
 //     D += A_lo B_hi;  D += A_hi B_lo;  D += A_hi B_hi
 // (the small terms first; A_lo B_lo, of relative size 2^-22, is dropped).
+//
+// Accumulation precision.  The tensor core's fp32 accumulation loses about
+// one unit in the last place towards zero per MMA instead of rounding to
+// nearest, so an error accumulated over all of K grows linearly with K (about
+// 7e-9 * K relative, measured on this part).  The kernel therefore lets the
+// tensor core accumulate only kTfChunkKB K blocks (256 values of K) into a
+// tensor-memory buffer; the epilogue warps add each finished chunk into an
+// fp32 register accumulator with ordinary round-to-nearest additions, and
+// store the tile after its last chunk.  The remaining error is about
+// 7e-9 * 256 ~ 2e-6 relative, independent of K.
+//
+// Warp roles (384 threads, 3 warpgroups): warp 0 = TMA producer, warp 1 =
+// tensor-memory owner and MMA issuer (one thread), warps 2-3 idle; warps 4-11
+// = epilogue.  Epilogue warp e reads tensor-memory lanes 32*(e%4).. (a warp
+// may only touch the lane quarter of its warp index modulo 4) and columns
+// 128*(e/4)..+127, so each thread owns 128 accumulators of one output row.
+// Two chunk buffers of 256 columns (all 512 tensor-memory columns) let the
+// epilogue drain one chunk while the MMAs fill the next.
 
-constexpr int kTfThreads = 192;
+constexpr int kTfThreads = 384;
+constexpr int kTfLaunchRegs = 168, kTfIssueRegs = 56, kTfEpiRegs = 224;
+static_assert(4 * 32 * kTfIssueRegs + 8 * 32 * kTfEpiRegs == kTfThreads * kTfLaunchRegs,
+              "setmaxnreg split must balance the launch allocation");
+constexpr int kTfChunkKB = 16;                                     // K blocks per chunk (256 of K)
 constexpr uint32_t kTfAStage = kTf32BM * kTf32BK * 4;              // 8 KiB
 constexpr uint32_t kTfBStage = kTf32BN * kTf32BK * 4;              // 16 KiB
 constexpr uint32_t kTfStageBytes = 2 * (kTfAStage + kTfBStage);     // 48 KiB
-constexpr int kEpiPitch = 36;  // floats per staged row: 16-byte aligned, conflict-free
-constexpr uint32_t kTfEpiBytes = 4 * 32 * kEpiPitch * 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSw64RowGroupBytes = 8 * 64;  // 8 rows of one 64-byte swizzle row
 constexpr uint32_t kDescSwizzle64 = 4;
 constexpr int kTfBars = 2 * kTf32Stages + 5;
-constexpr size_t kTfSmemBytes =
-    1024 + (size_t)kTf32Stages * kTfStageBytes + kTfEpiBytes + kTfBars * 8 + 16;
+constexpr size_t kTfSmemBytes = 1024 + (size_t)kTf32Stages * kTfStageBytes + kTfBars * 8 + 16;
 
 __global__ void __launch_bounds__(kTfThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi,
@@ -310,11 +325,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK, ST = kTf32Stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
-    float* epi = reinterpret_cast<float*>(smem + ST * kTfStageBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * kTfStageBytes + kTfEpiBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * kTfStageBytes);
     uint64_t* empty = full + ST;
-    uint64_t* tfull = empty + ST;  // [2] accumulator ready
-    uint64_t* tempty = tfull + 2;  // [2] accumulator drained by the epilogue
+    uint64_t* tfull = empty + ST;  // [2] chunk accumulated
+    uint64_t* tempty = tfull + 2;  // [2] chunk drained by the epilogue
     uint64_t* drain = tempty + 2;  // every MMA of this CTA completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
@@ -328,7 +342,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], 8);
         }
         mbar_init(drain, 1);
         fence_barrier_init();
@@ -342,8 +356,9 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {  // ---------------------------------------- producer
-        if (lane == 0) {
+    if (warp < 4) {
+        regs_dec<kTfIssueRegs>();
+        if (warp == 0 && lane == 0) {  // ------------------------- producer
             tma_prefetch_desc(&tmAhi);
             tma_prefetch_desc(&tmAlo);
             tma_prefetch_desc(&tmBhi);
@@ -374,95 +389,101 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             }
             for (int s = 0; s < ST; ++s)
                 if ((issued >> s) & 1u) mbar_drain(&full[s], (last_par >> s) & 1u, args.timeout_ns);
-        }
-    } else if (warp == 1) {  // --------------------------------- MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {  // ---------------- MMA issuer
             constexpr uint32_t idesc = idesc_tf32(BM, BN);
             int stage = 0;
-            uint32_t phase = 0, iter = 0;
+            uint32_t phase = 0, chunk = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x, ++iter) {
+            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
                 const Unit t = decode_unit(args, u, BM, BN);
-                const uint32_t buf = iter & 1u, par = (iter >> 1) & 1u;
-                if (!mbar_wait(&tempty[buf], par ^ 1u, wc, kSiteTfMmaTmem)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, wc, kSiteTfMmaSmem)) {
+                for (int c0 = t.kb0; ok && c0 < t.kb1; c0 += kTfChunkKB, ++chunk) {
+                    const int c1 = min(c0 + kTfChunkKB, t.kb1);
+                    const uint32_t buf = chunk & 1u, par = (chunk >> 1) & 1u;
+                    if (!mbar_wait(&tempty[buf], par ^ 1u, wc, kSiteTfMmaTmem)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a_hi = smem_addr(smem + stage * kTfStageBytes);
-                    const uint32_t a_lo = a_hi + kTfAStage;
-                    const uint32_t b_hi = a_hi + 2 * kTfAStage;
-                    const uint32_t b_lo = b_hi + kTfBStage;
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    for (int kb = c0; kb < c1; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, wc, kSiteTfMmaSmem)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a_hi = smem_addr(smem + stage * kTfStageBytes);
+                        const uint32_t a_lo = a_hi + kTfAStage;
+                        const uint32_t b_hi = a_hi + 2 * kTfAStage;
+                        const uint32_t b_lo = b_hi + kTfBStage;
 #pragma unroll
-                    for (int ks = 0; ks < BK / 8; ++ks) {
-                        const uint32_t ko = ks * 32;  // 8 tf32 values along K
-                        const uint64_t dahi = smem_desc_kmajor(a_hi + ko, kSw64RowGroupBytes, kDescSwizzle64);
-                        const uint64_t dalo = smem_desc_kmajor(a_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
-                        const uint64_t dbhi = smem_desc_kmajor(b_hi + ko, kSw64RowGroupBytes, kDescSwizzle64);
-                        const uint64_t dblo = smem_desc_kmajor(b_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
-                        mma_tf32_ss(d_tmem, dalo, dbhi, idesc, (kb > t.kb0 || ks > 0) ? 1u : 0u);
-                        mma_tf32_ss(d_tmem, dahi, dblo, idesc, 1u);
-                        mma_tf32_ss(d_tmem, dahi, dbhi, idesc, 1u);
+                        for (int ks = 0; ks < BK / 8; ++ks) {
+                            const uint32_t ko = ks * 32;  // 8 tf32 values along K
+                            const uint64_t dahi = smem_desc_kmajor(a_hi + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                            const uint64_t dalo = smem_desc_kmajor(a_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                            const uint64_t dbhi = smem_desc_kmajor(b_hi + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                            const uint64_t dblo = smem_desc_kmajor(b_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
+                            mma_tf32_ss(d_tmem, dalo, dbhi, idesc, (kb > c0 || ks > 0) ? 1u : 0u);
+                            mma_tf32_ss(d_tmem, dahi, dblo, idesc, 1u);
+                            mma_tf32_ss(d_tmem, dahi, dbhi, idesc, 1u);
+                        }
+                        mma_commit(&empty[stage]);  // frees the stage once these MMAs are done
+                        if (++stage == ST) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    mma_commit(&empty[stage]);  // frees the stage once these MMAs are done
-                    if (++stage == ST) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    if (ok) mma_commit(&tfull[buf]);
                 }
-                if (!ok) break;
-                mma_commit(&tfull[buf]);
             }
             // no tensor-memory access may be in flight when the CTA frees it
             mma_commit(drain);
             mbar_drain(drain, 0, args.timeout_ns);
         }
     } else {  // ---------------------------------------------------- epilogue
-        const int q = warp & 3;  // this warp may access tensor-memory lanes 32q..32q+31
-        float* stg = epi + (warp - 2) * 32 * kEpiPitch;
+        regs_inc<kTfEpiRegs>();
+        const int e = warp - 4;
+        const int q = warp & 3;        // tensor-memory lanes 32q..32q+31 = tile rows
+        const int h = e >> 2;          // tile columns 128h..128h+127
         const bool vec = args.vec_out != 0;
-        uint32_t iter = 0;
-        for (long long u = blockIdx.x; u < args.units; u += gridDim.x, ++iter) {
+        uint32_t chunk = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
             const Unit t = decode_unit(args, u, BM, BN);
-            const uint32_t buf = iter & 1u, par = (iter >> 1) & 1u;
-            const bool got = mbar_wait(&tfull[buf], par, wc, kSiteTfEpilogue);
-            if (!__all_sync(0xffffffffu, got)) break;
-            tc_fence_after_sync();
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
-            const int row0 = t.m0 + q * 32;
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, r);
-                tmem_ld_wait(r);
-                if (c == BN / 32 - 1) {  // accumulator fully read: hand it back
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[buf]);
-                }
-                // lane i holds row row0+i, columns c*32..c*32+31; transpose
-                // through shared memory so each store covers whole row segments
+            float acc[128];
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    *reinterpret_cast<float4*>(stg + lane * kEpiPitch + 4 * v) =
-                        make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                __syncwarp();
-                const int col = t.n0 + c * 32 + 4 * (lane & 7);
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int rr = it * 4 + (lane >> 3);
-                    const float4 v = *reinterpret_cast<const float4*>(stg + rr * kEpiPitch + 4 * (lane & 7));
-                    const int grow = row0 + rr;
-                    if (grow < args.M) store_row4(t.out + (long long)grow * args.ldo, col, args.N, v, vec);
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int c0 = t.kb0; c0 < t.kb1; c0 += kTfChunkKB, ++chunk) {
+                const uint32_t buf = chunk & 1u, par = (chunk >> 1) & 1u;
+                const bool got = mbar_wait(&tfull[buf], par, wc, kSiteTfEpilogue);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after_sync();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + h * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + c * 32, r);
+                    tmem_ld_wait(r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc[c * 32 + i] += __uint_as_float(r[i]);
+                }
+                tc_fence_before_sync();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);  // chunk buffer may be refilled
+            }
+            if (!ok) break;
+            // guarded store of this thread's row segment (row-contiguous 512 B)
+            const int grow = t.m0 + q * 32 + lane;
+            if (grow < args.M) {
+                float* row = t.out + (long long)grow * args.ldo;
+                const int col0 = t.n0 + h * 128;
+#pragma unroll
+                for (int v = 0; v < 32; ++v)
+                    store_row4(row, col0 + 4 * v, args.N,
+                               make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]), vec);
             }
         }
     }
@@ -664,14 +685,17 @@ tg_status last_launch_status() {
 }  // namespace
 
 tg_status prepare_device_kernels() {
-    // The FFMA kernel's warpgroup register split is only balanced when it is
-    // launched with exactly kFfmaLaunchRegs registers per thread.
+    // The warpgroup register splits of both GEMM kernels only balance when the
+    // kernels are launched with exactly the register counts they were designed
+    // for; refuse to run a build that differs.
     cudaFuncAttributes fa{};
     if (cudaFuncGetAttributes(&fa, ffma_gemm_kernel) != cudaSuccess) return TG_ERR_CUDA;
     if (fa.numRegs != kFfmaLaunchRegs) return TG_ERR_CUDA;
     if (cudaFuncSetAttribute(ffma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFfmaSmemBytes) != cudaSuccess)
         return TG_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, tf32x3_gemm_kernel) != cudaSuccess) return TG_ERR_CUDA;
+    if (fa.numRegs != kTfLaunchRegs) return TG_ERR_CUDA;
     if (cudaFuncSetAttribute(tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kTfSmemBytes) != cudaSuccess)
         return TG_ERR_CUDA;
