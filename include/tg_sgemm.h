@@ -151,6 +151,40 @@ unsigned int tg_sgemm_error_site(cudaStream_t stream);
  * the caller then expects tg_sgemm_sync_status == TG_ERR_TIMEOUT. */
 tg_status tg_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
 
+/* Bytes of the fixed device scratch array behind tg_sgemm_noalloc (64 MiB). */
+#define TG_SGEMM_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* C = A x B on the 3xTF32 path without allocating any memory.  The surveyed
+ * pages have no counterpart of this entry point; it exists for callers that
+ * cannot allocate device memory at call time -- for example a host
+ * application that owns the whole device-memory budget through its own
+ * allocator and does not let libraries allocate, a latency-critical loop that
+ * must never enter the CUDA allocator, or code that must not be able to fail
+ * with out-of-memory once it runs.  tg_sgemm needs scratch memory (the hi/lo
+ * copies of A and B, and K-slice partials); here that scratch is a fixed
+ * array of TG_SGEMM_NOALLOC_SCRATCH_BYTES in device memory that CUDA reserves
+ * when it loads this library's device code on a GPU (with CUDA's default lazy
+ * loading: at the first tg_sgemm_noalloc call there) and that every such GPU
+ * holds until the process exits.  This call makes no cudaMalloc, cudaFree or
+ * other allocating call.
+ *
+ * Arguments, layout, ownership and results are those of tg_sgemm.  Limit: the
+ * hi/lo copies need 8*(M+N)*roundup(K,4) bytes (plus split-K partials, which
+ * are dropped when they would not fit); a product whose scratch exceeds
+ * TG_SGEMM_NOALLOC_SCRATCH_BYTES returns TG_ERR_WORKSPACE_TOO_SMALL and
+ * launches nothing (M = N = K = 2048 fits exactly).
+ *
+ * The first call on each device does a one-time set-up there (capability
+ * check, kernel attributes, and the scratch's device address via
+ * cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device shares the one scratch array, which keeps the last
+ * call's contents (nothing in it needs to start at zero): calls whose work
+ * overlaps on the GPU -- on different streams, or from host threads that do
+ * not order them -- race on it and give wrong results.  Order such calls, for
+ * example by issuing them on one stream. */
+tg_status tg_sgemm_noalloc(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                           float* C, int ldc, cudaStream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char* tg_status_string(tg_status status);
 

@@ -32,6 +32,7 @@ EXPORTS = (
     "tg_sgemm_plan",
     "tg_sgemm_workspace_bytes",
     "tg_sgemm_host",
+    "tg_sgemm_noalloc",
     "tg_sgemm_sync_status",
     "tg_sgemm_error_site",
     "tg_selftest_wait_timeout",
@@ -100,6 +101,8 @@ def lib():
         L.tg_sgemm_ex.restype = i
         L.tg_sgemm_host.argtypes = gemm + [ctypes.POINTER(Opts)]
         L.tg_sgemm_host.restype = i
+        L.tg_sgemm_noalloc.argtypes = gemm
+        L.tg_sgemm_noalloc.restype = i
         L.tg_sgemm_plan.argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
         L.tg_sgemm_plan.restype = i
         L.tg_sgemm_workspace_bytes.argtypes = [i, i, i, p, i, p, i, p, i, i, i]
@@ -185,6 +188,21 @@ def matmul(A, B, out=None, *, path="auto", split_k=0, workspace=None, main_begin
         st = lib().tg_sgemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
                                _stream_handle(stream), ctypes.byref(o))
     _check(st, "tg_sgemm_ex")
+    return out
+
+
+def matmul_noalloc(A, B, out, *, stream=None):
+    """C = A @ B through tg_sgemm_noalloc: 3xTF32 with the library's fixed
+    device scratch array instead of any allocation (``out`` must be given)."""
+    import torch
+
+    M, K = A.shape
+    _, N = B.shape
+    lda, ldb, ldc = _rowmajor_ld(A, "A"), _rowmajor_ld(B, "B"), _rowmajor_ld(out, "out")
+    with torch.cuda.device(A.device):
+        st = lib().tg_sgemm_noalloc(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                                    _stream_handle(stream))
+    _check(st, "tg_sgemm_noalloc")
     return out
 
 
