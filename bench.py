@@ -66,6 +66,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks (identity when not
+    distributed).  The timed region of the slowest rank bounds the job."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tflops(flop_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs one product per step."""
+    return flop_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -284,15 +301,12 @@ def main():
     clocks = sampler.stop(wall0, wall1)
     elapsed_ms = t_start.elapsed_time(t_end)
     main_ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
-    if world > 1:
-        t = torch.tensor([elapsed_ms, main_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms, main_ms = float(t[0]), float(t[1])
+    elapsed_ms, main_ms = max_over_ranks([elapsed_ms, main_ms], dev)
     status = tg.sync_status()
     if status != 0:
         raise RuntimeError(f"a kernel reported status {status} in the timed region")
     ms_per_step = elapsed_ms / args.steps
-    value = w.flop * world / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(w.flop, world, ms_per_step)
 
     # end to end through the host-buffer entry point (pinned memory)
     Ap, Bp = A.pin_memory(), B.pin_memory()

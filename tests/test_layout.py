@@ -1,0 +1,119 @@
+"""Host model of shared-memory banks for the access patterns the kernels use.
+
+Bank model ("03 CUDA Shared Memory: Tiling, Bank Conflicts, and Reduction",
+section "Bank Conflict"): 32 banks of 4-byte words; lanes hitting different
+words of one bank are serialised; lanes reading the same word share it
+(broadcast).  For 16-byte accesses a warp's request is served in 128-byte
+wavefronts: the cost is the largest number of distinct 16-byte words that fall
+on the same group of four banks.
+
+Each test restates, from the kernel source, the address a lane uses and checks
+that the pattern needs the minimum number of wavefronts.
+"""
+from math import gcd
+
+import pytest
+
+
+def wavefronts_32(addrs):
+    """Serialisation degree of one warp-wide 4-byte access."""
+    per_bank = {}
+    for a in addrs:
+        per_bank.setdefault((a // 4) % 32, set()).add(a // 4)
+    return max(len(v) for v in per_bank.values())
+
+
+def wavefronts_128(addrs):
+    """Wavefronts of one warp-wide 16-byte access (addresses 16-byte aligned)."""
+    words = {a // 16 for a in addrs}
+    per_quad = {}
+    for w in words:
+        per_quad.setdefault(w % 8, set()).add(w)
+    return max(len(v) for v in per_quad.values())
+
+
+def min_wavefronts_128(addrs):
+    return -(-len({a // 16 for a in addrs}) // 8)
+
+
+# ------------------------------------------------------------- the pages' rules
+
+
+@pytest.mark.parametrize("stride,degree", [(1, 1), (2, 2), (4, 4), (32, 32), (33, 1)])
+def test_stride_conflict_degree_is_gcd(stride, degree):
+    """Lane i reads word i*S: degree gcd(S, 32) (stride 2 is 2-way, 33 is free)."""
+    assert wavefronts_32([4 * stride * lane for lane in range(32)]) == degree == gcd(stride, 32)
+
+
+def test_transpose_padding():
+    """tile[32][32] read down a column is 32-way; tile[32][33] is conflict-free."""
+    col = 5
+    assert wavefronts_32([4 * (r * 32 + col) for r in range(32)]) == 32
+    assert wavefronts_32([4 * (r * 33 + col) for r in range(32)]) == 1
+
+
+def test_xor_swizzle_rows_and_columns():
+    """tile[r][c ^ r]: both a row and a column read touch all 32 banks once."""
+    def addr(r, c):
+        return 4 * (r * 32 + (c ^ r))
+    for r in range(32):
+        assert wavefronts_32([addr(r, c) for c in range(32)]) == 1
+    for c in range(32):
+        assert wavefronts_32([addr(r, c) for r in range(32)]) == 1
+
+
+# ------------------------------------------------------------ FFMA kernel reads
+
+BK = 32        # floats per A tile row (128 bytes, 128-byte TMA swizzle)
+BN = 256       # floats per B tile row (no swizzle)
+
+
+def ffma_a_addr(mw, lane, i, kk):
+    """A fragment: float4 of row wm*32 + lm + 4i at 16-byte chunk kk/4,
+    stored at chunk (kk/4) ^ (row % 8) (the 128-byte TMA swizzle)."""
+    wm, lm = mw & 3, lane & 3
+    r = wm * 32 + lm + 4 * i
+    return r * BK * 4 + (((kk >> 2) ^ (r & 7)) * 16)
+
+
+def ffma_b_addr(mw, lane, j, k):
+    wn, ln = mw >> 2, lane >> 2
+    return (k * BN + wn * 128 + 32 * j + 4 * ln) * 4
+
+
+@pytest.mark.parametrize("mw", range(8))
+def test_ffma_a_fragment_reads_conflict_free(mw):
+    for i in range(8):
+        for kk in range(0, BK, 4):
+            addrs = [ffma_a_addr(mw, lane, i, kk) for lane in range(32)]
+            assert wavefronts_128(addrs) == min_wavefronts_128(addrs) == 1
+
+
+@pytest.mark.parametrize("mw", range(8))
+def test_ffma_b_fragment_reads_conflict_free(mw):
+    for j in range(4):
+        for k in range(BK):
+            addrs = [ffma_b_addr(mw, lane, j, k) for lane in range(32)]
+            assert wavefronts_128(addrs) == min_wavefronts_128(addrs) == 1
+
+
+def test_unswizzled_a_would_conflict():
+    """Without the swizzle, the 4 rows read together (8 rows apart in a naive
+    mapping, or 1 row apart at a 128-byte pitch) share a bank group."""
+    addrs = [(lm + 4 * 0) * BK * 4 + 0 for lm in range(4) for _ in range(8)]
+    assert wavefronts_128(addrs) == 4
+
+
+# -------------------------------------------------------- pre-pass transpose
+
+
+def test_prepass_transpose_tile_conflict_free():
+    """B is staged as tile[ty + 8r][tx] (row writes) and read as tile[tx][ty + 8r]
+    with a 33-float pitch: both are conflict-free."""
+    pitch = 33
+    for ty in range(8):
+        for r in range(4):
+            writes = [4 * ((ty + 8 * r) * pitch + tx) for tx in range(32)]
+            reads = [4 * (tx * pitch + ty + 8 * r) for tx in range(32)]
+            assert wavefronts_32(writes) == 1
+            assert wavefronts_32(reads) == 1
