@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline (profiling runs)")
+    ap.add_argument("--no-probes", action="store_true", help="skip the instruction-mix peak probes")
     return ap.parse_args()
 
 
@@ -353,6 +354,15 @@ def main():
         elt = float(np.abs(got - r64).max() / np.abs(r64).max())
         max_rel = {"normwise_rel": max_rel, "max_abs_over_max_ref": elt, "rows_checked": len(rows)}
 
+    # ceilings of the two instruction mixes on this GPU (context for the roofline)
+    probes = None
+    if not args.no_probes:
+        probes = {"tf32_mma_tensor_tflops": tg.binding.probe_tf32_mma_tflops(use_collector=False),
+                  "tf32_mma_tensor_tflops_collector": tg.binding.probe_tf32_mma_tflops(use_collector=True),
+                  "ffma_tflops": tg.binding.probe_ffma_tflops(),
+                  "note": "tcgen05 kind::tf32 M128 N256 K8 issue loop with operands resident in shared "
+                          "memory; 16 independent FMA chains per thread"}
+
     line = {
         "metric": METRIC,
         "value": value,
@@ -382,6 +392,7 @@ def main():
         "gpu_launches": plan["launches"] * args.steps,
         "max_rel_error": max_rel,
         "clocks": clocks,
+        "probes": probes,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -99,6 +99,8 @@ typedef struct tg_plan_info {
     int prepass;       /* 1 = an operand re-layout kernel runs first */
     int launches;      /* kernels one call launches */
     size_t workspace_bytes;
+    int pair;          /* 3xTF32: CTAs per cluster sharing one B tile by TMA multicast (1 or 2);
+                          a unit is then `pair` vertically adjacent tiles */
 } tg_plan_info;
 
 /* C = A x B with automatic path and split choice (see the file comment for

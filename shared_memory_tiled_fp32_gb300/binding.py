@@ -25,7 +25,7 @@ STATUS = {
 PATHS = {"auto": 0, "ffma": 1, "tf32x3": 2}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
-# Every symbol include/tg_sgemm.h declares.
+# Every symbol include/tg_sgemm.h and include/tg_probes.h declare.
 EXPORTS = (
     "tg_sgemm",
     "tg_sgemm_ex",
@@ -38,6 +38,8 @@ EXPORTS = (
     "tg_selftest_wait_timeout",
     "tg_status_string",
     "tg_sgemm_version",
+    "tg_probe_tf32_mma",
+    "tg_probe_ffma",
 )
 
 
@@ -73,6 +75,7 @@ class PlanInfo(ctypes.Structure):
         ("prepass", ctypes.c_int),
         ("launches", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
+        ("pair", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -117,6 +120,10 @@ def lib():
         L.tg_status_string.restype = ctypes.c_char_p
         L.tg_sgemm_version.argtypes = []
         L.tg_sgemm_version.restype = i
+        L.tg_probe_tf32_mma.argtypes = [i, i, vp, ctypes.POINTER(ctypes.c_double)]
+        L.tg_probe_tf32_mma.restype = i
+        L.tg_probe_ffma.argtypes = [i, p, vp, ctypes.POINTER(ctypes.c_double)]
+        L.tg_probe_ffma.restype = i
         _lib = L
     return _lib
 
@@ -252,3 +259,41 @@ def selftest_wait_timeout(timeout_us: int, stream=None) -> int:
 
 def status_string(status: int) -> str:
     return lib().tg_status_string(status).decode()
+
+
+def _time_probe(launch):
+    import torch
+
+    stream = torch.cuda.current_stream()
+    launch(stream)  # warm-up
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    flop = launch(stream)
+    e1.record(stream)
+    e1.synchronize()
+    return flop / (e0.elapsed_time(e1) * 1e-3) / 1e12
+
+
+def probe_tf32_mma_tflops(iters=100000, use_collector=True) -> float:
+    """Tensor TFLOP/s of the 3xTF32 main loop's MMA issue pattern, operands
+    resident in shared memory (see include/tg_probes.h)."""
+    def launch(stream):
+        f = ctypes.c_double()
+        _check(lib().tg_probe_tf32_mma(iters, int(use_collector), _stream_handle(stream), ctypes.byref(f)),
+               "tg_probe_tf32_mma")
+        return f.value
+    return _time_probe(launch)
+
+
+def probe_ffma_tflops(iters=100000) -> float:
+    """fp32 FMA TFLOP/s with 16 independent chains per thread."""
+    import torch
+
+    sink = torch.zeros(1, device="cuda")
+
+    def launch(stream):
+        f = ctypes.c_double()
+        _check(lib().tg_probe_ffma(iters, sink.data_ptr(), _stream_handle(stream), ctypes.byref(f)),
+               "tg_probe_ffma")
+        return f.value
+    return _time_probe(launch)

@@ -82,6 +82,7 @@ void fill_info(const Plan& p, tg_plan_info* out) {
     out->prepass = (p.path == TG_PATH_TF32X3 && !p.zero_fill && p.M > 0 && p.N > 0) || p.pack_a || p.pack_b;
     out->launches = p.launches;
     out->workspace_bytes = p.ws_bytes;
+    out->pair = p.pair;
 }
 
 }  // namespace

@@ -29,8 +29,10 @@ struct Plan {
     int split = 1;
     int bm = 0, bn = 0, bk = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0;
-    long long units = 0;
+    int pair = 1;        // 3xTF32: CTAs per cluster sharing one B tile (TMA multicast)
+    long long units = 0; // work units (a unit is `pair` vertically adjacent tiles x one K slice)
     int grid = 0;
+    int num_sms = 0;     // SMs planned for
     int nkb = 0;         // K blocks of bk
     int k4 = 0, n4 = 0;  // K and N rounded up to a multiple of 4 (16-byte rows)
     bool zero_fill = false;  // K == 0: C = 0, nothing else runs

@@ -45,7 +45,8 @@ enum : uint32_t {
 
 struct GemmArgs {
     int M, N, K;
-    int tiles_m, tiles_n;
+    int tiles_m, tiles_n;    // tiles_m counts rows of `pair` tiles
+    int pair;                // CTAs per cluster sharing a B tile (1 or 2)
     int split, nkb;
     long long units;
     float* out;              // C (split == 1) or the first K-slice partial
@@ -62,10 +63,12 @@ struct Unit {
 
 // Work unit u -> (K slice, output tile).  Tiles are visited in groups of
 // kGroupM tile rows, column by column inside a group, so CTAs running at the
-// same time share A rows and B columns in L2.
+// same time share A rows and B columns in L2.  With pair = 2 a unit is two
+// vertically adjacent tiles; the CTA of cluster rank `rank` takes tile row
+// 2*row + rank.
 constexpr int kGroupM = 8;
 
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int BM, int BN) {
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int rank, int BM, int BN) {
     const long long tiles = (long long)a.tiles_m * a.tiles_n;
     const int s = (int)(u / tiles);
     const int t = (int)(u - (long long)s * tiles);
@@ -75,7 +78,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int 
     const int gm = min(a.tiles_m - first_m, kGroupM);
     const int r = t - g * per_group;
     Unit x;
-    x.m0 = (first_m + r % gm) * BM;
+    x.m0 = ((first_m + r % gm) * a.pair + rank) * BM;
     x.n0 = (r / gm) * BN;
     x.kb0 = (int)((long long)s * a.nkb / a.split);
     x.kb1 = (int)((long long)(s + 1) * a.nkb / a.split);
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
             for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-                const Unit t = decode_unit(args, u, BM, BN);
+                const Unit t = decode_unit(args, u, 0, BM, BN);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteFfmaProducer)) {
                         ok = false;
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     for (long long u = blockIdx.x; u < args.units; u += gridDim.x) {
-        const Unit t = decode_unit(args, u, BM, BN);
+        const Unit t = decode_unit(args, u, 0, BM, BN);
         float acc[8][16];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -282,8 +285,10 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 // K-major layout expects.
 //
 // Per 8-wide K slice the MMA thread issues
-//     D += A_lo B_hi;  D += A_hi B_lo;  D += A_hi B_hi
-// (the small terms first; A_lo B_lo, of relative size 2^-22, is dropped).
+//     D += A_hi B_lo;  D += A_hi B_hi;  D += A_lo B_hi
+// (A_lo B_lo, of relative size 2^-22, is dropped).  The first two share A_hi,
+// which the tensor core keeps in its A collector buffer, so each slice reads
+// A_hi from shared memory once.
 //
 // Accumulation precision.  The tensor core's fp32 accumulation loses about
 // one unit in the last place towards zero per MMA instead of rounding to
@@ -317,6 +322,7 @@ constexpr uint32_t kDescSwizzle64 = 4;
 constexpr int kTfBars = 2 * kTf32Stages + 5;
 constexpr size_t kTfSmemBytes = 1024 + (size_t)kTf32Stages * kTfStageBytes + kTfBars * 8 + 16;
 
+template <int kPair>
 __global__ void __launch_bounds__(kTfThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi,
                        const __grid_constant__ CUtensorMap tmAlo,
@@ -334,11 +340,18 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WaitCtl wc{&g_error_word, args.timeout_ns};
+    // cluster of kPair CTAs: CTA `rank` computes tile row 2*row + rank and
+    // loads rank's half of the shared B tile for both CTAs (TMA multicast)
+    const int rank = kPair > 1 ? (int)cluster_ctarank() : 0;
+    const long long first_unit = blockIdx.x / kPair, unit_stride = gridDim.x / kPair;
+    constexpr uint16_t kPairMask = (uint16_t)((1u << kPair) - 1u);
+    constexpr uint32_t kBHalf = kTfBStage / kPair;  // bytes of B (hi or lo) one CTA loads
+    constexpr int kBRows = BN / kPair;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kPair);  // one MMA commit from each CTA of the pair
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -353,6 +366,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (kPair > 1) cluster_sync_all();  // the peer's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -366,19 +380,30 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-                const Unit t = decode_unit(args, u, BM, BN);
+            for (long long u = first_unit; ok && u < args.units; u += unit_stride) {
+                const Unit t = decode_unit(args, u, rank, BM, BN);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    // with a pair, "empty" completes only when both CTAs are done
+                    // with the stage, since this CTA's B half lands in both
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteTfProducer)) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = smem + stage * kTfStageBytes;
+                    // this CTA receives all of A_hi, A_lo, B_hi, B_lo (48 KiB),
+                    // half of B from its own loads and half from the peer's
                     mbar_arrive_expect_tx(&full[stage], kTfStageBytes);
                     tma_load_2d(st, &tmAhi, &full[stage], kb * BK, t.m0);
                     tma_load_2d(st + kTfAStage, &tmAlo, &full[stage], kb * BK, t.m0);
-                    tma_load_2d(st + 2 * kTfAStage, &tmBhi, &full[stage], kb * BK, t.n0);
-                    tma_load_2d(st + 2 * kTfAStage + kTfBStage, &tmBlo, &full[stage], kb * BK, t.n0);
+                    if (kPair > 1) {
+                        tma_load_2d_multicast(st + 2 * kTfAStage + rank * kBHalf, &tmBhi, &full[stage],
+                                              kb * BK, t.n0 + rank * kBRows, kPairMask);
+                        tma_load_2d_multicast(st + 2 * kTfAStage + kTfBStage + rank * kBHalf, &tmBlo,
+                                              &full[stage], kb * BK, t.n0 + rank * kBRows, kPairMask);
+                    } else {
+                        tma_load_2d(st + 2 * kTfAStage, &tmBhi, &full[stage], kb * BK, t.n0);
+                        tma_load_2d(st + 2 * kTfAStage + kTfBStage, &tmBlo, &full[stage], kb * BK, t.n0);
+                    }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == ST) {
@@ -394,8 +419,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             int stage = 0;
             uint32_t phase = 0, chunk = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-                const Unit t = decode_unit(args, u, BM, BN);
+            for (long long u = first_unit; ok && u < args.units; u += unit_stride) {
+                const Unit t = decode_unit(args, u, rank, BM, BN);
                 for (int c0 = t.kb0; ok && c0 < t.kb1; c0 += kTfChunkKB, ++chunk) {
                     const int c1 = min(c0 + kTfChunkKB, t.kb1);
                     const uint32_t buf = chunk & 1u, par = (chunk >> 1) & 1u;
@@ -422,11 +447,17 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                             const uint64_t dalo = smem_desc_kmajor(a_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
                             const uint64_t dbhi = smem_desc_kmajor(b_hi + ko, kSw64RowGroupBytes, kDescSwizzle64);
                             const uint64_t dblo = smem_desc_kmajor(b_lo + ko, kSw64RowGroupBytes, kDescSwizzle64);
-                            mma_tf32_ss(d_tmem, dalo, dbhi, idesc, (kb > c0 || ks > 0) ? 1u : 0u);
-                            mma_tf32_ss(d_tmem, dahi, dblo, idesc, 1u);
-                            mma_tf32_ss(d_tmem, dahi, dbhi, idesc, 1u);
+                            // A_hi is read from shared memory once and kept in the
+                            // tensor core's A collector for its second product
+                            mma_tf32_ss_fill_a(d_tmem, dahi, dblo, idesc, (kb > c0 || ks > 0) ? 1u : 0u);
+                            mma_tf32_ss_lastuse_a(d_tmem, dahi, dbhi, idesc, 1u);
+                            mma_tf32_ss(d_tmem, dalo, dbhi, idesc, 1u);
                         }
-                        mma_commit(&empty[stage]);  // frees the stage once these MMAs are done
+                        // frees the stage (in both CTAs of a pair) once these MMAs are done
+                        if (kPair > 1)
+                            mma_commit_multicast(&empty[stage], kPairMask);
+                        else
+                            mma_commit(&empty[stage]);
                         if (++stage == ST) {
                             stage = 0;
                             phase ^= 1u;
@@ -447,8 +478,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         const bool vec = args.vec_out != 0;
         uint32_t chunk = 0;
         bool ok = true;
-        for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-            const Unit t = decode_unit(args, u, BM, BN);
+        for (long long u = first_unit; ok && u < args.units; u += unit_stride) {
+            const Unit t = decode_unit(args, u, rank, BM, BN);
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
@@ -494,6 +525,9 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);
     }
+    // neither CTA of a pair may exit while the other can still multicast into
+    // its shared memory or arrive on its barriers
+    if (kPair > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------ pre-pass
@@ -502,9 +536,13 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 //   hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32).
 // PACK (FFMA, operand not TMA-legal): A -> [M][k4], B -> [K][n4].
 // Padding columns (k >= K, n >= N) are written as zeros (ghost elements).
-// Work is cut into 32 x 32 tiles, one per 256-thread block iteration.  B's
-// transpose goes through a [32][33] shared tile: the padded row makes the
-// column read conflict-free ("Bank Conflict", padding: gcd(33, 32) = 1).
+//
+// Memory-bound: the row-wise parts (A always, B when packing) move 4 values
+// per item with 16-byte stores (and 16-byte loads when the source rows are
+// 16-byte aligned), four items in flight per thread.  B's transpose runs on
+// 64 x 64 tiles through a [64][65] shared tile, 16 values per thread in
+// flight; the padded row makes the column read conflict-free ("Bank
+// Conflict", padding: gcd(65, 32) = 1).  Loads and stores are row-coalesced.
 
 struct PrepassArgs {
     const float* A;
@@ -512,70 +550,96 @@ struct PrepassArgs {
     const float* B;
     long long ldb;
     int M, N, K, k4, n4;
-    float* a0;
-    float* a1;
-    float* b0;
-    float* b1;
-    long long a_tiles, b_tiles;
-    int a_tiles_inner, b_tiles_inner;
+    float* a0;  // SPLIT: A_hi; PACK: copy of A (nullptr = no A part)
+    float* a1;  // SPLIT: A_lo
+    float* b0;  // SPLIT: B_hi^T; PACK: copy of B (nullptr = no B part)
+    float* b1;  // SPLIT: B_lo^T
+    int vec_a, vec_b;  // source rows start on 16-byte boundaries
+    long long a_items, b_items;  // A: M*k4/4; B: K*n4/4 (PACK) or 64x64 tiles (SPLIT)
+    int b_tiles_k;               // SPLIT: 64-wide tiles along k4
 };
+
+__device__ __forceinline__ float4 load_row4(const float* src, long long ld, int row, int col,
+                                            int cols, bool vec) {
+    const float* p = src + (long long)row * ld + col;
+    if (vec && col + 3 < cols) return *reinterpret_cast<const float4*>(p);
+    float4 v;
+    v.x = col < cols ? p[0] : 0.0f;
+    v.y = col + 1 < cols ? p[1] : 0.0f;
+    v.z = col + 2 < cols ? p[2] : 0.0f;
+    v.w = col + 3 < cols ? p[3] : 0.0f;
+    return v;
+}
+
+template <bool SPLIT>
+__device__ __forceinline__ void store_split4(float* d0, float* d1, long long o, float4 x) {
+    if (SPLIT) {
+        const float4 hi = make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
+        *reinterpret_cast<float4*>(d0 + o) = hi;
+        *reinterpret_cast<float4*>(d1 + o) =
+            make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
+    } else {
+        *reinterpret_cast<float4*>(d0 + o) = x;
+    }
+}
+
+// dst[r][c..c+3] (row pitch cols4) from src[r][c..c+3] (row pitch ld, valid
+// columns < cols, zero beyond), for every 4-column item of rows x cols4.
+template <bool SPLIT>
+__device__ __forceinline__ void rowwise_pass(const float* src, long long ld, int cols, int cols4,
+                                             bool vec, float* d0, float* d1, long long items) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const int groups = cols4 / 4;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < items; i += 4 * stride) {
+        float4 v[4];
+        long long o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long long it = i + u * stride;
+            o[u] = -1;
+            if (it < items) {
+                const int r = (int)(it / groups), c = (int)(it % groups) * 4;
+                v[u] = load_row4(src, ld, r, c, cols, vec);
+                o[u] = (long long)r * cols4 + c;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (o[u] >= 0) store_split4<SPLIT>(d0, d1, o[u], v[u]);
+    }
+}
 
 template <bool SPLIT>
 __global__ void __launch_bounds__(256) prepass_kernel(PrepassArgs p) {
-    __shared__ float tile[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const long long total = p.a_tiles + p.b_tiles;
-    for (long long t = blockIdx.x; t < total; t += gridDim.x) {
-        if (t < p.a_tiles) {
-            const int tm = (int)(t / p.a_tiles_inner), tk = (int)(t % p.a_tiles_inner);
-            const int k = tk * 32 + tx;
+    __shared__ float tile[64][65];
+    if (p.a0 != nullptr)
+        rowwise_pass<SPLIT>(p.A, p.lda, p.K, p.k4, p.vec_a != 0, p.a0, p.a1, p.a_items);
+    if (p.b0 == nullptr) return;
+    if (!SPLIT) {
+        rowwise_pass<false>(p.B, p.ldb, p.N, p.n4, p.vec_b != 0, p.b0, nullptr, p.b_items);
+        return;
+    }
+    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4 threads
+    for (long long t = blockIdx.x; t < p.b_items; t += gridDim.x) {
+        const int n0 = (int)(t / p.b_tiles_k) * 64, k0 = (int)(t % p.b_tiles_k) * 64;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int m = tm * 32 + ty + 8 * r;
-                if (m < p.M && k < p.k4) {
-                    const float x = (k < p.K) ? p.A[(long long)m * p.lda + k] : 0.0f;
-                    const long long o = (long long)m * p.k4 + k;
-                    if (SPLIT) {
-                        const float hi = to_tf32(x);
-                        p.a0[o] = hi;
-                        p.a1[o] = to_tf32(x - hi);
-                    } else {
-                        p.a0[o] = x;
-                    }
-                }
-            }
-        } else if (SPLIT) {
-            const long long tb = t - p.a_tiles;
-            const int tn = (int)(tb / p.b_tiles_inner), tk = (int)(tb % p.b_tiles_inner);
+        for (int j = 0; j < 16; ++j) {
+            const int k = k0 + ty + 4 * j, n = n0 + tx;
+            tile[ty + 4 * j][tx] = (k < p.K && n < p.N) ? p.B[(long long)k * p.ldb + n] : 0.0f;
+        }
+        __syncthreads();
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int k = tk * 32 + ty + 8 * r, n = tn * 32 + tx;
-                tile[ty + 8 * r][tx] = (k < p.K && n < p.N) ? p.B[(long long)k * p.ldb + n] : 0.0f;
-            }
-            __syncthreads();
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int n = tn * 32 + ty + 8 * r, k = tk * 32 + tx;
-                if (n < p.N && k < p.k4) {
-                    const float x = tile[tx][ty + 8 * r];
-                    const float hi = to_tf32(x);
-                    const long long o = (long long)n * p.k4 + k;
-                    p.b0[o] = hi;
-                    p.b1[o] = to_tf32(x - hi);
-                }
-            }
-            __syncthreads();
-        } else {
-            const long long tb = t - p.a_tiles;
-            const int tk = (int)(tb / p.b_tiles_inner), tn = (int)(tb % p.b_tiles_inner);
-            const int n = tn * 32 + tx;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int k = tk * 32 + ty + 8 * r;
-                if (k < p.K && n < p.n4)
-                    p.b0[(long long)k * p.n4 + n] = (n < p.N) ? p.B[(long long)k * p.ldb + n] : 0.0f;
+        for (int j = 0; j < 16; ++j) {
+            const int n = n0 + ty + 4 * j, k = k0 + tx;
+            if (n < p.N && k < p.k4) {
+                const float x = tile[tx][ty + 4 * j];
+                const float hi = to_tf32(x);
+                const long long o = (long long)n * p.k4 + k;
+                p.b0[o] = hi;
+                p.b1[o] = to_tf32(x - hi);
             }
         }
+        __syncthreads();
     }
 }
 
@@ -684,7 +748,18 @@ tg_status last_launch_status() {
 
 }  // namespace
 
+// Resident 256-thread blocks per SM of the two pre-pass kernels (the grid is
+// sized to exactly fill the GPU once).
+int g_prepass_blocks_per_sm[2] = {4, 4};
+// CTA pairs of the 3xTF32 kernel resident at once (0 = unknown).
+int g_tf32_pair_clusters = 0;
+
 tg_status prepare_device_kernels() {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<false>, 256, 0) == cudaSuccess && nb > 0)
+        g_prepass_blocks_per_sm[0] = nb;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<true>, 256, 0) == cudaSuccess && nb > 0)
+        g_prepass_blocks_per_sm[1] = nb;
     // The warpgroup register splits of both GEMM kernels only balance when the
     // kernels are launched with exactly the register counts they were designed
     // for; refuse to run a build that differs.
@@ -694,11 +769,30 @@ tg_status prepare_device_kernels() {
     if (cudaFuncSetAttribute(ffma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFfmaSmemBytes) != cudaSuccess)
         return TG_ERR_CUDA;
-    if (cudaFuncGetAttributes(&fa, tf32x3_gemm_kernel) != cudaSuccess) return TG_ERR_CUDA;
-    if (fa.numRegs != kTfLaunchRegs) return TG_ERR_CUDA;
-    if (cudaFuncSetAttribute(tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kTfSmemBytes) != cudaSuccess)
-        return TG_ERR_CUDA;
+    for (auto kern : {tf32x3_gemm_kernel<1>, tf32x3_gemm_kernel<2>}) {
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TG_ERR_CUDA;
+        if (fa.numRegs != kTfLaunchRegs) return TG_ERR_CUDA;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTfSmemBytes) !=
+            cudaSuccess)
+            return TG_ERR_CUDA;
+    }
+    // how many CTA pairs the GPU holds at once (one CTA per SM)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kTfThreads);
+    cfg.dynamicSmemBytes = kTfSmemBytes;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, tf32x3_gemm_kernel<2>, &cfg) == cudaSuccess && clusters > 0)
+        g_tf32_pair_clusters = clusters;
+    else
+        cudaGetLastError();
     return TG_OK;
 }
 
@@ -714,7 +808,8 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     ga.M = p.M;
     ga.N = p.N;
     ga.K = p.K;
-    ga.tiles_m = p.tiles_m;
+    ga.pair = p.pair;
+    ga.tiles_m = (p.tiles_m + p.pair - 1) / p.pair;
     ga.tiles_n = p.tiles_n;
     ga.split = p.split;
     ga.nkb = p.nkb;
@@ -742,6 +837,10 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     pa.K = p.K;
     pa.k4 = p.k4;
     pa.n4 = p.n4;
+    pa.vec_a = (reinterpret_cast<uintptr_t>(A) % 16 == 0 && p.lda % 4 == 0) ? 1 : 0;
+    pa.vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0 && p.ldb % 4 == 0) ? 1 : 0;
+    // one full wave of resident blocks keeps HBM busy without a tail
+    const int prepass_grid = g_prepass_blocks_per_sm[p.path == TG_PATH_TF32X3 ? 1 : 0] * p.num_sms;
 
     if (p.path == TG_PATH_TF32X3) {
         float* ahi = reinterpret_cast<float*>(w + p.off_a0);
@@ -752,23 +851,40 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         pa.a1 = alo;
         pa.b0 = bhi;
         pa.b1 = blo;
-        pa.a_tiles_inner = (p.k4 + 31) / 32;
-        pa.b_tiles_inner = (p.k4 + 31) / 32;
-        pa.a_tiles = (long long)((p.M + 31) / 32) * pa.a_tiles_inner;
-        pa.b_tiles = (long long)((p.N + 31) / 32) * pa.b_tiles_inner;
-        const long long tiles = pa.a_tiles + pa.b_tiles;
-        prepass_kernel<true><<<(int)(tiles < 8192 ? tiles : 8192), 256, 0, stream>>>(pa);
+        pa.a_items = (long long)p.M * (p.k4 / 4);
+        pa.b_tiles_k = (p.k4 + 63) / 64;
+        pa.b_items = (long long)((p.N + 63) / 64) * pa.b_tiles_k;
+        prepass_kernel<true><<<prepass_grid, 256, 0, stream>>>(pa);
         if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
 
         CUtensorMap mAhi, mAlo, mBhi, mBlo;
         const uint64_t row = 4ull * p.k4;
         if (!make_map(&mAhi, ahi, p.K, p.M, row, kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
             !make_map(&mAlo, alo, p.K, p.M, row, kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
-            !make_map(&mBhi, bhi, p.K, p.N, row, kTf32BK, kTf32BN, CU_TENSOR_MAP_SWIZZLE_64B) ||
-            !make_map(&mBlo, blo, p.K, p.N, row, kTf32BK, kTf32BN, CU_TENSOR_MAP_SWIZZLE_64B))
+            !make_map(&mBhi, bhi, p.K, p.N, row, kTf32BK, kTf32BN / p.pair, CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !make_map(&mBlo, blo, p.K, p.N, row, kTf32BK, kTf32BN / p.pair, CU_TENSOR_MAP_SWIZZLE_64B))
             return TG_ERR_CUDA;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
-        tf32x3_gemm_kernel<<<p.grid, kTfThreads, kTfSmemBytes, stream>>>(mAhi, mAlo, mBhi, mBlo, ga);
+        if (p.pair == 2) {
+            int clusters = p.grid / 2;
+            if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3(2 * clusters);
+            cfg.blockDim = dim3(kTfThreads);
+            cfg.dynamicSmemBytes = kTfSmemBytes;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr{};
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cfg, tf32x3_gemm_kernel<2>, mAhi, mAlo, mBhi, mBlo, ga) != cudaSuccess)
+                return TG_ERR_CUDA;
+        } else {
+            tf32x3_gemm_kernel<1><<<p.grid, kTfThreads, kTfSmemBytes, stream>>>(mAhi, mAlo, mBhi, mBlo, ga);
+        }
         if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
     } else {
@@ -778,12 +894,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         if (p.pack_a || p.pack_b) {
             pa.a0 = p.pack_a ? reinterpret_cast<float*>(w + p.off_a0) : nullptr;
             pa.b0 = p.pack_b ? reinterpret_cast<float*>(w + p.off_b0) : nullptr;
-            pa.a_tiles_inner = (p.k4 + 31) / 32;
-            pa.b_tiles_inner = (p.n4 + 31) / 32;
-            pa.a_tiles = p.pack_a ? (long long)((p.M + 31) / 32) * pa.a_tiles_inner : 0;
-            pa.b_tiles = p.pack_b ? (long long)((p.K + 31) / 32) * pa.b_tiles_inner : 0;
-            const long long tiles = pa.a_tiles + pa.b_tiles;
-            prepass_kernel<false><<<(int)(tiles < 8192 ? tiles : 8192), 256, 0, stream>>>(pa);
+            pa.a_items = (long long)p.M * (p.k4 / 4);
+            pa.b_items = (long long)p.K * (p.n4 / 4);
+            prepass_kernel<false><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
             if (p.pack_a) {
                 a_src = pa.a0;

@@ -11,6 +11,8 @@
 // Block 크기", taken at its extreme: few warps, each with much work).
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "tg_internal.h"
 
@@ -62,6 +64,7 @@ void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int l
     p->lda = lda;
     p->ldb = ldb;
     p->ldc = ldc;
+    p->num_sms = num_sms;
     p->path = (path == TG_PATH_FFMA) ? TG_PATH_FFMA : TG_PATH_TF32X3;
     p->vec_c = C != nullptr && (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
     if (p->path == TG_PATH_TF32X3) {
@@ -96,8 +99,14 @@ void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int l
         S = (int)std::max<long long>(1, s);
     }
     p->split = S;
-    p->units = tiles * S;
-    p->grid = (int)std::min<long long>(p->units, num_sms);
+    // 3xTF32: two CTAs of a cluster take vertically adjacent tiles and share
+    // the B tile, each loading half of it for both (TMA multicast), which
+    // halves the B traffic from L2.  TG_TF32X3_PAIR=0 turns this off.
+    const char* pair_env = std::getenv("TG_TF32X3_PAIR");
+    const bool pair_off = pair_env != nullptr && std::strcmp(pair_env, "0") == 0;
+    p->pair = (p->path == TG_PATH_TF32X3 && p->tiles_m >= 2 && num_sms >= 2 && !pair_off) ? 2 : 1;
+    p->units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n * S;
+    p->grid = p->pair * (int)std::min<long long>(p->units, num_sms / p->pair);
 
     size_t off = 0;
     auto take = [&](size_t bytes) {

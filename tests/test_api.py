@@ -11,11 +11,12 @@ import shared_memory_tiled_fp32_gb300 as tg
 from shared_memory_tiled_fp32_gb300 import binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "tg_sgemm.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 def header_functions():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:unsigned\s+)?[a-z_]+\s*\**\s*(tg_\w+)\s*\(", src, flags=re.M)))
 
@@ -69,12 +70,17 @@ def test_plan_tiles_split_and_workspace():
     sms = 152
     p = tg.plan(8192, 8192, 8192, num_sms=sms)
     assert (p["path"], p["tiles_m"], p["tiles_n"], p["split_k"]) == ("tf32x3", 64, 32, 1)
-    assert p["grid"] == sms and p["units"] == 2048 and p["launches"] == 2
+    # pairs of vertically adjacent tiles share B (cluster of 2 CTAs)
+    assert p["pair"] == 2 and p["grid"] == sms and p["units"] == 32 * 32 and p["launches"] == 2
     assert p["workspace_bytes"] == 4 * 8192 * 8192 * 4  # A_hi, A_lo, B_hi^T, B_lo^T
     # ragged: ceil(777/128) x ceil(1029/256) tiles, split to fill the SMs
     p = tg.plan(777, 1029, 513, num_sms=sms)
     assert (p["tiles_m"], p["tiles_n"]) == (7, 5)
-    assert p["split_k"] == 4 and p["units"] == 140 and p["launches"] == 3
+    assert p["split_k"] == 4 and p["pair"] == 2 and p["units"] == 4 * 5 * 4 and p["launches"] == 3
+    assert p["grid"] == 2 * min(p["units"], sms // 2)
+    # one tile row cannot be paired; FFMA never pairs
+    assert tg.plan(100, 4096, 4096, num_sms=sms)["pair"] == 1
+    assert tg.plan(4096, 4096, 4096, num_sms=sms, path="ffma")["pair"] == 1
     # an explicit split is capped by the K blocks
     p = tg.plan(64, 64, 32, num_sms=sms, split_k=9)
     assert p["split_k"] == 2  # ceil(32/16) K blocks

@@ -199,3 +199,17 @@ def test_plan_on_device(tg):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert p["grid"] == min(p["units"], sms)
     assert p["path"] == "tf32x3"
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_tf32x3_cluster_pairs_on_and_off(tg, pair, monkeypatch):
+    """The 3xTF32 kernel with and without CTA pairs sharing B by TMA multicast,
+    including odd tile-row counts (the last pair's second CTA is all ghost)."""
+    monkeypatch.setenv("TG_TF32X3_PAIR", pair)
+    for i, (M, N, K) in enumerate([(129, 300, 700), (383, 513, 300), (640, 256, 2048), (1, 7, 9)]):
+        A, B = make_inputs(M, N, K, "uniform", 900 + i)
+        ref = oracle.sgemm(A.numpy(), B.numpy())
+        p = tg.plan(M, N, K, path="tf32x3")
+        assert p["tiles_m"] == -(-M // 128)
+        for split in (0, 1, 2):
+            assert_close(run(tg, A, B, path="tf32x3", split_k=split), ref, K, f"pair={pair} {M}x{N}x{K} s{split}")
