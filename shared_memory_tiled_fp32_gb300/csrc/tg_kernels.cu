@@ -110,7 +110,9 @@ __device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {
 // is the producer (one thread issues the TMA loads); warpgroups 1-2 (math
 // warps 0-7) do the math.  Each math thread keeps an 8 x 16 block of C in registers
 // (register tiling: "Occupancy와 Block 크기" and PMPP ch. 6 coarsening): per
-// k it reads 8 values of A and 16 of B from shared memory and issues 128 FMAs.
+// k it reads 8 values of A and 16 of B from shared memory and performs 128
+// FMAs as 64 packed fma.rn.f32x2 (two lanes of fp32 per instruction, same
+// rounding as fmaf), which leaves issue slots for the shared-memory loads.
 //
 // Shared-memory layouts and banks ("Bank Conflict" section):
 //  * A tile [128 rows][32 k] arrives with the 128-byte TMA swizzle: the 16-byte
@@ -205,11 +207,12 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
     uint32_t phase = 0;
     for (long long u = blockIdx.x; u < args.units; u += gridDim.x) {
         const Unit t = decode_unit(args, u, 0, BM, BN);
-        float acc[8][16];
+        // acc[i][p] holds columns 32*(p/2) + 4ln + 2*(p%2) + {0, 1} of row i
+        unsigned long long acc[8][8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0ull;
 
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
@@ -231,19 +234,18 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
                 }
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
-                    float4 bv[4];
+                    // B as packed pairs: bv[j].x = columns (0,1), .y = (2,3) of chunk j
+                    ulonglong2 bv[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        bv[j] = *reinterpret_cast<const float4*>(b + (kk + k4) * BN + 32 * j);
+                        bv[j] = *reinterpret_cast<const ulonglong2*>(b + (kk + k4) * BN + 32 * j);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float x = lanef(av[i], k4);
+                        const unsigned long long x2 = f32x2_splat(lanef(av[i], k4));
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            acc[i][4 * j + 0] = fmaf(x, bv[j].x, acc[i][4 * j + 0]);
-                            acc[i][4 * j + 1] = fmaf(x, bv[j].y, acc[i][4 * j + 1]);
-                            acc[i][4 * j + 2] = fmaf(x, bv[j].z, acc[i][4 * j + 2]);
-                            acc[i][4 * j + 3] = fmaf(x, bv[j].w, acc[i][4 * j + 3]);
+                            fma_f32x2(acc[i][2 * j], x2, bv[j].x);
+                            fma_f32x2(acc[i][2 * j + 1], x2, bv[j].y);
                         }
                     }
                 }
@@ -267,10 +269,8 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int c = t.n0 + wn * 128 + 32 * j + 4 * ln;
-                    store_row4(row, c, args.N,
-                               make_float4(acc[i][4 * j], acc[i][4 * j + 1], acc[i][4 * j + 2],
-                                           acc[i][4 * j + 3]),
-                               vec);
+                    const float2 lo = f32x2_unpack(acc[i][2 * j]), hi = f32x2_unpack(acc[i][2 * j + 1]);
+                    store_row4(row, c, args.N, make_float4(lo.x, lo.y, hi.x, hi.y), vec);
                 }
             }
         }

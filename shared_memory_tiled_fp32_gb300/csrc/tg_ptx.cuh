@@ -286,6 +286,28 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// ------------------------------------------------------ packed fp32 FMA
+
+// {x, x} as one 64-bit register pair.
+__device__ __forceinline__ unsigned long long f32x2_splat(float x) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+    return r;
+}
+
+// Element-wise fma of two packed fp32 pairs, round to nearest: c.lo = a.lo*b.lo
+// + c.lo, c.hi = a.hi*b.hi + c.hi (the same results as two fmaf).
+__device__ __forceinline__ void fma_f32x2(unsigned long long& c, unsigned long long a,
+                                          unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ float2 f32x2_unpack(unsigned long long v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
 // --------------------------------------------------------------- tf32
 
 // Round a float to tf32 (10 explicit mantissa bits), nearest with ties away
