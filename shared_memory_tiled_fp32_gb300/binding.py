@@ -76,6 +76,8 @@ class PlanInfo(ctypes.Structure):
         ("launches", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("pair", ctypes.c_int),
+        ("tail_units", ctypes.c_longlong),
+        ("tail_split", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

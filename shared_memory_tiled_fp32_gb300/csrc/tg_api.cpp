@@ -83,6 +83,8 @@ void fill_info(const Plan& p, tg_plan_info* out) {
     out->launches = p.launches;
     out->workspace_bytes = p.ws_bytes;
     out->pair = p.pair;
+    out->tail_units = p.tail_units;
+    out->tail_split = p.tail_split;
 }
 
 }  // namespace

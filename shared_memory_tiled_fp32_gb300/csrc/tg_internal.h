@@ -31,6 +31,11 @@ struct Plan {
     int tiles_m = 0, tiles_n = 0;
     int pair = 1;        // 3xTF32: CTAs per cluster sharing one B tile (TMA multicast)
     long long units = 0; // work units (a unit is `pair` vertically adjacent tiles x one K slice)
+    // last-round balancing: the tile units past full_units are each cut into
+    // tail_split K slices (partials in the workspace, then a tail reduce)
+    long long full_units = 0;
+    int tail_split = 1;
+    long long tail_units = 0;
     int grid = 0;
     int num_sms = 0;     // SMs planned for
     int nkb = 0;         // K blocks of bk
@@ -39,7 +44,7 @@ struct Plan {
     bool pack_a = false, pack_b = false;  // FFMA: copy an operand to a 16-byte-pitched buffer
     bool vec_c = false;  // C rows start on 16-byte boundaries
     // workspace layout (byte offsets; a region absent from the plan has size 0)
-    size_t off_a0 = 0, off_a1 = 0, off_b0 = 0, off_b1 = 0, off_part = 0;
+    size_t off_a0 = 0, off_a1 = 0, off_b0 = 0, off_b1 = 0, off_part = 0, off_tail = 0;
     long long ldp = 0;           // partial-product row stride (elements)
     long long part_stride = 0;   // elements between two K-slice partials
     size_t ws_bytes = 0;

@@ -53,36 +53,67 @@ struct GemmArgs {
     long long ldo;           // row stride of `out`
     long long slice_stride;  // elements between K-slice partials
     int vec_out;             // rows of `out` start on 16-byte boundaries
+    // last-round balancing: units >= full_units are the remaining tile units,
+    // each cut into tail_split K slices whose partials go to `tail`
+    // ([slot][pair*BM][BN] floats, slot = unit offset * tail_split + slice)
+    long long full_units;
+    int tail_split;
+    float* tail;
     uint64_t timeout_ns;
 };
 
 struct Unit {
     int m0, n0, kb0, kb1;
     float* out;
+    long long ldo;
 };
 
-// Work unit u -> (K slice, output tile).  Tiles are visited in groups of
-// kGroupM tile rows, column by column inside a group, so CTAs running at the
-// same time share A rows and B columns in L2.  With pair = 2 a unit is two
-// vertically adjacent tiles; the CTA of cluster rank `rank` takes tile row
-// 2*row + rank.
+// Tile-unit index t (K slices aside) -> (tile-unit row, tile column).  Tiles
+// are visited in groups of kGroupM tile-unit rows, column by column inside a
+// group, so CTAs running at the same time share A rows and B columns in L2.
 constexpr int kGroupM = 8;
 
+__host__ __device__ __forceinline__ void unit_tile(int tiles_m, int tiles_n, long long t, int* tm,
+                                                   int* tn) {
+    const long long per_group = (long long)kGroupM * tiles_n;
+    const int g = (int)(t / per_group);
+    const int first_m = g * kGroupM;
+    const int gm = min(tiles_m - first_m, kGroupM);
+    const int r = (int)(t - g * per_group);
+    *tm = first_m + r % gm;
+    *tn = r / gm;
+}
+
+// Work unit u -> (K slice, output tile).  With pair = 2 a unit is two
+// vertically adjacent tiles; the CTA of cluster rank `rank` takes tile row
+// 2*row + rank.  Units below full_units cover their whole K range (or one of
+// `split` K slices); the units after them are the last round's tile units cut
+// into tail_split K slices each.
 __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int rank, int BM, int BN) {
     const long long tiles = (long long)a.tiles_m * a.tiles_n;
-    const int s = (int)(u / tiles);
-    const int t = (int)(u - (long long)s * tiles);
-    const int per_group = kGroupM * a.tiles_n;
-    const int g = t / per_group;
-    const int first_m = g * kGroupM;
-    const int gm = min(a.tiles_m - first_m, kGroupM);
-    const int r = t - g * per_group;
     Unit x;
-    x.m0 = ((first_m + r % gm) * a.pair + rank) * BM;
-    x.n0 = (r / gm) * BN;
+    int tm, tn;
+    if (a.tail_split > 1 && u >= a.full_units) {
+        const long long v = u - a.full_units;
+        const int s = (int)(v % a.tail_split);
+        unit_tile(a.tiles_m, a.tiles_n, a.full_units + v / a.tail_split, &tm, &tn);
+        x.m0 = (tm * a.pair + rank) * BM;
+        x.n0 = tn * BN;
+        x.kb0 = (int)((long long)s * a.nkb / a.tail_split);
+        x.kb1 = (int)((long long)(s + 1) * a.nkb / a.tail_split);
+        // this slot's [pair*BM][BN] block, addressed with global row/column
+        x.ldo = BN;
+        x.out = a.tail + v * ((long long)a.pair * BM * BN) - (long long)tm * a.pair * BM * BN - x.n0;
+        return x;
+    }
+    const int s = (int)(u / tiles);
+    unit_tile(a.tiles_m, a.tiles_n, u - (long long)s * tiles, &tm, &tn);
+    x.m0 = (tm * a.pair + rank) * BM;
+    x.n0 = tn * BN;
     x.kb0 = (int)((long long)s * a.nkb / a.split);
     x.kb1 = (int)((long long)(s + 1) * a.nkb / a.split);
     x.out = a.out + (long long)s * a.slice_stride;
+    x.ldo = a.ldo;
     return x;
 }
 
@@ -265,7 +296,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
         for (int i = 0; i < 8; ++i) {
             const int r = t.m0 + wm * 32 + lm + 4 * i;
             if (r < args.M) {
-                float* row = t.out + (long long)r * args.ldo;
+                float* row = t.out + (long long)r * t.ldo;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int c = t.n0 + wn * 128 + 32 * j + 4 * ln;
@@ -509,7 +540,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             // guarded store of this thread's row segment (row-contiguous 512 B)
             const int grow = t.m0 + q * 32 + lane;
             if (grow < args.M) {
-                float* row = t.out + (long long)grow * args.ldo;
+                float* row = t.out + (long long)grow * t.ldo;
                 const int col0 = t.n0 + h * 128;
 #pragma unroll
                 for (int v = 0; v < 32; ++v)
@@ -669,6 +700,36 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Last-round tile units: C = sum of their tail_split K-slice partials, in
+// slice order (deterministic), float4 per thread.
+__global__ void __launch_bounds__(256)
+    tail_reduce_kernel(GemmArgs a, float* C, long long ldc, int BM, int BN, int vec_c) {
+    const long long tail_units = (a.units - a.full_units) / a.tail_split;
+    const int rows = a.pair * BM, q4 = BN / 4;
+    const long long block = (long long)rows * BN;
+    const long long total = tail_units * rows * q4;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long q = i / ((long long)rows * q4);
+        const int rem = (int)(i - q * rows * q4);
+        const int r = rem / q4, c = (rem % q4) * 4;
+        int tm, tn;
+        unit_tile(a.tiles_m, a.tiles_n, a.full_units + q, &tm, &tn);
+        const int m = tm * rows + r, n = tn * BN + c;
+        if (m >= a.M || n >= a.N) continue;
+        const float* p = a.tail + q * a.tail_split * block + (long long)r * BN + c;
+        float4 s = *reinterpret_cast<const float4*>(p);
+        for (int t = 1; t < a.tail_split; ++t) {
+            const float4 v = *reinterpret_cast<const float4*>(p + t * block);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        store_row4(C + (long long)m * ldc, n, a.N, s, vec_c != 0);
+    }
+}
+
 // K == 0: the empty sum.
 __global__ void __launch_bounds__(256) fill_zero_kernel(float* C, long long ldc, int M, int N) {
     const long long total = (long long)M * N;
@@ -814,6 +875,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     ga.split = p.split;
     ga.nkb = p.nkb;
     ga.units = p.units;
+    ga.full_units = p.full_units;
+    ga.tail_split = p.tail_split;
+    ga.tail = p.tail_split > 1 ? reinterpret_cast<float*>(w + p.off_tail) : nullptr;
     ga.timeout_ns = default_timeout_ns();
     if (p.split > 1) {
         ga.out = reinterpret_cast<float*>(w + p.off_part);
@@ -917,6 +981,12 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
     }
 
+    if (p.tail_split > 1) {
+        const long long work = p.tail_units * p.pair * p.bm * (p.bn / 4);
+        tail_reduce_kernel<<<elementwise_grid(work, 256), 256, 0, stream>>>(ga, C, p.ldc, p.bm, p.bn,
+                                                                           p.vec_c ? 1 : 0);
+        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+    }
     if (p.split > 1) {
         const long long work = (long long)p.M * ((p.N + 3) / 4);
         splitk_reduce_kernel<<<elementwise_grid(work, 256), 256, 0, stream>>>(

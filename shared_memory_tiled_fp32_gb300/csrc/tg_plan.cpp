@@ -107,6 +107,27 @@ void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int l
     p->pair = (p->path == TG_PATH_TF32X3 && p->tiles_m >= 2 && num_sms >= 2 && !pair_off) ? 2 : 1;
     p->units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n * S;
     p->grid = p->pair * (int)std::min<long long>(p->units, num_sms / p->pair);
+    p->full_units = p->units;
+
+    // Last-round balancing.  When the units do not divide into whole rounds of
+    // the resident CTAs (or pairs), the last round would leave most of them
+    // idle; instead its tile units are cut into tail_split K slices (at most
+    // 4, each at least 8 K blocks), so more CTAs share the last round.  Only
+    // with the automatic split and no K split.
+    const long long lanes = p->grid / p->pair;  // units in flight at once
+    if (split_k == 0 && S == 1 && p->units > lanes) {
+        const long long rem = p->units % lanes;
+        if (rem > 0 && 2 * rem <= lanes) {
+            int ts = (int)std::min<long long>(lanes / rem, 4);
+            while (ts > 1 && p->nkb < 8 * ts) --ts;
+            if (ts > 1) {
+                p->full_units = p->units - rem;
+                p->tail_units = rem;
+                p->tail_split = ts;
+                p->units = p->full_units + rem * ts;
+            }
+        }
+    }
 
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -135,9 +156,11 @@ void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int l
         p->part_stride = (long long)M * p->n4;
         p->off_part = take(4ull * S * M * p->n4);
     }
+    if (p->tail_split > 1)
+        p->off_tail = take(4ull * p->tail_units * p->tail_split * p->pair * p->bm * p->bn);
     p->ws_bytes = off;
     const bool prepass = p->path == TG_PATH_TF32X3 || p->pack_a || p->pack_b;
-    p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0);
+    p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_split > 1 ? 1 : 0);
 }
 
 }  // namespace tg

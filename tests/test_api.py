@@ -70,9 +70,16 @@ def test_plan_tiles_split_and_workspace():
     sms = 152
     p = tg.plan(8192, 8192, 8192, num_sms=sms)
     assert (p["path"], p["tiles_m"], p["tiles_n"], p["split_k"]) == ("tf32x3", 64, 32, 1)
-    # pairs of vertically adjacent tiles share B (cluster of 2 CTAs)
-    assert p["pair"] == 2 and p["grid"] == sms and p["units"] == 32 * 32 and p["launches"] == 2
-    assert p["workspace_bytes"] == 4 * 8192 * 8192 * 4  # A_hi, A_lo, B_hi^T, B_lo^T
+    # pairs of vertically adjacent tiles share B (cluster of 2 CTAs); 1024 pair
+    # units on 76 pairs leave 36 for a last round, which is cut into 2 K slices
+    assert p["pair"] == 2 and p["grid"] == sms and p["launches"] == 3
+    assert (p["tail_units"], p["tail_split"]) == (36, 2)
+    assert p["units"] == (32 * 32 - 36) + 36 * 2
+    # A_hi, A_lo, B_hi^T, B_lo^T, plus the tail partials: 36 units x 2 slices x 256 x 256
+    assert p["workspace_bytes"] == 4 * 8192 * 8192 * 4 + 36 * 2 * 256 * 256 * 4
+    # an explicit split turns the last-round balancing off
+    q = tg.plan(8192, 8192, 8192, num_sms=sms, split_k=1)
+    assert q["tail_units"] == 0 and q["units"] == 1024 and q["launches"] == 2
     # ragged: ceil(777/128) x ceil(1029/256) tiles, split to fill the SMs
     p = tg.plan(777, 1029, 513, num_sms=sms)
     assert (p["tiles_m"], p["tiles_n"]) == (7, 5)

@@ -47,7 +47,7 @@ CASES = [
     ("ragged_777x1029x513", "tf32x3", 0), ("ragged_777x1029x513", "tf32x3", 1),
     ("ragged_777x1029x513", "tf32x3", 3), ("ragged_777x1029x513", "ffma", 0),
     ("ragged_777x1029x513", "ffma", 1),
-    ("sq4096_uniform", "tf32x3", 0), ("sq4096_uniform", "ffma", 0),
+    ("sq4096_uniform", "tf32x3", 0), ("sq4096_uniform", "tf32x3", 1), ("sq4096_uniform", "ffma", 0),
     ("sq4096_int", "tf32x3", 0), ("sq4096_int", "ffma", 0),
     ("sq8192_normal", "tf32x3", 0), ("sq8192_normal", "ffma", 0),
     ("longk_2048x2048x16384_normal", "tf32x3", 0), ("longk_2048x2048x16384_normal", "tf32x3", 2),
