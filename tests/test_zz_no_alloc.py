@@ -54,9 +54,9 @@ def test_noalloc_matches_allocating_entry(lib, M, N, K):
 
 def test_noalloc_rejects_oversized_products(lib):
     limit = 64 << 20
-    M = N = 4096
-    K = 2048  # hi/lo copies: 8 * (M + N) * K = 128 MiB > 64 MiB
-    assert 8 * (M + N) * K > limit
+    M, N = 512, 8192
+    K = 2048  # B's hi/lo copies alone: 8 * N * K = 128 MiB > 64 MiB
+    assert 8 * N * K > limit
     A = torch.empty(M, K, device="cuda")
     B = torch.empty(K, N, device="cuda")
     C = torch.empty(M, N, device="cuda")
