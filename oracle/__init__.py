@@ -55,6 +55,9 @@ def _declare(lib):
     lib.tg_oracle_sgemm.restype = ctypes.c_int
     lib.tg_oracle_sgemm_rows.argtypes = [i64, fp, i64, i64, i64, fp, i64, fp, i64, fp, i64]
     lib.tg_oracle_sgemm_rows.restype = ctypes.c_int
+    lib.tg_oracle_sgemm_general.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, ctypes.c_float, fp, i64,
+                                            fp, i64, ctypes.c_float, fp, i64]
+    lib.tg_oracle_sgemm_general.restype = ctypes.c_int
     lib.tg_oracle_threads.argtypes = []
     lib.tg_oracle_threads.restype = ctypes.c_int
     return lib
@@ -105,6 +108,27 @@ def sgemm_rows(A: np.ndarray, B: np.ndarray, rows, lib=None) -> np.ndarray:
     if rc != 0:
         raise RuntimeError(f"tg_oracle_sgemm_rows failed with code {rc}")
     return out
+
+
+def sgemm_general(op_a: int, op_b: int, alpha: float, A: np.ndarray, B: np.ndarray, beta: float,
+                  C: np.ndarray, lib=None) -> np.ndarray:
+    """C = alpha * op(A) @ op(B) + beta * C in place (op = transpose when the
+    flag is 1); A and B are the stored matrices.  Returns C."""
+    lib = lib or load()
+    A, lda = _as_rowmajor_f32(A, "A")
+    B, ldb = _as_rowmajor_f32(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if op_a else A.shape
+    Kb, N = (B.shape[1], B.shape[0]) if op_b else B.shape
+    if Kb != K:
+        raise ValueError("inner dimensions differ")
+    Cv, ldc = _as_rowmajor_f32(C, "C")
+    if Cv is not C or C.shape != (M, N):
+        raise ValueError("C must be an (M, N) float32 array with unit column stride")
+    rc = lib.tg_oracle_sgemm_general(int(op_a), int(op_b), M, N, K, float(alpha), A.ctypes.data, lda,
+                                     B.ctypes.data, ldb, float(beta), C.ctypes.data, ldc)
+    if rc != 0:
+        raise RuntimeError(f"tg_oracle_sgemm_general failed with code {rc}")
+    return C
 
 
 def threads(lib=None) -> int:

@@ -38,7 +38,8 @@
  * Parity status: every entry point here is pinned by tests/test_oracle.py
  * (hand-worked products, identities, permutations, the transpose law, exact
  * rational brute force, closed forms, zero-padding invariance and integer
- * exactness).
+ * exactness; for the general form also alpha/beta closed forms, stored
+ * transposes and exact rational brute force).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -121,6 +122,53 @@ int tg_oracle_sgemm_rows(int64_t nrows, const int64_t* rows, int64_t M,
         free(acc);
     }
     return failed ? 2 : 0;
+}
+
+/*
+ * General form: C = alpha * op(A) * op(B) + beta * C.
+ *
+ * op(A) is M x K: A is stored M x K (lda >= K) when op_a == 0 and K x M
+ * (lda >= M) when op_a == 1 (transposed); op(B) is K x N: B is stored K x N
+ * (ldb >= N) when op_b == 0 and N x K (ldb >= K) when op_b == 1.  These are
+ * the shapes of the backward products of a fully connected layer
+ * ("PMPP 단권화", deep-learning chapter: FC layer = GEMM; dW = X^T dY and
+ * dX = dY W^T).  Per element, in double: s = sum_k op(A)[i][k] op(B)[k][j]
+ * (k ascending, from +0.0), r = alpha * s + beta * C[i][j], rounded once to
+ * float.  When beta == 0, C is not read (it may hold NaN), as in BLAS.
+ * K == 0 gives r = beta * C[i][j] (the empty sum).
+ */
+static int bad_general(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc) {
+    if (op_a < 0 || op_a > 1 || op_b < 0 || op_b > 1) return 1;
+    if (M < 0 || N < 0 || K < 0) return 1;
+    const int64_t a_row = op_a ? M : K, b_row = op_b ? K : N;
+    if (lda < (a_row > 1 ? a_row : 1)) return 1;
+    if (ldb < (b_row > 1 ? b_row : 1)) return 1;
+    if (ldc < (N > 1 ? N : 1)) return 1;
+    return 0;
+}
+
+int tg_oracle_sgemm_general(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                            float alpha, const float* A, int64_t lda,
+                            const float* B, int64_t ldb, float beta, float* C,
+                            int64_t ldc) {
+    if (bad_general(op_a, op_b, M, N, K, lda, ldb, ldc)) return 1;
+    if (M == 0 || N == 0) return 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = op_a ? (double)A[k * lda + i] : (double)A[i * lda + k];
+                const double b = op_b ? (double)B[j * ldb + k] : (double)B[k * ldb + j];
+                s += a * b;
+            }
+            double r = (double)alpha * s;
+            if (beta != 0.0f) r += (double)beta * (double)C[i * ldc + j];
+            C[i * ldc + j] = (float)r;
+        }
+    }
+    return 0;
 }
 
 /* Number of threads the two entry points above use. */

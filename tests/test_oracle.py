@@ -38,7 +38,7 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 # ---------------------------------------------------------------- helpers
 
 
-def read_golden(name):
+def read_golden(name, tags=("A", "B", "C")):
     mats = {}
     with open(os.path.join(GOLDEN, name)) as f:
         lines = [ln.strip() for ln in f if ln.strip() and not ln.lstrip().startswith("#")]
@@ -49,7 +49,7 @@ def read_golden(name):
         rows = [[float(v) for v in lines[i + 1 + k].split()] for k in range(r)]
         mats[tag] = np.array(rows, dtype=np.float32).reshape(r, c)
         i += 1 + r
-    return mats["A"], mats["B"], mats["C"]
+    return tuple(mats[t] for t in tags)
 
 
 def bits(x):
@@ -260,9 +260,82 @@ def pin_rows_entry(lib):
     assert ulp_distance(oracle.sgemm_rows(A, B, rows, lib=lib), want).max() <= 1
 
 
+# ------------------------------------------------- general form (op, alpha, beta)
+
+
+def general(lib, op_a, op_b, alpha, A, B, beta, C0):
+    C = np.array(C0, dtype=np.float32, copy=True)
+    return oracle.sgemm_general(op_a, op_b, alpha, A, B, beta, C, lib=lib)
+
+
+def pin_general_hand_worked(lib):
+    A, B, C0, C = read_golden("hand_general_2x2.txt", ("A", "B", "C0", "C"))
+    assert_bitexact(general(lib, 1, 0, 2.0, A, B, -0.5, C0), C, "hand general")
+
+
+def pin_general_reduces_and_transposes(lib):
+    """op N/N with alpha 1, beta 0 is the plain product; storing A or B
+    transposed and flagging it gives the same bits; alpha = 2^e scales exactly."""
+    rng = np.random.default_rng(31)
+    for (M, N, K) in [(5, 7, 9), (17, 3, 40), (1, 1, 1)]:
+        A = rand_f32(rng, (M, K))
+        B = rand_f32(rng, (K, N))
+        ref = oracle.sgemm(A, B, lib=lib)
+        junk = np.full((M, N), np.nan, np.float32)
+        assert_bitexact(general(lib, 0, 0, 1.0, A, B, 0.0, junk), ref, "N/N")
+        At, Bt = np.ascontiguousarray(A.T), np.ascontiguousarray(B.T)
+        assert_bitexact(general(lib, 1, 0, 1.0, At, B, 0.0, junk), ref, "T/N")
+        assert_bitexact(general(lib, 0, 1, 1.0, A, Bt, 0.0, junk), ref, "N/T")
+        assert_bitexact(general(lib, 1, 1, 1.0, At, Bt, 0.0, junk), ref, "T/T")
+        assert_bitexact(general(lib, 0, 0, 4.0, A, B, 0.0, junk), 4 * ref, "alpha=4")
+        assert_bitexact(general(lib, 1, 1, -0.25, At, Bt, 0.0, junk), -0.25 * ref, "alpha=-1/4")
+
+
+def pin_general_alpha_beta_closed_forms(lib):
+    rng = np.random.default_rng(32)
+    M, N, K = 6, 5, 11
+    A, B = rand_f32(rng, (M, K)), rand_f32(rng, (K, N))
+    C0 = rand_f32(rng, (M, N), -3, 3)
+    assert_bitexact(general(lib, 0, 0, 0.0, A, B, 1.0, C0), C0 + np.float32(0.0), "alpha=0 beta=1")
+    assert_bitexact(general(lib, 0, 0, 0.0, A, B, -2.0, C0), -2 * C0 + np.float32(0.0), "alpha=0 beta=-2")
+    # beta = 0 never reads C: NaN there has no effect
+    assert_bitexact(general(lib, 0, 0, 1.0, A, B, 0.0, np.full((M, N), np.nan, np.float32)),
+                    oracle.sgemm(A, B, lib=lib), "beta=0 ignores C")
+    # K = 0: the empty sum, C = beta * C0
+    assert_bitexact(general(lib, 0, 0, 3.0, np.zeros((M, 0), np.float32), np.zeros((0, N), np.float32),
+                            0.5, C0), 0.5 * C0 + np.float32(0.0), "K=0")
+
+
+def pin_general_brute_force_exact(lib):
+    """Few-bit values: alpha*sum + beta*c is exact in double, so the oracle
+    equals the single correct rounding of the exact rational result."""
+    rng = random.Random(33)
+
+    def val(lo=-6, hi=6):
+        return rng.choice([-1, 1]) * rng.randint(0, 255) * 2.0 ** rng.randint(lo, hi)
+
+    for _ in range(40):
+        M, N, K = rng.randint(1, 4), rng.randint(1, 4), rng.randint(0, 5)
+        op_a, op_b = rng.randint(0, 1), rng.randint(0, 1)
+        alpha, beta = val(-3, 3), rng.choice([0.0, val(-3, 3)])
+        A = np.array([[val() for _ in range(K)] for _ in range(M)], dtype=np.float32).reshape(M, K)
+        B = np.array([[val() for _ in range(N)] for _ in range(K)], dtype=np.float32).reshape(K, N)
+        C0 = np.array([[val() for _ in range(N)] for _ in range(M)], dtype=np.float32)
+        exact = exact_product(A, B) if K > 0 else [[Fraction(0)] * N for _ in range(M)]
+        want = np.array([[round_fraction_to_f32(Fraction(float(np.float32(alpha))) * exact[i][j]
+                                                + Fraction(float(np.float32(beta))) * f32_to_fraction(C0[i, j]))
+                          for j in range(N)] for i in range(M)], dtype=np.float32)
+        As = np.ascontiguousarray(A.T) if op_a else A
+        Bs = np.ascontiguousarray(B.T) if op_b else B
+        got = general(lib, op_a, op_b, alpha, As.reshape(As.shape), Bs.reshape(Bs.shape), beta, C0)
+        assert_bitexact(got + np.float32(0.0), want + np.float32(0.0), f"general brute force {M}x{N}x{K}")
+
+
 PINS = [pin_hand_worked, pin_identity, pin_permutation, pin_transpose_law, pin_brute_force_exact,
         pin_brute_force_random, pin_closed_forms, pin_zero_padding, pin_integer_exact,
-        pin_float64_library, pin_strides_and_edges, pin_rows_entry]
+        pin_float64_library, pin_strides_and_edges, pin_rows_entry, pin_general_hand_worked,
+        pin_general_reduces_and_transposes, pin_general_alpha_beta_closed_forms,
+        pin_general_brute_force_exact]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -316,6 +389,14 @@ MUTANTS = {
     "c_row_stride": ("B, ldb, acc, C + i * ldc);", "B, ldb, acc, C + i * N);"),
     "transposed_A": ("const double a = (double)A_row[k];", "const double a = (double)A_row[k * 0] * (k + 1 > 0);"),
     "drop_last_column": ("for (int64_t j = 0; j < N; ++j) acc[j] += a", "for (int64_t j = 0; j + 1 < N; ++j) acc[j] += a"),
+    "general_a_not_transposed": ("const double a = op_a ? (double)A[k * lda + i] : (double)A[i * lda + k];",
+                                 "const double a = (double)A[i * lda + k];"),
+    "general_b_not_transposed": ("const double b = op_b ? (double)B[j * ldb + k] : (double)B[k * ldb + j];",
+                                 "const double b = (double)B[k * ldb + j];"),
+    "general_alpha_dropped": ("double r = (double)alpha * s;", "double r = s;"),
+    "general_beta_sign": ("if (beta != 0.0f) r += (double)beta", "if (beta != 0.0f) r -= (double)beta"),
+    "general_reads_c_at_beta0": ("if (beta != 0.0f) r += (double)beta * (double)C[i * ldc + j];",
+                                 "r += (double)beta * (double)C[i * ldc + j];"),
     "truncating_store": ("for (int64_t j = 0; j < N; ++j) C_row[j] = (float)acc[j];",
                          "for (int64_t j = 0; j < N; ++j) { float f = (float)acc[j]; if ((double)f - acc[j] > 0 && f > 0) f = nextafterf(f, 0.0f); else if ((double)f - acc[j] < 0 && f < 0) f = nextafterf(f, 0.0f); C_row[j] = f; }"),
 }
