@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--path", default="auto", choices=["auto", "tf32x3", "ffma"])
     ap.add_argument("--split-k", type=int, default=0)
+    ap.add_argument("--op-a", default="N", choices=["N", "T"], help="A stored transposed (K x M)")
+    ap.add_argument("--op-b", default="N", choices=["N", "T"], help="B stored transposed (N x K)")
+    ap.add_argument("--alpha", type=float, default=1.0)
+    ap.add_argument("--beta", type=float, default=0.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -263,13 +267,26 @@ def main():
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = torch.empty(w.M, w.N, device=dev)
     stream = torch.cuda.current_stream(dev)
-    plan = tg.plan(w.M, w.N, w.K, A=Ad.data_ptr(), B=Bd.data_ptr(), C=Cd.data_ptr(), path=args.path,
-                   split_k=args.split_k)
+    general = args.op_a == "T" or args.op_b == "T" or args.alpha != 1.0 or args.beta != 0.0
+    trans_a, trans_b = args.op_a == "T", args.op_b == "T"
+    # the general form's operands as stored (transposed copies of the same data)
+    As = Ad.t().contiguous() if trans_a else Ad
+    Bs = Bd.t().contiguous() if trans_b else Bd
+    if args.beta != 0.0:
+        Cd.normal_(generator=torch.Generator(device=dev).manual_seed(w.seed + 77))
+    plan = tg.plan_general(trans_a, trans_b, w.M, w.N, w.K, As.stride(0), Bs.stride(0), Cd.stride(0),
+                           A=As.data_ptr(), B=Bs.data_ptr(), C=Cd.data_ptr(), path=args.path,
+                           split_k=args.split_k)
     ws = torch.empty(max(1, plan["workspace_bytes"] // 4 + 64), device=dev)
 
     def step(ev0=None, ev1=None):
-        tg.matmul(Ad, Bd, out=Cd, path=args.path, split_k=args.split_k, workspace=ws,
-                  main_begin=ev0, main_end=ev1, stream=stream)
+        if general:
+            tg.matmul_general(As, Bs, Cd, trans_a=trans_a, trans_b=trans_b, alpha=args.alpha, beta=args.beta,
+                              path=args.path, split_k=args.split_k, workspace=ws, stream=stream,
+                              main_begin=ev0, main_end=ev1)
+        else:
+            tg.matmul(Ad, Bd, out=Cd, path=args.path, split_k=args.split_k, workspace=ws,
+                      main_begin=ev0, main_end=ev1, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -309,16 +326,19 @@ def main():
     ms_per_step = elapsed_ms / args.steps
     value = job_tflops(w.flop, world, ms_per_step)
 
-    # end to end through the host-buffer entry point (pinned memory)
-    Ap, Bp = A.pin_memory(), B.pin_memory()
-    Cp = torch.empty(w.M, w.N).pin_memory()
-    tg.sgemm_host(Ap, Bp, Cp, path=args.path, split_k=args.split_k)
-    e2e_times = []
-    for _ in range(args.e2e_steps):
-        t0 = time.perf_counter()
+    # end to end through the host-buffer entry point (pinned memory; the
+    # untransposed product, which is what that entry point computes)
+    e2e_s = None
+    if args.e2e_steps > 0 and not general:
+        Ap, Bp = A.pin_memory(), B.pin_memory()
+        Cp = torch.empty(w.M, w.N).pin_memory()
         tg.sgemm_host(Ap, Bp, Cp, path=args.path, split_k=args.split_k)
-        e2e_times.append(time.perf_counter() - t0)
-    e2e_s = float(np.mean(e2e_times))
+        e2e_times = []
+        for _ in range(args.e2e_steps):
+            t0 = time.perf_counter()
+            tg.sgemm_host(Ap, Bp, Cp, path=args.path, split_k=args.split_k)
+            e2e_times.append(time.perf_counter() - t0)
+        e2e_s = float(np.mean(e2e_times))
 
     if rank != 0:
         if world > 1:
@@ -346,7 +366,7 @@ def main():
     # correctness and the CPU baseline on the same seeded row sample
     cpu = None
     max_rel = None
-    if not args.no_cpu:
+    if not args.no_cpu and not general:
         rows, ref, cpu = cpu_baseline(w, A.numpy(), B.numpy(), args.cpu_seconds)
         got = Cd[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
         r64 = ref.astype(np.float64)
@@ -381,14 +401,17 @@ def main():
                    "tile": [plan["block_m"], plan["block_n"], plan["block_k"]],
                    "l2": "inputs larger than L2 (A+B = %d MiB, pre-pass copies %d MiB)"
                          % (4 * (w.M * w.K + w.K * w.N) >> 20, plan["workspace_bytes"] >> 20),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"op_a": args.op_a, "op_b": args.op_b, "alpha": args.alpha, "beta": args.beta}
+                      if general else {})},
         "roofline": {"bound": bound, "achieved": math_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": math_tflops / peak, "traffic": traffic, "peak_source": peak_note,
                      "kernel": kernel_tag, "kernel_ms": main_ms},
         "cpu_baseline": cpu,
-        "e2e": {"value": w.flop / e2e_s / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 4 * w.M * w.N,
-                "ms_per_step": e2e_s * 1e3},
+        "e2e": None if e2e_s is None else {
+            "value": w.flop / e2e_s / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 4 * w.M * w.N,
+            "ms_per_step": e2e_s * 1e3},
         "gpu_launches": plan["launches"] * args.steps,
         "max_rel_error": max_rel,
         "clocks": clocks,

@@ -56,6 +56,10 @@ typedef enum tg_status {
     TG_ERR_WORKSPACE_TOO_SMALL = 6 /* caller workspace smaller than tg_sgemm_plan's workspace_bytes */
 } tg_status;
 
+/* Operand form for tg_sgemm_general: TG_OP_N = as stored, TG_OP_T =
+ * transposed (the stored matrix is op(X)^T). */
+typedef enum tg_op { TG_OP_N = 0, TG_OP_T = 1 } tg_op;
+
 /* Math paths.  Both are hand-written sm_103a kernels fed by TMA through an
  * mbarrier pipeline with warp-specialised producer and consumer warps.
  *  - TG_PATH_TF32X3: tensor cores (tcgen05.mma kind::tf32, accumulator in
@@ -116,6 +120,22 @@ tg_status tg_sgemm(int M, int N, int K, const float* A, int lda, const float* B,
 tg_status tg_sgemm_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                       float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts);
 
+/* General form: C = alpha * op(A) * op(B) + beta * C, with op(A) M x K and
+ * op(B) K x N.  A is stored M x K (lda >= max(1,K)) for TG_OP_N and K x M
+ * (lda >= max(1,M)) for TG_OP_T; B is stored K x N (ldb >= max(1,N)) for
+ * TG_OP_N and N x K (ldb >= max(1,K)) for TG_OP_T; all row-major.  These are
+ * the products of a fully connected layer's forward and backward passes
+ * ("PMPP 단권화", deep-learning chapter: FC layer = GEMM, dW = X^T dY,
+ * dX = dY W^T).  When beta == 0, C is not read (it may hold NaN); K == 0 gives
+ * C = beta * C.  alpha and beta are applied in fp32 where C is written
+ * (alpha * sum + beta * C with one fused multiply-add).  tg_sgemm_ex is this
+ * call with TG_OP_N, TG_OP_N, alpha = 1, beta = 0.  Other semantics and
+ * return codes as tg_sgemm_ex, plus TG_ERR_INVALID_VALUE for an op other than
+ * TG_OP_N / TG_OP_T. */
+tg_status tg_sgemm_general(int op_a, int op_b, int M, int N, int K, float alpha, const float* A,
+                           int lda, const float* B, int ldb, float beta, float* C, int ldc,
+                           cudaStream_t stream, const tg_sgemm_opts* opts);
+
 /* Plan a call without launching anything: host arithmetic only.  Pointers
  * may be NULL (then the most conservative alignment is assumed).  num_sms is
  * the SM count to plan for; 0 = query the current device.  path/split_k as in
@@ -124,6 +144,12 @@ tg_status tg_sgemm_ex(int M, int N, int K, const float* A, int lda, const float*
 tg_status tg_sgemm_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
                         const void* C, int ldc, int path, int split_k, int num_sms,
                         tg_plan_info* out);
+
+/* tg_sgemm_plan for tg_sgemm_general's operand forms (op_a, op_b as there;
+ * the leading dimensions refer to the stored matrices). */
+tg_status tg_sgemm_plan_general(int op_a, int op_b, int M, int N, int K, const void* A, int lda,
+                                const void* B, int ldb, const void* C, int ldc, int path,
+                                int split_k, int num_sms, tg_plan_info* out);
 
 /* Workspace bytes tg_sgemm_ex needs for these arguments on the current
  * device (0 on invalid arguments).  Same as tg_sgemm_plan(...).workspace_bytes. */

@@ -12,7 +12,10 @@ from .binding import (  # noqa: F401
     error_site,
     lib,
     matmul,
+    matmul_general,
+    matmul_noalloc,
     plan,
+    plan_general,
     selftest_wait_timeout,
     sgemm_host,
     status_string,

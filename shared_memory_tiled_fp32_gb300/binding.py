@@ -29,7 +29,9 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 EXPORTS = (
     "tg_sgemm",
     "tg_sgemm_ex",
+    "tg_sgemm_general",
     "tg_sgemm_plan",
+    "tg_sgemm_plan_general",
     "tg_sgemm_workspace_bytes",
     "tg_sgemm_host",
     "tg_sgemm_noalloc",
@@ -110,6 +112,11 @@ def lib():
         L.tg_sgemm_noalloc.restype = i
         L.tg_sgemm_plan.argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
         L.tg_sgemm_plan.restype = i
+        f = ctypes.c_float
+        L.tg_sgemm_general.argtypes = [i, i, i, i, i, f, p, i, p, i, f, p, i, vp, ctypes.POINTER(Opts)]
+        L.tg_sgemm_general.restype = i
+        L.tg_sgemm_plan_general.argtypes = [i, i, i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
+        L.tg_sgemm_plan_general.restype = i
         L.tg_sgemm_workspace_bytes.argtypes = [i, i, i, p, i, p, i, p, i, i, i]
         L.tg_sgemm_workspace_bytes.restype = ctypes.c_size_t
         L.tg_sgemm_sync_status.argtypes = [vp]
@@ -155,6 +162,8 @@ def _event_handle(ev):
 def _rowmajor_ld(t, name):
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D")
+    if t.numel() == 0:  # nothing is read: any strides will do
+        return max(t.shape[1], 1)
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must have unit stride along its last dimension")
     return max(t.stride(0) if t.shape[0] > 1 else t.shape[1], t.shape[1], 1)
@@ -200,6 +209,36 @@ def matmul(A, B, out=None, *, path="auto", split_k=0, workspace=None, main_begin
     return out
 
 
+def matmul_general(A, B, C=None, *, trans_a=False, trans_b=False, alpha=1.0, beta=0.0, path="auto",
+                   split_k=0, workspace=None, stream=None, main_begin=None, main_end=None):
+    """C = alpha * op(A) @ op(B) + beta * C for float32 CUDA tensors, where
+    op(X) is X.T when the trans_ flag is set (A and B are the stored
+    matrices).  C is required when beta != 0; it is returned."""
+    import torch
+
+    for name, t in (("A", A), ("B", B)):
+        if t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a float32 CUDA tensor")
+    M, K = (A.shape[1], A.shape[0]) if trans_a else tuple(A.shape)
+    Kb, N = (B.shape[1], B.shape[0]) if trans_b else tuple(B.shape)
+    if Kb != K:
+        raise ValueError("inner dimensions differ")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("C is required when beta != 0")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if C.dtype != torch.float32 or not C.is_cuda or tuple(C.shape) != (M, N):
+        raise ValueError("C must be an (M, N) float32 CUDA tensor")
+    lda, ldb, ldc = _rowmajor_ld(A, "A"), _rowmajor_ld(B, "B"), _rowmajor_ld(C, "C")
+    o = make_opts(path, split_k, workspace, main_begin, main_end)
+    with torch.cuda.device(A.device):
+        st = lib().tg_sgemm_general(int(trans_a), int(trans_b), M, N, K, float(alpha), A.data_ptr(), lda,
+                                    B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc, _stream_handle(stream),
+                                    ctypes.byref(o))
+    _check(st, "tg_sgemm_general")
+    return C
+
+
 def matmul_noalloc(A, B, out, *, stream=None):
     """C = A @ B through tg_sgemm_noalloc: 3xTF32 with the library's fixed
     device scratch array instead of any allocation (``out`` must be given)."""
@@ -243,6 +282,17 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, *, A=0, B=0, C=0, path="auto", s
                              PATHS[path] if isinstance(path, str) else int(path), split_k, num_sms,
                              ctypes.byref(info))
     _check(st, "tg_sgemm_plan")
+    return info.as_dict()
+
+
+def plan_general(trans_a, trans_b, M, N, K, lda, ldb, ldc, *, A=0, B=0, C=0, path="auto", split_k=0,
+                 num_sms=0) -> dict:
+    """What tg_sgemm_general would launch (stored-matrix leading dimensions)."""
+    info = PlanInfo()
+    st = lib().tg_sgemm_plan_general(int(trans_a), int(trans_b), M, N, K, A or None, lda, B or None, ldb,
+                                     C or None, ldc, PATHS[path] if isinstance(path, str) else int(path),
+                                     split_k, num_sms, ctypes.byref(info))
+    _check(st, "tg_sgemm_plan_general")
     return info.as_dict()
 
 

@@ -109,11 +109,11 @@ const char* tg_status_string(tg_status s) {
 
 int tg_sgemm_version(void) { return 100; }
 
-tg_status tg_sgemm_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
-                        const void* C, int ldc, int path, int split_k, int num_sms,
-                        tg_plan_info* out) {
+tg_status tg_sgemm_plan_general(int op_a, int op_b, int M, int N, int K, const void* A, int lda,
+                                const void* B, int ldb, const void* C, int ldc, int path,
+                                int split_k, int num_sms, tg_plan_info* out) {
     if (out == nullptr) return TG_ERR_INVALID_VALUE;
-    tg_status st = validate(M, N, K, A, lda, B, ldb, C, ldc, path, split_k, false);
+    tg_status st = validate(op_a, op_b, M, N, K, A, lda, B, ldb, C, ldc, path, split_k, false);
     if (st != TG_OK) return st;
     if (num_sms <= 0) {
         DeviceState* d = nullptr;
@@ -122,9 +122,16 @@ tg_status tg_sgemm_plan(int M, int N, int K, const void* A, int lda, const void*
         num_sms = d->num_sms;
     }
     Plan p;
-    make_plan(M, N, K, A, lda, B, ldb, C, ldc, path, split_k, num_sms, &p);
+    make_plan(op_a, op_b, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, path, split_k, num_sms, &p);
     fill_info(p, out);
     return TG_OK;
+}
+
+tg_status tg_sgemm_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
+                        const void* C, int ldc, int path, int split_k, int num_sms,
+                        tg_plan_info* out) {
+    return tg_sgemm_plan_general(TG_OP_N, TG_OP_N, M, N, K, A, lda, B, ldb, C, ldc, path, split_k,
+                                 num_sms, out);
 }
 
 size_t tg_sgemm_workspace_bytes(int M, int N, int K, const void* A, int lda, const void* B,
@@ -134,10 +141,11 @@ size_t tg_sgemm_workspace_bytes(int M, int N, int K, const void* A, int lda, con
     return info.workspace_bytes;
 }
 
-tg_status tg_sgemm_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-                      float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts) {
+tg_status tg_sgemm_general(int op_a, int op_b, int M, int N, int K, float alpha, const float* A,
+                           int lda, const float* B, int ldb, float beta, float* C, int ldc,
+                           cudaStream_t stream, const tg_sgemm_opts* opts) {
     const tg_sgemm_opts o = opts ? *opts : default_opts();
-    tg_status st = validate(M, N, K, A, lda, B, ldb, C, ldc, o.path, o.split_k);
+    tg_status st = validate(op_a, op_b, M, N, K, A, lda, B, ldb, C, ldc, o.path, o.split_k);
     if (st != TG_OK) return st;
     if (M == 0 || N == 0) return TG_OK;
     DeviceState* d = nullptr;
@@ -145,7 +153,7 @@ tg_status tg_sgemm_ex(int M, int N, int K, const float* A, int lda, const float*
     if (st != TG_OK) return st;
 
     Plan p;
-    make_plan(M, N, K, A, lda, B, ldb, C, ldc, o.path, o.split_k, d->num_sms, &p);
+    make_plan(op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, o.path, o.split_k, d->num_sms, &p);
     void* ws = nullptr;
     bool owned = false;
     if (p.ws_bytes > 0) {
@@ -166,6 +174,11 @@ tg_status tg_sgemm_ex(int M, int N, int K, const float* A, int lda, const float*
     return st;
 }
 
+tg_status tg_sgemm_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                      float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts) {
+    return tg_sgemm_general(TG_OP_N, TG_OP_N, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, stream, opts);
+}
+
 tg_status tg_sgemm(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                    float* C, int ldc, cudaStream_t stream) {
     return tg_sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
@@ -174,7 +187,7 @@ tg_status tg_sgemm(int M, int N, int K, const float* A, int lda, const float* B,
 tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                         float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts) {
     const tg_sgemm_opts o = opts ? *opts : default_opts();
-    tg_status st = validate(M, N, K, A, lda, B, ldb, C, ldc, o.path, o.split_k);
+    tg_status st = validate(TG_OP_N, TG_OP_N, M, N, K, A, lda, B, ldb, C, ldc, o.path, o.split_k);
     if (st != TG_OK) return st;
     if (M == 0 || N == 0) return TG_OK;
     DeviceState* d = nullptr;

@@ -25,6 +25,8 @@ constexpr size_t kWsAlign = 256;
 struct Plan {
     int M = 0, N = 0, K = 0;
     long long lda = 0, ldb = 0, ldc = 0;
+    int op_a = TG_OP_N, op_b = TG_OP_N;  // stored A / B transposed (TG_OP_T)
+    float alpha = 1.0f, beta = 0.0f;      // C = alpha * op(A) op(B) + beta * C
     int path = TG_PATH_TF32X3;
     int split = 1;
     int bm = 0, bn = 0, bk = 0, stages = 0;
@@ -40,7 +42,7 @@ struct Plan {
     int num_sms = 0;     // SMs planned for
     int nkb = 0;         // K blocks of bk
     int k4 = 0, n4 = 0;  // K and N rounded up to a multiple of 4 (16-byte rows)
-    bool zero_fill = false;  // K == 0: C = 0, nothing else runs
+    bool zero_fill = false;  // K == 0: C = beta * C, nothing else runs
     bool pack_a = false, pack_b = false;  // FFMA: copy an operand to a 16-byte-pitched buffer
     bool vec_c = false;  // C rows start on 16-byte boundaries
     // workspace layout (byte offsets; a region absent from the plan has size 0)
@@ -53,12 +55,13 @@ struct Plan {
 
 // Argument checks of the C ABI (pure host arithmetic).  With need_pointers
 // false (planning only) NULL pointers are accepted and skip the overlap check.
-tg_status validate(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
-                   const void* C, int ldc, int path, int split_k, bool need_pointers = true);
+tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int lda, const void* B,
+                   int ldb, const void* C, int ldc, int path, int split_k, bool need_pointers = true);
 
 // Fill `p` for the given call; num_sms > 0.  Assumes validate() passed.
-void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
-               const void* C, int ldc, int path, int split_k, int num_sms, Plan* p);
+void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
+               const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
+               int num_sms, Plan* p);
 
 // Enqueue every kernel of plan `p` on `stream` (defined in tg_kernels.cu).
 tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, void* ws,

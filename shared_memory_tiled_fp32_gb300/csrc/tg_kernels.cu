@@ -59,6 +59,10 @@ struct GemmArgs {
     long long full_units;
     int tail_split;
     float* tail;
+    // C = alpha * op(A) op(B) + beta * C, applied where C is written (scaled
+    // = 0: a plain store of the product; beta == 0: C is not read)
+    float alpha, beta;
+    int scaled;
     uint64_t timeout_ns;
 };
 
@@ -66,6 +70,7 @@ struct Unit {
     int m0, n0, kb0, kb1;
     float* out;
     long long ldo;
+    bool direct;  // writes C itself (not a partial)
 };
 
 // Tile-unit index t (K slices aside) -> (tile-unit row, tile column).  Tiles
@@ -104,6 +109,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int 
         // this slot's [pair*BM][BN] block, addressed with global row/column
         x.ldo = BN;
         x.out = a.tail + v * ((long long)a.pair * BM * BN) - (long long)tm * a.pair * BM * BN - x.n0;
+        x.direct = false;
         return x;
     }
     const int s = (int)(u / tiles);
@@ -114,6 +120,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int 
     x.kb1 = (int)((long long)(s + 1) * a.nkb / a.split);
     x.out = a.out + (long long)s * a.slice_stride;
     x.ldo = a.ldo;
+    x.direct = a.split == 1;
     return x;
 }
 
@@ -128,6 +135,28 @@ __device__ __forceinline__ void store_row4(float* row, int col, int N, float4 v,
         if (col + 2 < N) row[col + 2] = v.z;
         if (col + 3 < N) row[col + 3] = v.w;
     }
+}
+
+// The final value alpha * v + beta * C of 4 consecutive outputs (C read only
+// when beta != 0), then the guarded store.
+__device__ __forceinline__ void store_row4_scaled(float* row, int col, int N, float4 v, bool vec,
+                                                  float alpha, float beta) {
+    if (beta != 0.0f) {
+        float4 c;
+        if (vec && col + 3 < N) {
+            c = *reinterpret_cast<const float4*>(row + col);
+        } else {
+            c.x = col < N ? row[col] : 0.0f;
+            c.y = col + 1 < N ? row[col + 1] : 0.0f;
+            c.z = col + 2 < N ? row[col + 2] : 0.0f;
+            c.w = col + 3 < N ? row[col + 3] : 0.0f;
+        }
+        v = make_float4(fmaf(alpha, v.x, beta * c.x), fmaf(alpha, v.y, beta * c.y), fmaf(alpha, v.z, beta * c.z),
+                        fmaf(alpha, v.w, beta * c.w));
+    } else {
+        v = make_float4(alpha * v.x, alpha * v.y, alpha * v.z, alpha * v.w);
+    }
+    store_row4(row, col, N, v, vec);
 }
 
 __device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {
@@ -292,6 +321,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 
         // guarded store: 4 rows x 128 contiguous bytes per warp instruction
         const bool vec = args.vec_out != 0;
+        const bool scale = args.scaled != 0 && t.direct;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = t.m0 + wm * 32 + lm + 4 * i;
@@ -301,7 +331,11 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
                 for (int j = 0; j < 4; ++j) {
                     const int c = t.n0 + wn * 128 + 32 * j + 4 * ln;
                     const float2 lo = f32x2_unpack(acc[i][2 * j]), hi = f32x2_unpack(acc[i][2 * j + 1]);
-                    store_row4(row, c, args.N, make_float4(lo.x, lo.y, hi.x, hi.y), vec);
+                    const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    if (scale)
+                        store_row4_scaled(row, c, args.N, v, vec, args.alpha, args.beta);
+                    else
+                        store_row4(row, c, args.N, v, vec);
                 }
             }
         }
@@ -542,10 +576,18 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             if (grow < args.M) {
                 float* row = t.out + (long long)grow * t.ldo;
                 const int col0 = t.n0 + h * 128;
+                if (args.scaled != 0 && t.direct) {
 #pragma unroll
-                for (int v = 0; v < 32; ++v)
-                    store_row4(row, col0 + 4 * v, args.N,
-                               make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]), vec);
+                    for (int v = 0; v < 32; ++v)
+                        store_row4_scaled(row, col0 + 4 * v, args.N,
+                                          make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]),
+                                          vec, args.alpha, args.beta);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 32; ++v)
+                        store_row4(row, col0 + 4 * v, args.N,
+                                   make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]), vec);
+                }
             }
         }
     }
@@ -563,31 +605,36 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 
 // ------------------------------------------------------------ pre-pass
 //
-// SPLIT (3xTF32):  A -> A_hi, A_lo [M][k4];  B -> B_hi^T, B_lo^T [N][k4]
-//   hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32).
-// PACK (FFMA, operand not TMA-legal): A -> [M][k4], B -> [K][n4].
-// Padding columns (k >= K, n >= N) are written as zeros (ghost elements).
-//
-// Memory-bound: the row-wise parts (A always, B when packing) move 4 values
-// per item with 16-byte stores (and 16-byte loads when the source rows are
-// 16-byte aligned), four items in flight per thread.  B's transpose runs on
-// 64 x 64 tiles through a [64][65] shared tile, 16 values per thread in
-// flight; the padded row makes the column read conflict-free ("Bank
+// Lays each operand out K-major for the GEMM kernels, zero-padding columns
+// past the valid extent (ghost elements):
+//   SPLIT (3xTF32): op(A) -> A_hi, A_lo [M][k4];  op(B)^T -> B_hi, B_lo [N][k4];
+//     hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32).
+//   PACK (FFMA, operand not TMA-legal or transposed): op(A) -> [M][k4],
+//     op(B) -> [K][n4].
+// Each operand is either copied row by row (its stored rows already run along
+// the destination rows) or transposed.  Memory-bound: the row-wise pass moves
+// 4 values per item with 16-byte stores (and 16-byte loads when the source
+// rows are 16-byte aligned), four items in flight per thread; the transpose
+// runs on 64 x 64 tiles through a [64][65] shared tile, 16 values per thread
+// in flight; the padded row makes the column read conflict-free ("Bank
 // Conflict", padding: gcd(65, 32) = 1).  Loads and stores are row-coalesced.
 
+struct OperandPass {
+    const float* src;
+    long long ld;    // source row stride (elements)
+    int rows;        // destination rows
+    int cols;        // valid destination columns (source extent)
+    int pitch;       // destination row pitch = padded columns (multiple of 4)
+    int trans;       // 1: dst[r][c] = src[c*ld + r]; 0: dst[r][c] = src[r*ld + c]
+    int vec;         // row-wise only: source rows start on 16-byte boundaries
+    float* d0;       // SPLIT: hi; PACK: copy (nullptr = part not needed)
+    float* d1;       // SPLIT: lo
+    long long items; // row-wise: rows * pitch/4; transpose: 64x64 tiles
+    int tiles_c;     // transpose: 64-wide tiles along the destination columns
+};
+
 struct PrepassArgs {
-    const float* A;
-    long long lda;
-    const float* B;
-    long long ldb;
-    int M, N, K, k4, n4;
-    float* a0;  // SPLIT: A_hi; PACK: copy of A (nullptr = no A part)
-    float* a1;  // SPLIT: A_lo
-    float* b0;  // SPLIT: B_hi^T; PACK: copy of B (nullptr = no B part)
-    float* b1;  // SPLIT: B_lo^T
-    int vec_a, vec_b;  // source rows start on 16-byte boundaries
-    long long a_items, b_items;  // A: M*k4/4; B: K*n4/4 (PACK) or 64x64 tiles (SPLIT)
-    int b_tiles_k;               // SPLIT: 64-wide tiles along k4
+    OperandPass op[2];  // A, then B
 };
 
 __device__ __forceinline__ float4 load_row4(const float* src, long long ld, int row, int col,
@@ -614,63 +661,72 @@ __device__ __forceinline__ void store_split4(float* d0, float* d1, long long o, 
     }
 }
 
-// dst[r][c..c+3] (row pitch cols4) from src[r][c..c+3] (row pitch ld, valid
-// columns < cols, zero beyond), for every 4-column item of rows x cols4.
 template <bool SPLIT>
-__device__ __forceinline__ void rowwise_pass(const float* src, long long ld, int cols, int cols4,
-                                             bool vec, float* d0, float* d1, long long items) {
+__device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
     const long long stride = (long long)gridDim.x * blockDim.x;
-    const int groups = cols4 / 4;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < items; i += 4 * stride) {
+    const int groups = p.pitch / 4;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < p.items; i += 4 * stride) {
         float4 v[4];
         long long o[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const long long it = i + u * stride;
             o[u] = -1;
-            if (it < items) {
+            if (it < p.items) {
                 const int r = (int)(it / groups), c = (int)(it % groups) * 4;
-                v[u] = load_row4(src, ld, r, c, cols, vec);
-                o[u] = (long long)r * cols4 + c;
+                v[u] = load_row4(p.src, p.ld, r, c, p.cols, p.vec != 0);
+                o[u] = (long long)r * p.pitch + c;
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            if (o[u] >= 0) store_split4<SPLIT>(d0, d1, o[u], v[u]);
+            if (o[u] >= 0) store_split4<SPLIT>(p.d0, p.d1, o[u], v[u]);
     }
 }
 
 template <bool SPLIT>
-__global__ void __launch_bounds__(256) prepass_kernel(PrepassArgs p) {
-    __shared__ float tile[64][65];
-    if (p.a0 != nullptr)
-        rowwise_pass<SPLIT>(p.A, p.lda, p.K, p.k4, p.vec_a != 0, p.a0, p.a1, p.a_items);
-    if (p.b0 == nullptr) return;
-    if (!SPLIT) {
-        rowwise_pass<false>(p.B, p.ldb, p.N, p.n4, p.vec_b != 0, p.b0, nullptr, p.b_items);
-        return;
-    }
+__device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*tile)[65]) {
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4 threads
-    for (long long t = blockIdx.x; t < p.b_items; t += gridDim.x) {
-        const int n0 = (int)(t / p.b_tiles_k) * 64, k0 = (int)(t % p.b_tiles_k) * 64;
+    for (long long t = blockIdx.x; t < p.items; t += gridDim.x) {
+        const int r0 = (int)(t / p.tiles_c) * 64, c0 = (int)(t % p.tiles_c) * 64;
+        // source row c, column r: coalesced along r
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const int k = k0 + ty + 4 * j, n = n0 + tx;
-            tile[ty + 4 * j][tx] = (k < p.K && n < p.N) ? p.B[(long long)k * p.ldb + n] : 0.0f;
+            const int c = c0 + ty + 4 * j, r = r0 + tx;
+            tile[ty + 4 * j][tx] = (c < p.cols && r < p.rows) ? p.src[(long long)c * p.ld + r] : 0.0f;
         }
         __syncthreads();
+        // destination row r, column c: coalesced along c
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const int n = n0 + ty + 4 * j, k = k0 + tx;
-            if (n < p.N && k < p.k4) {
+            const int r = r0 + ty + 4 * j, c = c0 + tx;
+            if (r < p.rows && c < p.pitch) {
                 const float x = tile[tx][ty + 4 * j];
-                const float hi = to_tf32(x);
-                const long long o = (long long)n * p.k4 + k;
-                p.b0[o] = hi;
-                p.b1[o] = to_tf32(x - hi);
+                const long long o = (long long)r * p.pitch + c;
+                if (SPLIT) {
+                    const float hi = to_tf32(x);
+                    p.d0[o] = hi;
+                    p.d1[o] = to_tf32(x - hi);
+                } else {
+                    p.d0[o] = x;
+                }
             }
         }
         __syncthreads();
+    }
+}
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(256) prepass_kernel(PrepassArgs a) {
+    __shared__ float tile[64][65];
+#pragma unroll 1
+    for (int k = 0; k < 2; ++k) {
+        const OperandPass& p = a.op[k];
+        if (p.d0 == nullptr) continue;
+        if (p.trans)
+            transpose_pass<SPLIT>(p, tile);
+        else
+            rowwise_pass<SPLIT>(p);
     }
 }
 
@@ -681,7 +737,8 @@ __global__ void __launch_bounds__(256) prepass_kernel(PrepassArgs p) {
 // partials.
 __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ part, long long ldp, long long slice, int S,
-                         float* C, long long ldc, int M, int N, int vec_c) {
+                         float* C, long long ldc, int M, int N, int vec_c, int scaled, float alpha,
+                         float beta) {
     const int n4g = (N + 3) / 4;
     const long long total = (long long)M * n4g;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -696,7 +753,10 @@ __global__ void __launch_bounds__(256)
             s.z += v.z;
             s.w += v.w;
         }
-        store_row4(C + (long long)m * ldc, c, N, s, vec_c != 0);
+        if (scaled)
+            store_row4_scaled(C + (long long)m * ldc, c, N, s, vec_c != 0, alpha, beta);
+        else
+            store_row4(C + (long long)m * ldc, c, N, s, vec_c != 0);
     }
 }
 
@@ -726,16 +786,21 @@ __global__ void __launch_bounds__(256)
             s.z += v.z;
             s.w += v.w;
         }
-        store_row4(C + (long long)m * ldc, n, a.N, s, vec_c != 0);
+        if (a.scaled)
+            store_row4_scaled(C + (long long)m * ldc, n, a.N, s, vec_c != 0, a.alpha, a.beta);
+        else
+            store_row4(C + (long long)m * ldc, n, a.N, s, vec_c != 0);
     }
 }
 
-// K == 0: the empty sum.
-__global__ void __launch_bounds__(256) fill_zero_kernel(float* C, long long ldc, int M, int N) {
+// K == 0: the empty sum, so C = beta * C (C not read when beta == 0).
+__global__ void __launch_bounds__(256) scale_c_kernel(float* C, long long ldc, int M, int N, float beta) {
     const long long total = (long long)M * N;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x)
-        C[(i / N) * ldc + (i % N)] = 0.0f;
+         i += (long long)gridDim.x * blockDim.x) {
+        float* c = C + (i / N) * ldc + (i % N);
+        *c = beta != 0.0f ? beta * *c : 0.0f;
+    }
 }
 
 // Waits on an mbarrier that nothing arrives on; the bounded wait gives up,
@@ -860,8 +925,9 @@ tg_status prepare_device_kernels() {
 tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, void* ws,
                       cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
     if (p.M == 0 || p.N == 0) return TG_OK;
-    if (p.zero_fill) {
-        fill_zero_kernel<<<elementwise_grid((long long)p.M * p.N, 256), 256, 0, stream>>>(C, p.ldc, p.M, p.N);
+    if (p.zero_fill) {  // K == 0: C = beta * C
+        scale_c_kernel<<<elementwise_grid((long long)p.M * p.N, 256), 256, 0, stream>>>(C, p.ldc, p.M, p.N,
+                                                                                       p.beta);
         return last_launch_status();
     }
     uint8_t* w = static_cast<uint8_t*>(ws);
@@ -878,6 +944,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     ga.full_units = p.full_units;
     ga.tail_split = p.tail_split;
     ga.tail = p.tail_split > 1 ? reinterpret_cast<float*>(w + p.off_tail) : nullptr;
+    ga.alpha = p.alpha;
+    ga.beta = p.beta;
+    ga.scaled = (p.alpha != 1.0f || p.beta != 0.0f) ? 1 : 0;
     ga.timeout_ns = default_timeout_ns();
     if (p.split > 1) {
         ga.out = reinterpret_cast<float*>(w + p.off_part);
@@ -891,18 +960,25 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         ga.vec_out = p.vec_c ? 1 : 0;
     }
 
+    // Operand passes of the pre-pass.  A is stored M x K (op N) or K x M
+    // (op T); B is stored K x N (op N) or N x K (op T).
+    auto pass = [](const float* src, long long ld, int rows, int cols, int pitch, bool trans, float* d0,
+                   float* d1) {
+        OperandPass o{};
+        o.src = src;
+        o.ld = ld;
+        o.rows = rows;
+        o.cols = cols;
+        o.pitch = pitch;
+        o.trans = trans ? 1 : 0;
+        o.vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && ld % 4 == 0) ? 1 : 0;
+        o.d0 = d0;
+        o.d1 = d1;
+        o.tiles_c = (pitch + 63) / 64;
+        o.items = trans ? (long long)((rows + 63) / 64) * o.tiles_c : (long long)rows * (pitch / 4);
+        return o;
+    };
     PrepassArgs pa{};
-    pa.A = A;
-    pa.lda = p.lda;
-    pa.B = B;
-    pa.ldb = p.ldb;
-    pa.M = p.M;
-    pa.N = p.N;
-    pa.K = p.K;
-    pa.k4 = p.k4;
-    pa.n4 = p.n4;
-    pa.vec_a = (reinterpret_cast<uintptr_t>(A) % 16 == 0 && p.lda % 4 == 0) ? 1 : 0;
-    pa.vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0 && p.ldb % 4 == 0) ? 1 : 0;
     // one full wave of resident blocks keeps HBM busy without a tail
     const int prepass_grid = g_prepass_blocks_per_sm[p.path == TG_PATH_TF32X3 ? 1 : 0] * p.num_sms;
 
@@ -911,13 +987,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         float* alo = reinterpret_cast<float*>(w + p.off_a1);
         float* bhi = reinterpret_cast<float*>(w + p.off_b0);
         float* blo = reinterpret_cast<float*>(w + p.off_b1);
-        pa.a0 = ahi;
-        pa.a1 = alo;
-        pa.b0 = bhi;
-        pa.b1 = blo;
-        pa.a_items = (long long)p.M * (p.k4 / 4);
-        pa.b_tiles_k = (p.k4 + 63) / 64;
-        pa.b_items = (long long)((p.N + 63) / 64) * pa.b_tiles_k;
+        // A_hi/A_lo [M][k4] from op(A); B_hi/B_lo [N][k4] from op(B)^T
+        pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, ahi, alo);
+        pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k4, p.op_b == TG_OP_N, bhi, blo);
         prepass_kernel<true><<<prepass_grid, 256, 0, stream>>>(pa);
         if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
 
@@ -956,18 +1028,19 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         const float* b_src = B;
         long long a_row = p.lda, b_row = p.ldb;
         if (p.pack_a || p.pack_b) {
-            pa.a0 = p.pack_a ? reinterpret_cast<float*>(w + p.off_a0) : nullptr;
-            pa.b0 = p.pack_b ? reinterpret_cast<float*>(w + p.off_b0) : nullptr;
-            pa.a_items = (long long)p.M * (p.k4 / 4);
-            pa.b_items = (long long)p.K * (p.n4 / 4);
+            // A_pack [M][k4] from op(A); B_pack [K][n4] from op(B)
+            float* ap = p.pack_a ? reinterpret_cast<float*>(w + p.off_a0) : nullptr;
+            float* bp = p.pack_b ? reinterpret_cast<float*>(w + p.off_b0) : nullptr;
+            pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, ap, nullptr);
+            pa.op[1] = pass(B, p.ldb, p.K, p.N, p.n4, p.op_b == TG_OP_T, bp, nullptr);
             prepass_kernel<false><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
             if (p.pack_a) {
-                a_src = pa.a0;
+                a_src = ap;
                 a_row = p.k4;
             }
             if (p.pack_b) {
-                b_src = pa.b0;
+                b_src = bp;
                 b_row = p.n4;
             }
         }
@@ -990,7 +1063,8 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     if (p.split > 1) {
         const long long work = (long long)p.M * ((p.N + 3) / 4);
         splitk_reduce_kernel<<<elementwise_grid(work, 256), 256, 0, stream>>>(
-            ga.out, p.ldp, p.part_stride, p.split, C, p.ldc, p.M, p.N, p.vec_c ? 1 : 0);
+            ga.out, p.ldp, p.part_stride, p.split, C, p.ldc, p.M, p.N, p.vec_c ? 1 : 0, ga.scaled, p.alpha,
+            p.beta);
         if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
     }
     return TG_OK;

@@ -79,7 +79,7 @@ tg_status noalloc_device(NoallocDevice** out) {
 extern "C" tg_status tg_sgemm_noalloc(int M, int N, int K, const float* A, int lda, const float* B,
                                       int ldb, float* C, int ldc, cudaStream_t stream) {
     using namespace tg;
-    tg_status st = validate(M, N, K, A, lda, B, ldb, C, ldc, TG_PATH_TF32X3, 0);
+    tg_status st = validate(TG_OP_N, TG_OP_N, M, N, K, A, lda, B, ldb, C, ldc, TG_PATH_TF32X3, 0);
     if (st != TG_OK) return st;
     if (M == 0 || N == 0) return TG_OK;
     NoallocDevice* d = nullptr;
@@ -87,9 +87,12 @@ extern "C" tg_status tg_sgemm_noalloc(int M, int N, int K, const float* A, int l
     if (st != TG_OK) return st;
 
     Plan p;
-    make_plan(M, N, K, A, lda, B, ldb, C, ldc, TG_PATH_TF32X3, 0, d->num_sms, &p);
-    if (p.ws_bytes > TG_SGEMM_NOALLOC_SCRATCH_BYTES && p.split > 1)  // drop the split partials
-        make_plan(M, N, K, A, lda, B, ldb, C, ldc, TG_PATH_TF32X3, 1, d->num_sms, &p);
+    make_plan(TG_OP_N, TG_OP_N, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, TG_PATH_TF32X3, 0,
+              d->num_sms, &p);
+    if (p.ws_bytes > TG_SGEMM_NOALLOC_SCRATCH_BYTES && (p.split > 1 || p.tail_split > 1))
+        // drop the split and last-round partials
+        make_plan(TG_OP_N, TG_OP_N, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, TG_PATH_TF32X3, 1,
+                  d->num_sms, &p);
     if (p.ws_bytes > TG_SGEMM_NOALLOC_SCRATCH_BYTES) return TG_ERR_WORKSPACE_TOO_SMALL;
     // Nothing in the scratch has to start at zero: the pre-pass writes every
     // hi/lo element it later reads (padding included), and the reduce stores

@@ -29,10 +29,15 @@ bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
 
 }  // namespace
 
-tg_status validate(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
-                   const void* C, int ldc, int path, int split_k, bool need_pointers) {
+tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int lda, const void* B,
+                   int ldb, const void* C, int ldc, int path, int split_k, bool need_pointers) {
+    if (op_a != TG_OP_N && op_a != TG_OP_T) return TG_ERR_INVALID_VALUE;
+    if (op_b != TG_OP_N && op_b != TG_OP_T) return TG_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_VALUE;
-    if (lda < std::max(1, K) || ldb < std::max(1, N) || ldc < std::max(1, N))
+    // stored shapes: A is M x K (op N) or K x M (op T); B is K x N or N x K
+    const int a_rows = op_a == TG_OP_N ? M : K, a_cols = op_a == TG_OP_N ? K : M;
+    const int b_rows = op_b == TG_OP_N ? K : N, b_cols = op_b == TG_OP_N ? N : K;
+    if (lda < std::max(1, a_cols) || ldb < std::max(1, b_cols) || ldc < std::max(1, N))
         return TG_ERR_INVALID_VALUE;
     if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3)
         return TG_ERR_INVALID_VALUE;
@@ -46,17 +51,18 @@ tg_status validate(int M, int N, int K, const void* A, int lda, const void* B, i
     const uintptr_t c1 = c0 + 4ull * ((unsigned long long)(M - 1) * ldc + N);
     if (K > 0) {
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(A);
-        const uintptr_t a1 = a0 + 4ull * ((unsigned long long)(M - 1) * lda + K);
+        const uintptr_t a1 = a0 + 4ull * ((unsigned long long)(a_rows - 1) * lda + a_cols);
         const uintptr_t b0 = reinterpret_cast<uintptr_t>(B);
-        const uintptr_t b1 = b0 + 4ull * ((unsigned long long)(K - 1) * ldb + N);
+        const uintptr_t b1 = b0 + 4ull * ((unsigned long long)(b_rows - 1) * ldb + b_cols);
         if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
             return TG_ERR_INVALID_VALUE;
     }
     return TG_OK;
 }
 
-void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int ldb,
-               const void* C, int ldc, int path, int split_k, int num_sms, Plan* p) {
+void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
+               const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
+               int num_sms, Plan* p) {
     *p = Plan{};
     p->M = M;
     p->N = N;
@@ -64,6 +70,10 @@ void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int l
     p->lda = lda;
     p->ldb = ldb;
     p->ldc = ldc;
+    p->op_a = op_a;
+    p->op_b = op_b;
+    p->alpha = alpha;
+    p->beta = beta;
     p->num_sms = num_sms;
     p->path = (path == TG_PATH_FFMA) ? TG_PATH_FFMA : TG_PATH_TF32X3;
     p->vec_c = C != nullptr && (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
@@ -78,7 +88,7 @@ void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int l
         p->launches = 0;
         return;
     }
-    if (K == 0) {  // the empty sum: C = +0.0, one fill kernel
+    if (K == 0) {  // the empty sum: C = beta * C, one kernel
         p->zero_fill = true;
         p->split = 1;
         p->launches = 1;
@@ -143,11 +153,14 @@ void make_plan(int M, int N, int K, const void* A, int lda, const void* B, int l
         p->off_b0 = take(b_bytes);
         p->off_b1 = take(b_bytes);
     } else {
-        // TMA reads the operands in place when their base is 16-byte aligned
-        // and their row pitch a multiple of 16 bytes; otherwise a pre-pass
-        // copies them to a padded buffer (A: [M][k4], B: [K][n4]).
-        p->pack_a = A == nullptr || (reinterpret_cast<uintptr_t>(A) % 16 != 0) || (lda % 4 != 0);
-        p->pack_b = B == nullptr || (reinterpret_cast<uintptr_t>(B) % 16 != 0) || (ldb % 4 != 0);
+        // TMA reads the operands in place when they are stored untransposed,
+        // their base is 16-byte aligned and their row pitch a multiple of 16
+        // bytes; otherwise a pre-pass copies them (transposing a transposed
+        // one) to a padded buffer (A: [M][k4], B: [K][n4]).
+        p->pack_a = op_a == TG_OP_T || A == nullptr || (reinterpret_cast<uintptr_t>(A) % 16 != 0) ||
+                    (lda % 4 != 0);
+        p->pack_b = op_b == TG_OP_T || B == nullptr || (reinterpret_cast<uintptr_t>(B) % 16 != 0) ||
+                    (ldb % 4 != 0);
         if (p->pack_a) p->off_a0 = take(4ull * M * p->k4);
         if (p->pack_b) p->off_b0 = take(4ull * K * p->n4);
     }

@@ -117,3 +117,35 @@ def test_plan_split_ranges_cover_k(M, N, K):
         bounds = [s * nkb // S for s in range(S + 1)]
         assert bounds[0] == 0 and bounds[-1] == nkb
         assert all(b1 > b0 for b0, b1 in zip(bounds, bounds[1:]))
+
+
+def _general(opa, opb, M, N, K, lda, ldb, ldc, A=1 << 20, B=1 << 32, C=1 << 36):
+    o = binding.Opts()
+    return tg.lib().tg_sgemm_general(opa, opb, M, N, K, 1.0, A, lda, B, ldb, 0.0, C, ldc, None, ctypes.byref(o))
+
+
+def test_general_argument_errors_need_no_gpu():
+    # stored shapes: A is K x M for op T (lda >= M); B is N x K for op T (ldb >= K)
+    assert _general(1, 0, 8, 4, 6, 7, 4, 4) == 1   # op T: lda < M
+    assert _general(0, 1, 8, 4, 6, 6, 5, 4) == 1   # op T: ldb < K
+    assert _general(2, 0, 8, 4, 6, 8, 4, 4) == 1   # bad op
+    assert _general(0, -1, 8, 4, 6, 8, 4, 4) == 1
+    # C overlapping a transposed A: A spans K rows of lda
+    assert _general(1, 0, 8, 4, 6, 8, 4, 4, A=1 << 20, C=(1 << 20) + 4 * 8 * 5) == 1
+    assert _general(1, 0, 0, 4, 6, 8, 4, 4) == 0   # empty output: no-op, no device touched
+
+
+def test_general_plan_packs_transposed_operands():
+    sms = 152
+    one = dict(num_sms=sms, path="ffma", split_k=1, A=4096, B=1 << 20, C=1 << 24)
+    # FFMA reads untransposed, aligned operands in place; a transposed one is packed
+    assert tg.plan_general(0, 0, 512, 512, 512, 512, 512, 512, **one)["prepass"] == 0
+    pa = tg.plan_general(1, 0, 512, 512, 256, 512, 512, 512, **one)
+    assert pa["prepass"] == 1 and pa["workspace_bytes"] == 512 * 256 * 4
+    pb = tg.plan_general(0, 1, 512, 768, 256, 256, 256, 768, **one)
+    assert pb["prepass"] == 1 and pb["workspace_bytes"] == 256 * 768 * 4
+    # 3xTF32 always re-lays both operands; the workspace does not depend on ops
+    t = [tg.plan_general(a, b, 777, 1029, 513, 777 if a else 513, 513 if b else 1029, 1029, num_sms=sms)
+         for a in (0, 1) for b in (0, 1)]
+    assert len({x["workspace_bytes"] for x in t}) == 1
+
