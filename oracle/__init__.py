@@ -58,6 +58,8 @@ def _declare(lib):
     lib.tg_oracle_sgemm_general.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, ctypes.c_float, fp, i64,
                                             fp, i64, ctypes.c_float, fp, i64]
     lib.tg_oracle_sgemm_general.restype = ctypes.c_int
+    lib.tg_oracle_transpose.argtypes = [i64, i64, fp, i64, fp, i64]
+    lib.tg_oracle_transpose.restype = ctypes.c_int
     lib.tg_oracle_threads.argtypes = []
     lib.tg_oracle_threads.restype = ctypes.c_int
     return lib
@@ -129,6 +131,18 @@ def sgemm_general(op_a: int, op_b: int, alpha: float, A: np.ndarray, B: np.ndarr
     if rc != 0:
         raise RuntimeError(f"tg_oracle_sgemm_general failed with code {rc}")
     return C
+
+
+def transpose(X: np.ndarray, lib=None) -> np.ndarray:
+    """X^T (cols x rows, contiguous) by the oracle's index permutation."""
+    lib = lib or load()
+    X, ld = _as_rowmajor_f32(X, "X")
+    rows, cols = X.shape
+    out = np.empty((cols, rows), dtype=np.float32)
+    rc = lib.tg_oracle_transpose(rows, cols, X.ctypes.data, ld, out.ctypes.data, max(rows, 1))
+    if rc != 0:
+        raise RuntimeError(f"tg_oracle_transpose failed with code {rc}")
+    return out
 
 
 def threads(lib=None) -> int:

@@ -171,6 +171,24 @@ int tg_oracle_sgemm_general(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
     return 0;
 }
 
+/*
+ * Matrix transpose: out[c][r] = in[r][c] for 0 <= r < rows, 0 <= c < cols
+ * (in is rows x cols with row stride ld_in >= cols; out is cols x rows with
+ * ld_out >= rows).  The workload of "03 CUDA Shared Memory: Tiling, Bank
+ * Conflicts, and Reduction", section "Bank Conflict": a tile is read along
+ * rows and written along columns.  Pure index permutation, so any correct
+ * implementation matches bit for bit.  Returns 0, or 1 on a bad shape.
+ */
+int tg_oracle_transpose(int64_t rows, int64_t cols, const float* in, int64_t ld_in,
+                        float* out, int64_t ld_out) {
+    if (rows < 0 || cols < 0) return 1;
+    if (ld_in < (cols > 1 ? cols : 1) || ld_out < (rows > 1 ? rows : 1)) return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) out[c * ld_out + r] = in[r * ld_in + c];
+    return 0;
+}
+
 /* Number of threads the two entry points above use. */
 int tg_oracle_threads(void) {
 #ifdef _OPENMP

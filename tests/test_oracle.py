@@ -331,11 +331,34 @@ def pin_general_brute_force_exact(lib):
         assert_bitexact(got + np.float32(0.0), want + np.float32(0.0), f"general brute force {M}x{N}x{K}")
 
 
+# ------------------------------------------------------------------ transpose
+
+
+def pin_transpose_hand_worked(lib):
+    X, XT = read_golden("hand_transpose_2x3.txt", ("X", "XT"))
+    assert_bitexact(oracle.transpose(X, lib=lib), XT, "hand transpose")
+
+
+def pin_transpose_involution_and_library(lib):
+    rng = np.random.default_rng(41)
+    for (r, c) in [(1, 1), (1, 7), (33, 31), (64, 100)]:
+        X = rand_f32(rng, (r, c), -5, 5)
+        T = oracle.transpose(X, lib=lib)
+        assert T.shape == (c, r)
+        assert_bitexact(oracle.transpose(T, lib=lib), X, "transpose twice")
+        assert_bitexact(T, np.ascontiguousarray(X.T), "numpy transpose")
+        # element (r', c') of the result is X[c'][r'] (the definition)
+        assert T[c - 1, 0] == X[0, c - 1] and T[0, r - 1] == X[r - 1, 0]
+    # strided source (row pitch larger than the width)
+    big = rand_f32(rng, (5, 9))
+    assert_bitexact(oracle.transpose(big[:, :6], lib=lib), np.ascontiguousarray(big[:, :6].T), "strided")
+
+
 PINS = [pin_hand_worked, pin_identity, pin_permutation, pin_transpose_law, pin_brute_force_exact,
         pin_brute_force_random, pin_closed_forms, pin_zero_padding, pin_integer_exact,
         pin_float64_library, pin_strides_and_edges, pin_rows_entry, pin_general_hand_worked,
         pin_general_reduces_and_transposes, pin_general_alpha_beta_closed_forms,
-        pin_general_brute_force_exact]
+        pin_general_brute_force_exact, pin_transpose_hand_worked, pin_transpose_involution_and_library]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -397,13 +420,37 @@ MUTANTS = {
     "general_beta_sign": ("if (beta != 0.0f) r += (double)beta", "if (beta != 0.0f) r -= (double)beta"),
     "general_reads_c_at_beta0": ("if (beta != 0.0f) r += (double)beta * (double)C[i * ldc + j];",
                                  "r += (double)beta * (double)C[i * ldc + j];"),
+    "transpose_same_index": ("out[c * ld_out + r] = in[r * ld_in + c];", "out[r * ld_out + c] = in[r * ld_in + c];"),
+    "transpose_drops_last_col": ("for (int64_t c = 0; c < cols; ++c) out[c * ld_out + r]",
+                                 "for (int64_t c = 0; c + 1 < cols; ++c) out[c * ld_out + r]"),
     "truncating_store": ("for (int64_t j = 0; j < N; ++j) C_row[j] = (float)acc[j];",
                          "for (int64_t j = 0; j < N; ++j) { float f = (float)acc[j]; if ((double)f - acc[j] > 0 && f > 0) f = nextafterf(f, 0.0f); else if ((double)f - acc[j] < 0 && f < 0) f = nextafterf(f, 0.0f); C_row[j] = f; }"),
 }
 
 
+_MUTANT_RUNNER = """
+import sys
+sys.path.insert(0, {tests!r}); sys.path.insert(0, {root!r})
+import oracle, test_oracle
+lib = oracle.load({so!r})
+caught = []
+for pin in test_oracle.PINS:
+    try:
+        pin(lib)
+    except (AssertionError, RuntimeError, ValueError):
+        caught.append(pin.__name__)
+print("CAUGHT", ",".join(caught))
+"""
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutants_are_caught(name, tmp_path):
+    """Each planted mistake fails at least one pin.  The pins run in a child
+    process: a mutant that writes out of bounds may crash it, which also
+    counts as caught."""
+    import subprocess
+    import sys
+
     old, new = MUTANTS[name]
     with open(oracle._SRC) as f:
         src = f.read()
@@ -414,11 +461,11 @@ def test_mutants_are_caught(name, tmp_path):
     cpath = tmp_path / f"{name}.c"
     cpath.write_text(src)
     so = oracle.build(str(cpath), str(tmp_path / f"lib{name}.so"), extra_flags=["-lm"])
-    lib = oracle.load(so)
-    caught = []
-    for pin in PINS:
-        try:
-            pin(lib)
-        except (AssertionError, RuntimeError, ValueError):
-            caught.append(pin.__name__)
+    tests_dir = os.path.dirname(os.path.abspath(__file__))
+    code = _MUTANT_RUNNER.format(tests=tests_dir, root=os.path.dirname(tests_dir), so=so)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    if r.returncode != 0:
+        return  # the mutant crashed the pins' process: caught
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("CAUGHT")][-1]
+    caught = [c for c in line[len("CAUGHT"):].strip().split(",") if c]
     assert caught, f"mutant {name} passed every pin"
