@@ -61,6 +61,9 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline (profiling runs)")
     ap.add_argument("--no-probes", action="store_true", help="skip the instruction-mix peak probes")
+    ap.add_argument("--transpose", action="store_true",
+                    help="measure the tiled-transpose variants instead of the GEMM")
+    ap.add_argument("--transpose-n", type=int, default=16384)
     return ap.parse_args()
 
 
@@ -244,6 +247,52 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_transpose(args, world, rank, local):
+    """The pages' transpose study on GB300: every variant on an n x n fp32
+    matrix (inputs larger than L2), 8 bytes moved per element, against the
+    measured copy bandwidth."""
+    import shared_memory_tiled_fp32_gb300 as tg
+    import oracle
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n = args.transpose_n
+    gen = torch.Generator(device=dev).manual_seed(11)
+    X = torch.randn(n, n, device=dev, generator=gen)
+    Y = torch.empty(n, n, device=dev)
+    peaks, src = load_peaks()
+    out = {}
+    for name in ("direct", "tile32", "padded", "swizzled"):
+        for _ in range(args.warmup):
+            tg.transpose(X, Y, variant=name)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(args.steps):
+            tg.transpose(X, Y, variant=name)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        gbs = 8.0 * n * n / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "GB/s": gbs, "frac_of_copy": gbs / peaks["hbm_gbs"]}
+    # parity on a sampled block against the oracle's index permutation
+    r0 = n // 3
+    blk = X[r0:r0 + 256, :512].cpu().numpy()
+    ok = bool(np.array_equal(Y[:512, r0:r0 + 256].cpu().numpy(), oracle.transpose(blk)))
+    best = max(out, key=lambda k: out[k]["GB/s"])
+    line = {"metric": "tiled transpose GB/s (8 bytes per element)", "value": out[best]["GB/s"], "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": out[best]["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": f"transpose_{n}x{n}", "best_variant": best,
+                                            "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": out[best]["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": out[best]["GB/s"] / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": f"copy bandwidth, {src}"},
+            "variants": out, "parity_sample_bitexact": ok}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -252,6 +301,11 @@ def main():
         import torch.distributed as dist
 
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.transpose:
+        run_transpose(args, world, rank, local)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.impl == "reference":
         run_reference(args, w, world, rank)
         if world > 1:

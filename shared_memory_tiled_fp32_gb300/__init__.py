@@ -20,4 +20,5 @@ from .binding import (  # noqa: F401
     sgemm_host,
     status_string,
     sync_status,
+    transpose,
 )

@@ -25,7 +25,7 @@ STATUS = {
 PATHS = {"auto": 0, "ffma": 1, "tf32x3": 2}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
-# Every symbol include/tg_sgemm.h and include/tg_probes.h declare.
+# Every symbol the headers in include/ declare.
 EXPORTS = (
     "tg_sgemm",
     "tg_sgemm_ex",
@@ -42,6 +42,7 @@ EXPORTS = (
     "tg_sgemm_version",
     "tg_probe_tf32_mma",
     "tg_probe_ffma",
+    "tg_transpose",
 )
 
 
@@ -133,6 +134,8 @@ def lib():
         L.tg_probe_tf32_mma.restype = i
         L.tg_probe_ffma.argtypes = [i, p, vp, ctypes.POINTER(ctypes.c_double)]
         L.tg_probe_ffma.restype = i
+        L.tg_transpose.argtypes = [i, i, i, p, i, p, i, vp]
+        L.tg_transpose.restype = i
         _lib = L
     return _lib
 
@@ -237,6 +240,28 @@ def matmul_general(A, B, C=None, *, trans_a=False, trans_b=False, alpha=1.0, bet
                                     ctypes.byref(o))
     _check(st, "tg_sgemm_general")
     return C
+
+
+TRANSPOSE_VARIANTS = {"direct": 0, "tile32": 1, "padded": 2, "swizzled": 3}
+
+
+def transpose(X, out=None, *, variant="padded", stream=None):
+    """X^T of a float32 CUDA matrix through tg_transpose (include/tg_transpose.h)."""
+    import torch
+
+    if X.dtype != torch.float32 or not X.is_cuda:
+        raise TypeError("X must be a float32 CUDA tensor")
+    rows, cols = X.shape
+    if out is None:
+        out = torch.empty((cols, rows), dtype=torch.float32, device=X.device)
+    if tuple(out.shape) != (cols, rows):
+        raise ValueError("out must be (cols, rows)")
+    v = TRANSPOSE_VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    with torch.cuda.device(X.device):
+        st = lib().tg_transpose(v, rows, cols, X.data_ptr(), _rowmajor_ld(X, "X"), out.data_ptr(),
+                                _rowmajor_ld(out, "out"), _stream_handle(stream))
+    _check(st, "tg_transpose")
+    return out
 
 
 def matmul_noalloc(A, B, out, *, stream=None):

@@ -108,12 +108,40 @@ def test_unswizzled_a_would_conflict():
 
 
 def test_prepass_transpose_tile_conflict_free():
-    """B is staged as tile[ty + 8r][tx] (row writes) and read as tile[tx][ty + 8r]
-    with a 33-float pitch: both are conflict-free."""
-    pitch = 33
-    for ty in range(8):
-        for r in range(4):
-            writes = [4 * ((ty + 8 * r) * pitch + tx) for tx in range(32)]
-            reads = [4 * (tx * pitch + ty + 8 * r) for tx in range(32)]
+    """The pre-pass stages a 64 x 64 tile as tile[ty + 4j][tx] (row writes,
+    tx = 0..63, a warp holds 32 consecutive tx) and reads it as
+    tile[tx][ty + 4j] with a 65-float pitch: both are conflict-free."""
+    pitch = 65
+    for ty in range(4):
+        for half in (0, 32):
+            for j in range(16):
+                writes = [4 * ((ty + 4 * j) * pitch + tx) for tx in range(half, half + 32)]
+                reads = [4 * (tx * pitch + ty + 4 * j) for tx in range(half, half + 32)]
+                assert wavefronts_32(writes) == 1
+                assert wavefronts_32(reads) == 1
+
+
+# ------------------------------------------------------- transpose workload
+
+
+def transpose_tile_index(variant, r, c):
+    """tile_index of csrc/tg_transpose.cu, in floats."""
+    if variant == "padded":
+        return r * 33 + c
+    if variant == "swizzled":
+        return r * 32 + (c ^ r)
+    return r * 32 + c
+
+
+@pytest.mark.parametrize("variant,read_degree", [("tile32", 32), ("padded", 1), ("swizzled", 1)])
+def test_transpose_variants_bank_degrees(variant, read_degree):
+    """Row writes into the tile are conflict-free for all three layouts; the
+    column read (lane = tile row) is 32-way for tile[32][32] and free for the
+    padded and swizzled layouts."""
+    for ty in range(4):
+        for j in range(8):
+            writes = [4 * transpose_tile_index(variant, ty + 4 * j, tx) for tx in range(32)]
+            reads = [4 * transpose_tile_index(variant, tx, ty + 4 * j) for tx in range(32)]
             assert wavefronts_32(writes) == 1
-            assert wavefronts_32(reads) == 1
+            assert wavefronts_32(reads) == read_degree
+
