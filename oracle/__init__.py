@@ -60,6 +60,8 @@ def _declare(lib):
     lib.tg_oracle_sgemm_general.restype = ctypes.c_int
     lib.tg_oracle_transpose.argtypes = [i64, i64, fp, i64, fp, i64]
     lib.tg_oracle_transpose.restype = ctypes.c_int
+    lib.tg_oracle_sum.argtypes = [i64, fp, fp]
+    lib.tg_oracle_sum.restype = ctypes.c_int
     lib.tg_oracle_threads.argtypes = []
     lib.tg_oracle_threads.restype = ctypes.c_int
     return lib
@@ -143,6 +145,17 @@ def transpose(X: np.ndarray, lib=None) -> np.ndarray:
     if rc != 0:
         raise RuntimeError(f"tg_oracle_transpose failed with code {rc}")
     return out
+
+
+def reduce_sum(x: np.ndarray, lib=None) -> np.float32:
+    """Sum of a 1-D float32 array (double accumulation, one rounding)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.zeros(1, dtype=np.float32)
+    rc = lib.tg_oracle_sum(x.shape[0], x.ctypes.data, out.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"tg_oracle_sum failed with code {rc}")
+    return out[0]
 
 
 def threads(lib=None) -> int:

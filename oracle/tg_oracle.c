@@ -189,6 +189,21 @@ int tg_oracle_transpose(int64_t rows, int64_t cols, const float* in, int64_t ld_
     return 0;
 }
 
+/*
+ * Sum reduction: the sum of x[0..n) accumulated in double in ascending index
+ * order from +0.0, rounded once to float ("03 CUDA Shared Memory: Tiling,
+ * Bank Conflicts, and Reduction", section "Reduction": N values folded into
+ * one).  Any summation order agrees with it to within the rounding of its own
+ * fp32 partial sums.  Returns 0, or 1 on n < 0.
+ */
+int tg_oracle_sum(int64_t n, const float* x, float* result) {
+    if (n < 0) return 1;
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += (double)x[i];
+    *result = (float)s;
+    return 0;
+}
+
 /* Number of threads the two entry points above use. */
 int tg_oracle_threads(void) {
 #ifdef _OPENMP

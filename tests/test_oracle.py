@@ -354,11 +354,39 @@ def pin_transpose_involution_and_library(lib):
     assert_bitexact(oracle.transpose(big[:, :6], lib=lib), np.ascontiguousarray(big[:, :6].T), "strided")
 
 
+# ---------------------------------------------------------------- reduction
+
+
+def pin_sum_hand_worked_and_closed_forms(lib):
+    # 1 + 2 + ... + 100 = 5050 (Gauss); 0.5 + 0.25 + 0.125 = 0.875
+    assert oracle.reduce_sum(np.arange(1, 101, dtype=np.float32), lib=lib) == np.float32(5050)
+    assert oracle.reduce_sum(np.array([0.5, 0.25, 0.125], np.float32), lib=lib) == np.float32(0.875)
+    # the empty sum is +0.0; alternating +1/-1 cancels exactly
+    z = oracle.reduce_sum(np.zeros(0, np.float32), lib=lib)
+    assert z == 0 and not np.signbit(z)
+    assert oracle.reduce_sum(np.tile(np.array([1.0, -1.0], np.float32), 500), lib=lib) == 0
+    # a float accumulator would lose the small terms: 2^24 + 16 ones = 2^24 + 16
+    x = np.concatenate([np.array([2.0 ** 24], np.float32), np.ones(16, np.float32)])
+    assert oracle.reduce_sum(x, lib=lib) == np.float32(2 ** 24 + 16)
+
+
+def pin_sum_exact_rational(lib):
+    rng = np.random.default_rng(51)
+    for n in (1, 2, 7, 50):
+        x = (rng.standard_normal(n) * 2.0 ** rng.integers(-10, 10, size=n)).astype(np.float32)
+        exact = sum((f32_to_fraction(v) for v in x), Fraction(0))
+        want = round_fraction_to_f32(exact)
+        assert ulp_distance(oracle.reduce_sum(x, lib=lib), want) <= 1, n
+        ints = rng.integers(-2, 3, size=n).astype(np.float32)
+        assert oracle.reduce_sum(ints, lib=lib) == np.float32(int(ints.astype(np.int64).sum()))
+
+
 PINS = [pin_hand_worked, pin_identity, pin_permutation, pin_transpose_law, pin_brute_force_exact,
         pin_brute_force_random, pin_closed_forms, pin_zero_padding, pin_integer_exact,
         pin_float64_library, pin_strides_and_edges, pin_rows_entry, pin_general_hand_worked,
         pin_general_reduces_and_transposes, pin_general_alpha_beta_closed_forms,
-        pin_general_brute_force_exact, pin_transpose_hand_worked, pin_transpose_involution_and_library]
+        pin_general_brute_force_exact, pin_transpose_hand_worked, pin_transpose_involution_and_library,
+        pin_sum_hand_worked_and_closed_forms, pin_sum_exact_rational]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -423,6 +451,10 @@ MUTANTS = {
     "transpose_same_index": ("out[c * ld_out + r] = in[r * ld_in + c];", "out[r * ld_out + c] = in[r * ld_in + c];"),
     "transpose_drops_last_col": ("for (int64_t c = 0; c < cols; ++c) out[c * ld_out + r]",
                                  "for (int64_t c = 0; c + 1 < cols; ++c) out[c * ld_out + r]"),
+    "sum_float_accumulator": ("for (int64_t i = 0; i < n; ++i) s += (double)x[i];",
+                              "for (int64_t i = 0; i < n; ++i) s = (float)(s + (double)x[i]);"),
+    "sum_skips_first": ("for (int64_t i = 0; i < n; ++i) s += (double)x[i];",
+                        "for (int64_t i = 1; i < n; ++i) s += (double)x[i];"),
     "truncating_store": ("for (int64_t j = 0; j < N; ++j) C_row[j] = (float)acc[j];",
                          "for (int64_t j = 0; j < N; ++j) { float f = (float)acc[j]; if ((double)f - acc[j] > 0 && f > 0) f = nextafterf(f, 0.0f); else if ((double)f - acc[j] < 0 && f < 0) f = nextafterf(f, 0.0f); C_row[j] = f; }"),
 }
