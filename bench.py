@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--transpose", action="store_true",
                     help="measure the tiled-transpose variants instead of the GEMM")
     ap.add_argument("--transpose-n", type=int, default=16384)
+    ap.add_argument("--reduce", action="store_true", help="measure the sum-reduction variants instead")
+    ap.add_argument("--reduce-n", type=int, default=2 ** 28)
     return ap.parse_args()
 
 
@@ -293,6 +295,50 @@ def run_transpose(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_reduce(args, world, rank, local):
+    """The pages' reduction study on GB300: every variant summing n fp32
+    values (4 bytes read per value, inputs larger than L2) against the
+    measured copy bandwidth."""
+    import shared_memory_tiled_fp32_gb300 as tg
+    import oracle
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n = args.reduce_n
+    x = torch.randn(n, device=dev, generator=torch.Generator(device=dev).manual_seed(12))
+    res = torch.empty(1, device=dev)
+    peaks, src = load_peaks()
+    out = {}
+    for name in ("interleaved", "sequential", "shuffle", "atomic", "fast"):
+        for _ in range(args.warmup):
+            tg.reduce_sum(x, res, variant=name)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(args.steps):
+            tg.reduce_sum(x, res, variant=name)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        gbs = 4.0 * n / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "GB/s": gbs, "frac_of_copy": gbs / peaks["hbm_gbs"], "sum": float(res.item())}
+    ref = float(oracle.reduce_sum(x.cpu().numpy()))
+    for v in out.values():
+        v["abs_err_vs_oracle"] = abs(v["sum"] - ref)
+    best = max(out, key=lambda k: out[k]["GB/s"])
+    line = {"metric": "sum reduction GB/s (4 bytes read per value)", "value": out[best]["GB/s"], "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": out[best]["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": f"reduce_sum_{n}", "best_variant": best,
+                                            "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": out[best]["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": out[best]["GB/s"] / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": f"copy bandwidth, {src}"},
+            "variants": out, "oracle_sum": ref, "sum_abs": float(x.abs().sum().item())}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -301,6 +347,11 @@ def main():
         import torch.distributed as dist
 
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.reduce:
+        run_reduce(args, world, rank, local)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.transpose:
         run_transpose(args, world, rank, local)
         if world > 1:

@@ -19,6 +19,8 @@ from .binding import (  # noqa: F401
     selftest_wait_timeout,
     sgemm_host,
     status_string,
+    reduce_plan,
+    reduce_sum,
     sync_status,
     transpose,
 )

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtg_sgemm.so")
-SOURCES = ["tg_kernels.cu", "tg_noalloc.cu", "tg_probes.cu", "tg_transpose.cu", "tg_api.cpp", "tg_plan.cpp"]
+SOURCES = ["tg_kernels.cu", "tg_noalloc.cu", "tg_probes.cu", "tg_transpose.cu", "tg_reduce.cu", "tg_api.cpp", "tg_plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

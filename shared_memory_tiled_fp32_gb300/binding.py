@@ -43,6 +43,8 @@ EXPORTS = (
     "tg_probe_tf32_mma",
     "tg_probe_ffma",
     "tg_transpose",
+    "tg_reduce_sum",
+    "tg_reduce_plan",
 )
 
 
@@ -136,6 +138,11 @@ def lib():
         L.tg_probe_ffma.restype = i
         L.tg_transpose.argtypes = [i, i, i, p, i, p, i, vp]
         L.tg_transpose.restype = i
+        L.tg_reduce_sum.argtypes = [i, ctypes.c_longlong, p, p, vp]
+        L.tg_reduce_sum.restype = i
+        L.tg_reduce_plan.argtypes = [i, ctypes.c_longlong, i, ctypes.POINTER(ctypes.c_int),
+                                     ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_size_t)]
+        L.tg_reduce_plan.restype = i
         _lib = L
     return _lib
 
@@ -262,6 +269,37 @@ def transpose(X, out=None, *, variant="padded", stream=None):
                                 _rowmajor_ld(out, "out"), _stream_handle(stream))
     _check(st, "tg_transpose")
     return out
+
+
+REDUCE_VARIANTS = {"interleaved": 0, "sequential": 1, "shuffle": 2, "atomic": 3, "fast": 4}
+
+
+def reduce_sum(x, out=None, *, variant="fast", stream=None):
+    """Sum of a float32 CUDA tensor (flattened, contiguous) through
+    tg_reduce_sum (include/tg_reduce.h); returns a 1-element CUDA tensor."""
+    import torch
+
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    v = REDUCE_VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    with torch.cuda.device(x.device):
+        st = lib().tg_reduce_sum(v, x.numel(), x.data_ptr() if x.numel() else None, out.data_ptr(),
+                                 _stream_handle(stream))
+    _check(st, "tg_reduce_sum")
+    return out
+
+
+def reduce_plan(variant, n, num_sms=0) -> dict:
+    """Launches of one tg_reduce_sum call (host arithmetic)."""
+    passes = ctypes.c_int()
+    counts = (ctypes.c_longlong * 8)()
+    ws = ctypes.c_size_t()
+    v = REDUCE_VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    _check(lib().tg_reduce_plan(v, n, num_sms, ctypes.byref(passes), counts, ctypes.byref(ws)), "tg_reduce_plan")
+    return {"passes": passes.value, "counts": [counts[i] for i in range(passes.value)],
+            "workspace_bytes": ws.value}
 
 
 def matmul_noalloc(A, B, out, *, stream=None):

@@ -88,6 +88,20 @@ void fill_info(const Plan& p, tg_plan_info* out) {
 }
 
 }  // namespace
+
+tg_status workspace_alloc(size_t bytes, cudaStream_t stream, void** out) {
+    DeviceState* d = nullptr;
+    const tg_status st = current_device(&d);
+    if (st != TG_OK) return st;
+    if (cudaMallocFromPoolAsync(out, bytes, d->pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_OUT_OF_MEMORY;
+    }
+    return TG_OK;
+}
+
+void workspace_free(void* p, cudaStream_t stream) { cudaFreeAsync(p, stream); }
+
 }  // namespace tg
 
 using namespace tg;

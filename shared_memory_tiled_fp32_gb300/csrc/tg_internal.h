@@ -74,4 +74,9 @@ tg_status launch_wait_selftest(unsigned int timeout_us, cudaStream_t stream);
 // One-time per-device set-up of kernel attributes (tg_kernels.cu).
 tg_status prepare_device_kernels();
 
+// Stream-ordered scratch from the library's per-device memory pool
+// (tg_api.cpp); for the auxiliary workloads.
+tg_status workspace_alloc(size_t bytes, cudaStream_t stream, void** out);
+void workspace_free(void* p, cudaStream_t stream);
+
 }  // namespace tg
