@@ -3,6 +3,7 @@
 // workspace handling and the host-buffer convenience call.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -22,6 +23,31 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
+
+// Copy streams and events of the host-buffer entry point, per device.
+constexpr int kMaxHostBlocks = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev[3 + 2 * kMaxHostBlocks] = {};
+    std::mutex mu;
+};
+HostPipe g_host[kMaxDevices];
+
+tg_status host_pipe(int dev, HostPipe** out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    HostPipe& h = g_host[dev];
+    if (!h.ready) {
+        if (cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking) != cudaSuccess)
+            return TG_ERR_CUDA;
+        for (cudaEvent_t& e : h.ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return TG_ERR_CUDA;
+        h.ready = true;
+    }
+    *out = &h;
+    return TG_OK;
+}
 
 // State of the current device, initialised on first use.
 tg_status current_device(DeviceState** out) {
@@ -207,42 +233,102 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     DeviceState* d = nullptr;
     st = current_device(&d);
     if (st != TG_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TG_ERR_CUDA;
+    HostPipe* hp = nullptr;
+    st = host_pipe(dev, &hp);
+    if (st != TG_OK) return st;
+    std::lock_guard<std::mutex> lock(hp->mu);  // one host-buffer call per device at a time
 
-    const int dlda = K > 0 ? K : 1, dldb = N, dldc = N;
-    void *dA = nullptr, *dB = nullptr, *dC = nullptr;
-    const size_t a_bytes = 4ull * M * (size_t)(K > 0 ? K : 1);
-    const size_t b_bytes = 4ull * (size_t)(K > 0 ? K : 1) * N;
-    const size_t c_bytes = 4ull * M * N;
+    const int path = o.path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3;
+    const bool tf32 = path == TG_PATH_TF32X3;
+    const long long k4 = ((long long)std::max(K, 1) + 3) / 4 * 4, n4 = ((long long)N + 3) / 4 * 4;
+    // Row blocks: on large products the copies of one block overlap the
+    // product of another (A in, C out on two copy streams).
+    int P = 1;
+    if ((double)M * N * K >= 8589934592.0 && M >= 2048) P = std::min(kMaxHostBlocks, std::min(4, M / 1024));
+    const int mb = ((M + P - 1) / P + 127) / 128 * 128;
+    P = (M + mb - 1) / mb;
+
+    // device copies: 16-byte row pitches, so TMA reads them in place
+    const size_t a_bytes = 4ull * M * k4, b_bytes = 4ull * (size_t)std::max(K, 1) * n4,
+                 c_bytes = 4ull * M * n4;
+    const size_t b_split = tf32 ? (4ull * N * k4 + kWsAlign - 1) / kWsAlign * kWsAlign : 0;
+    // placeholder pointers with the alignment the real ones will have
+    const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
+    size_t ws_max = 0;
+    for (int i = 0; i < P; ++i) {
+        const int Mi = std::min(mb, M - i * mb);
+        Plan pl;
+        make_plan(TG_OP_N, TG_OP_N, Mi, N, K, 1.0f, al, (int)k4, al, (int)n4, 0.0f, al, (int)n4, path,
+                  o.split_k, d->num_sms, &pl, tf32);
+        ws_max = std::max(ws_max, pl.ws_bytes);
+    }
+    const size_t ws_total = 2 * b_split + ws_max;
+
+    void *dA = nullptr, *dB = nullptr, *dC = nullptr, *W = nullptr;
     if (cudaMallocFromPoolAsync(&dA, a_bytes, d->pool, stream) != cudaSuccess ||
         cudaMallocFromPoolAsync(&dB, b_bytes, d->pool, stream) != cudaSuccess ||
-        cudaMallocFromPoolAsync(&dC, c_bytes, d->pool, stream) != cudaSuccess) {
+        cudaMallocFromPoolAsync(&dC, c_bytes, d->pool, stream) != cudaSuccess ||
+        (ws_total > 0 && cudaMallocFromPoolAsync(&W, ws_total, d->pool, stream) != cudaSuccess)) {
         cudaGetLastError();
-        if (dA) cudaFreeAsync(dA, stream);
-        if (dB) cudaFreeAsync(dB, stream);
-        if (dC) cudaFreeAsync(dC, stream);
+        for (void* q : {dA, dB, dC, W})
+            if (q) cudaFreeAsync(q, stream);
         cudaStreamSynchronize(stream);
         return TG_ERR_OUT_OF_MEMORY;
     }
-    bool ok = true;
-    if (K > 0) {
-        ok = ok && cudaMemcpy2DAsync(dA, 4ull * dlda, A, 4ull * lda, 4ull * K, M,
-                                     cudaMemcpyHostToDevice, stream) == cudaSuccess;
-        ok = ok && cudaMemcpy2DAsync(dB, 4ull * dldb, B, 4ull * ldb, 4ull * N, K,
-                                     cudaMemcpyHostToDevice, stream) == cudaSuccess;
+    float* fA = static_cast<float*>(dA);
+    float* fB = static_cast<float*>(dB);
+    float* fC = static_cast<float*>(dC);
+    uint8_t* w8 = static_cast<uint8_t*>(W);
+    cudaEvent_t* ev = hp->ev;  // [0] alloc, [1] B in, [2+i] A_i in, [2+P+i] C_i done, [2+2P] out
+    bool ok = cudaEventRecord(ev[0], stream) == cudaSuccess &&
+              cudaStreamWaitEvent(hp->s_in, ev[0], 0) == cudaSuccess &&
+              cudaStreamWaitEvent(hp->s_out, ev[0], 0) == cudaSuccess;
+    if (ok && K > 0) {
+        ok = cudaMemcpy2DAsync(fB, 4ull * n4, B, 4ull * ldb, 4ull * N, K, cudaMemcpyHostToDevice, hp->s_in) ==
+                 cudaSuccess &&
+             cudaEventRecord(ev[1], hp->s_in) == cudaSuccess;
+        for (int i = 0; ok && i < P; ++i) {
+            const int i0 = i * mb, Mi = std::min(mb, M - i0);
+            ok = cudaMemcpy2DAsync(fA + (size_t)i0 * k4, 4ull * k4, A + (size_t)i0 * lda, 4ull * lda, 4ull * K, Mi,
+                                   cudaMemcpyHostToDevice, hp->s_in) == cudaSuccess &&
+                 cudaEventRecord(ev[2 + i], hp->s_in) == cudaSuccess;
+        }
     }
-    if (ok) {
-        st = tg_sgemm_ex(M, N, K, static_cast<const float*>(dA), dlda, static_cast<const float*>(dB),
-                         dldb, static_cast<float*>(dC), dldc, stream, &o);
-        ok = st == TG_OK;
-    } else {
-        st = TG_ERR_CUDA;
+    st = ok ? TG_OK : TG_ERR_CUDA;
+    for (int i = 0; st == TG_OK && i < P; ++i) {
+        const int i0 = i * mb, Mi = std::min(mb, M - i0);
+        if (K > 0 && ((i == 0 && cudaStreamWaitEvent(stream, ev[1], 0) != cudaSuccess) ||
+                      cudaStreamWaitEvent(stream, ev[2 + i], 0) != cudaSuccess)) {
+            st = TG_ERR_CUDA;
+            break;
+        }
+        const float* Ai = fA + (size_t)i0 * k4;
+        float* Ci = fC + (size_t)i0 * n4;
+        Plan pl;
+        make_plan(TG_OP_N, TG_OP_N, Mi, N, K, 1.0f, Ai, (int)k4, fB, (int)n4, 0.0f, Ci, (int)n4, path, o.split_k,
+                  d->num_sms, &pl, tf32);
+        if (tf32) {  // B is split once, by the first block, into the shared region
+            pl.ext_b0 = reinterpret_cast<float*>(w8);
+            pl.ext_b1 = reinterpret_cast<float*>(w8 + b_split);
+            pl.b_ready = i > 0;
+        }
+        st = launch_plan(pl, Ai, fB, Ci, w8 + 2 * b_split, stream, nullptr, nullptr);
+        if (st != TG_OK) break;
+        if (cudaEventRecord(ev[2 + P + i], stream) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->s_out, ev[2 + P + i], 0) != cudaSuccess ||
+            cudaMemcpy2DAsync(C + (size_t)i0 * ldc, 4ull * ldc, Ci, 4ull * n4, 4ull * N, Mi, cudaMemcpyDeviceToHost,
+                              hp->s_out) != cudaSuccess)
+            st = TG_ERR_CUDA;
     }
-    if (ok && cudaMemcpy2DAsync(C, 4ull * ldc, dC, 4ull * dldc, 4ull * N, M, cudaMemcpyDeviceToHost,
-                                stream) != cudaSuccess)
-        st = TG_ERR_CUDA;
-    cudaFreeAsync(dA, stream);
-    cudaFreeAsync(dB, stream);
-    cudaFreeAsync(dC, stream);
+    // the buffers are released on `stream` once both copy streams are done
+    cudaEventRecord(ev[2 + 2 * P], hp->s_out);
+    cudaStreamWaitEvent(stream, ev[2 + 2 * P], 0);
+    cudaEventRecord(ev[1], hp->s_in);
+    cudaStreamWaitEvent(stream, ev[1], 0);
+    for (void* q : {dA, dB, dC, W})
+        if (q) cudaFreeAsync(q, stream);
     if (cudaStreamSynchronize(stream) != cudaSuccess) return TG_ERR_CUDA;
     if (st != TG_OK) return st;
     unsigned int word = 0;

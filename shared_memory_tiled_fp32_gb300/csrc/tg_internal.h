@@ -51,6 +51,12 @@ struct Plan {
     long long part_stride = 0;   // elements between two K-slice partials
     size_t ws_bytes = 0;
     int launches = 0;
+    // 3xTF32 only: B_hi^T / B_lo^T live outside the workspace at ext_b0 /
+    // ext_b1 (planned with external_b); b_ready = they already hold op(B)'s
+    // split, so the pre-pass skips B
+    float* ext_b0 = nullptr;
+    float* ext_b1 = nullptr;
+    bool b_ready = false;
 };
 
 // Argument checks of the C ABI (pure host arithmetic).  With need_pointers
@@ -61,7 +67,7 @@ tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int l
 // Fill `p` for the given call; num_sms > 0.  Assumes validate() passed.
 void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
                const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
-               int num_sms, Plan* p);
+               int num_sms, Plan* p, bool external_b = false);
 
 // Enqueue every kernel of plan `p` on `stream` (defined in tg_kernels.cu).
 tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, void* ws,

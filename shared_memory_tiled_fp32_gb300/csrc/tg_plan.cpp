@@ -62,7 +62,7 @@ tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int l
 
 void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
                const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
-               int num_sms, Plan* p) {
+               int num_sms, Plan* p, bool external_b) {
     *p = Plan{};
     p->M = M;
     p->N = N;
@@ -150,8 +150,10 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         const size_t a_bytes = 4ull * M * p->k4, b_bytes = 4ull * N * p->k4;
         p->off_a0 = take(a_bytes);
         p->off_a1 = take(a_bytes);
-        p->off_b0 = take(b_bytes);
-        p->off_b1 = take(b_bytes);
+        if (!external_b) {  // else the caller provides B's hi/lo copies
+            p->off_b0 = take(b_bytes);
+            p->off_b1 = take(b_bytes);
+        }
     } else {
         // TMA reads the operands in place when they are stored untransposed,
         // their base is 16-byte aligned and their row pitch a multiple of 16

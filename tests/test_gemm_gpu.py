@@ -184,6 +184,27 @@ def test_host_buffer_entry(tg):
     assert np.array_equal(C.numpy().view(np.uint32), dev.view(np.uint32))
 
 
+@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+def test_host_buffer_entry_row_blocks(tg, path):
+    """A product large enough for the host entry point to pipeline row blocks
+    (copies of one block overlapping the product of another), with a ragged
+    last block and padded host rows; checked on sampled rows."""
+    M, N, K = 4100, 1030, 2050
+    A, B = make_inputs(M, N, K, "uniform", 321)
+    Abig = torch.zeros(M, K + 3)
+    Abig[:, :K] = A
+    Ap = Abig.pin_memory()[:, :K]
+    Bp = B.pin_memory()
+    Cbig = torch.full((M, N + 5), float("nan")).pin_memory()
+    C = Cbig[:, :N]
+    tg.sgemm_host(Ap, Bp, C, path=path)
+    rows = np.sort(np.random.default_rng(3).choice(M, 200, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, 1151, 1152, 2303, 2304, M - 1]]))
+    ref = oracle.sgemm_rows(A.numpy(), B.numpy(), rows)
+    assert_close(C.numpy()[rows], ref, K, f"host row blocks {path}")
+    assert np.all(np.isnan(Cbig.numpy()[:, N:])), "host entry wrote past column N"
+
+
 def test_side_stream(tg):
     A, B, _, ref = workload_case("sq256_uniform")
     s = torch.cuda.Stream()
