@@ -292,20 +292,31 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
                     const int chunk = (kk >> 2) ^ (r & 7);
                     av[i] = *reinterpret_cast<const float4*>(a + r * BK + chunk * 4);
                 }
+                // B as packed pairs: bv[j].x = columns (0,1), .y = (2,3) of chunk j;
+                // the next k's fragment is loaded while this k's FMAs run
+                ulonglong2 bnext[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bnext[j] = *reinterpret_cast<const ulonglong2*>(b + kk * BN + 32 * j);
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
-                    // B as packed pairs: bv[j].x = columns (0,1), .y = (2,3) of chunk j
                     ulonglong2 bv[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        bv[j] = *reinterpret_cast<const ulonglong2*>(b + (kk + k4) * BN + 32 * j);
+                    for (int j = 0; j < 4; ++j) bv[j] = bnext[j];
+                    if (k4 < 3) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            bnext[j] = *reinterpret_cast<const ulonglong2*>(b + (kk + k4 + 1) * BN + 32 * j);
+                    }
+                    // all eight broadcasts first, so no FMA waits on its own splat
+                    unsigned long long x2[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x2[i] = f32x2_splat(lanef(av[i], k4));
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const unsigned long long x2 = f32x2_splat(lanef(av[i], k4));
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            fma_f32x2(acc[i][2 * j], x2, bv[j].x);
-                            fma_f32x2(acc[i][2 * j + 1], x2, bv[j].y);
+                            fma_f32x2(acc[i][2 * j], x2[i], bv[j].x);
+                            fma_f32x2(acc[i][2 * j + 1], x2[i], bv[j].y);
                         }
                     }
                 }
