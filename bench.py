@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--transpose-n", type=int, default=16384)
     ap.add_argument("--reduce", action="store_true", help="measure the sum-reduction variants instead")
     ap.add_argument("--reduce-n", type=int, default=2 ** 28)
+    ap.add_argument("--all-configs", action="store_true",
+                    help="one JSON line per workload and path (step and kernel throughput)")
     return ap.parse_args()
 
 
@@ -341,6 +343,44 @@ def run_reduce(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_all_configs(args, local):
+    """Step and GEMM-kernel throughput of every workload on both paths."""
+    import shared_memory_tiled_fp32_gb300 as tg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    for name, w in WORKLOADS.items():
+        A, B = (t.to(dev) for t in make_inputs(w.M, w.N, w.K, w.dist, w.seed))
+        C = torch.empty(w.M, w.N, device=dev)
+        for path in ("tf32x3", "ffma"):
+            plan = tg.plan(w.M, w.N, w.K, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr(), path=path)
+            ws = torch.empty(max(1, plan["workspace_bytes"] // 4 + 64), device=dev)
+            steps = max(3, min(args.steps, int(2e12 / w.flop) + 3))
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for e0, e1 in evs:
+                e0.record(stream)
+                e1.record(stream)
+            for _ in range(args.warmup):
+                tg.matmul(A, B, out=C, path=path, workspace=ws, stream=stream)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            s0.record(stream)
+            for i in range(steps):
+                tg.matmul(A, B, out=C, path=path, workspace=ws, main_begin=evs[i][0], main_end=evs[i][1],
+                          stream=stream)
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = s0.elapsed_time(s1) / steps
+            kms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+            print(json.dumps({"workload": name, "path": path, "M": w.M, "N": w.N, "K": w.K, "steps": steps,
+                              "ms_per_step": ms, "tflops": w.flop / (ms * 1e-3) / 1e12, "kernel_ms": kms,
+                              "kernel_tflops": w.flop / (kms * 1e-3) / 1e12,
+                              "plan": {k: plan[k] for k in ("pair", "split_k", "units", "grid", "tail_units",
+                                                            "tail_split", "launches")}}), flush=True)
+        del A, B, C
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -349,6 +389,12 @@ def main():
         import torch.distributed as dist
 
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.all_configs:
+        if rank == 0:
+            run_all_configs(args, local)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.reduce:
         run_reduce(args, world, rank, local)
         if world > 1:
