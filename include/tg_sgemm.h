@@ -184,7 +184,7 @@ tg_status tg_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream)
 /* Bytes of the fixed device scratch array behind tg_sgemm_noalloc (64 MiB). */
 #define TG_SGEMM_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
-/* C = A x B on the 3xTF32 path without allocating any memory.  The surveyed
+/* C = A x B on the 3xTF32 path without allocating any memory.  The source
  * pages have no counterpart of this entry point; it exists for callers that
  * cannot allocate device memory at call time -- for example a host
  * application that owns the whole device-memory budget through its own

@@ -19,7 +19,7 @@
  *   (ghost) elements are zeros that do not change the sum, so the oracle needs
  *   no padding at all.
  *
- * Readings taken where the pages are silent (each listed in the design doc):
+ * Readings taken where the pages are silent:
  * - shapes: A is M x K, B is K x N, C is M x N, each row-major with leading
  *   dimensions lda >= K, ldb >= N, ldc >= N (the pages show only square
  *   matrices with the width as stride);
