@@ -377,7 +377,7 @@ def run_all_configs(args, local):
                               "ms_per_step": ms, "tflops": w.flop / (ms * 1e-3) / 1e12, "kernel_ms": kms,
                               "kernel_tflops": w.flop / (kms * 1e-3) / 1e12,
                               "plan": {k: plan[k] for k in ("pair", "split_k", "units", "grid", "tail_units",
-                                                            "tail_split", "launches")}}), flush=True)
+                                                            "tail_lanes", "launches")}}), flush=True)
         del A, B, C
 
 

@@ -105,8 +105,8 @@ typedef struct tg_plan_info {
     size_t workspace_bytes;
     int pair;          /* 3xTF32: CTAs per cluster sharing one B tile by TMA multicast (1 or 2);
                           a unit is then `pair` vertically adjacent tiles */
-    long long tail_units; /* last-round tile units cut into tail_split K slices (0 = none) */
-    int tail_split;
+    long long tail_units; /* units after the last whole round of lanes, run stream-K (0 = none) */
+    int tail_lanes;       /* lanes (CTAs, or CTA pairs) sharing those units' K blocks equally */
 } tg_plan_info;
 
 /* C = A x B with automatic path and split choice (see the file comment for

@@ -82,7 +82,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("pair", ctypes.c_int),
         ("tail_units", ctypes.c_longlong),
-        ("tail_split", ctypes.c_int),
+        ("tail_lanes", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -110,7 +110,7 @@ void fill_info(const Plan& p, tg_plan_info* out) {
     out->workspace_bytes = p.ws_bytes;
     out->pair = p.pair;
     out->tail_units = p.tail_units;
-    out->tail_split = p.tail_split;
+    out->tail_lanes = p.tail_lanes;
 }
 
 }  // namespace
@@ -147,7 +147,7 @@ const char* tg_status_string(tg_status s) {
     return "unknown tg_status";
 }
 
-int tg_sgemm_version(void) { return 100; }
+int tg_sgemm_version(void) { return 101; }
 
 tg_status tg_sgemm_plan_general(int op_a, int op_b, int M, int N, int K, const void* A, int lda,
                                 const void* B, int ldb, const void* C, int ldc, int path,

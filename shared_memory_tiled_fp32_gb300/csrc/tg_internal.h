@@ -22,6 +22,38 @@ constexpr int kFfmaBM = 128, kFfmaBN = 256, kFfmaBK = 32, kFfmaStages = 4;
 
 constexpr size_t kWsAlign = 256;
 
+#ifdef __CUDACC__
+#define TG_HOST_DEVICE __host__ __device__
+#else
+#define TG_HOST_DEVICE
+#endif
+
+// Tile-unit index t (K slices aside) -> (tile-unit row, tile column).  Tiles
+// are visited in groups of kGroupM tile-unit rows, column by column inside a
+// group, so CTAs running at the same time share A rows and B columns in L2.
+constexpr int kGroupM = 8;
+
+TG_HOST_DEVICE inline void unit_tile(int tiles_m, int tiles_n, long long t, int* tm, int* tn) {
+    const long long per_group = (long long)kGroupM * tiles_n;
+    const int g = (int)(t / per_group);
+    const int first_m = g * kGroupM;
+    const int gm = tiles_m - first_m < kGroupM ? tiles_m - first_m : kGroupM;
+    const int r = (int)(t - g * per_group);
+    *tm = first_m + r % gm;
+    *tn = r / gm;
+}
+
+// Stream-K tail: every lane's share of the tail is at least this much of K
+// (so a partial store is amortised over at least two 256-wide chunks).
+constexpr int kTailMinK = 512;
+// The 3xTF32 kernel needs most of its operand tiles from L2 (each byte read
+// by several CTAs at about the same K): a stream-K tail, whose lanes run at
+// different K, keeps that only while the tail's A and B rows fit in L2, so
+// larger tails are cut into equal K slices instead (measured on GB300: a
+// 96 MiB tail ran as fast stream-K as sliced, a 208 MiB one 3 % slower
+// overall and a 512 MiB one 10 %).
+constexpr long long kTailL2Bytes = 112ll << 20;
+
 struct Plan {
     int M = 0, N = 0, K = 0;
     long long lda = 0, ldb = 0, ldc = 0;
@@ -33,11 +65,12 @@ struct Plan {
     int tiles_m = 0, tiles_n = 0;
     int pair = 1;        // 3xTF32: CTAs per cluster sharing one B tile (TMA multicast)
     long long units = 0; // work units (a unit is `pair` vertically adjacent tiles x one K slice)
-    // last-round balancing: the tile units past full_units are each cut into
-    // tail_split K slices (partials in the workspace, then a tail reduce)
+    // stream-K tail: the tile units past full_units (tail_units of them) are
+    // shared out over tail_lanes lanes, each running an equal share of their
+    // K blocks; pieces of a unit go to partial slots, then a tail reduce
     long long full_units = 0;
-    int tail_split = 1;
     long long tail_units = 0;
+    int tail_lanes = 0;
     int grid = 0;
     int num_sms = 0;     // SMs planned for
     int nkb = 0;         // K blocks of bk

@@ -53,11 +53,12 @@ struct GemmArgs {
     long long ldo;           // row stride of `out`
     long long slice_stride;  // elements between K-slice partials
     int vec_out;             // rows of `out` start on 16-byte boundaries
-    // last-round balancing: units >= full_units are the remaining tile units,
-    // each cut into tail_split K slices whose partials go to `tail`
-    // ([slot][pair*BM][BN] floats, slot = unit offset * tail_split + slice)
-    long long full_units;
-    int tail_split;
+    // stream-K tail: the tail_units tile units after full_units are shared
+    // out over tail_lanes lanes (see work_item); pieces of a unit go to
+    // partial slot 2*lane (a lane's first piece) or 2*lane + 1 (its last) of
+    // `tail` ([slot][pair*BM][BN] floats)
+    long long full_units, tail_units;
+    int tail_lanes;
     float* tail;
     // C = alpha * op(A) op(B) + beta * C, applied where C is written (scaled
     // = 0: a plain store of the product; beta == 0: C is not read)
@@ -73,45 +74,14 @@ struct Unit {
     bool direct;  // writes C itself (not a partial)
 };
 
-// Tile-unit index t (K slices aside) -> (tile-unit row, tile column).  Tiles
-// are visited in groups of kGroupM tile-unit rows, column by column inside a
-// group, so CTAs running at the same time share A rows and B columns in L2.
-constexpr int kGroupM = 8;
-
-__host__ __device__ __forceinline__ void unit_tile(int tiles_m, int tiles_n, long long t, int* tm,
-                                                   int* tn) {
-    const long long per_group = (long long)kGroupM * tiles_n;
-    const int g = (int)(t / per_group);
-    const int first_m = g * kGroupM;
-    const int gm = min(tiles_m - first_m, kGroupM);
-    const int r = (int)(t - g * per_group);
-    *tm = first_m + r % gm;
-    *tn = r / gm;
-}
-
 // Work unit u -> (K slice, output tile).  With pair = 2 a unit is two
 // vertically adjacent tiles; the CTA of cluster rank `rank` takes tile row
 // 2*row + rank.  Units below full_units cover their whole K range (or one of
-// `split` K slices); the units after them are the last round's tile units cut
-// into tail_split K slices each.
+// `split` K slices).
 __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int rank, int BM, int BN) {
     const long long tiles = (long long)a.tiles_m * a.tiles_n;
     Unit x;
     int tm, tn;
-    if (a.tail_split > 1 && u >= a.full_units) {
-        const long long v = u - a.full_units;
-        const int s = (int)(v % a.tail_split);
-        unit_tile(a.tiles_m, a.tiles_n, a.full_units + v / a.tail_split, &tm, &tn);
-        x.m0 = (tm * a.pair + rank) * BM;
-        x.n0 = tn * BN;
-        x.kb0 = (int)((long long)s * a.nkb / a.tail_split);
-        x.kb1 = (int)((long long)(s + 1) * a.nkb / a.tail_split);
-        // this slot's [pair*BM][BN] block, addressed with global row/column
-        x.ldo = BN;
-        x.out = a.tail + v * ((long long)a.pair * BM * BN) - (long long)tm * a.pair * BM * BN - x.n0;
-        x.direct = false;
-        return x;
-    }
     const int s = (int)(u / tiles);
     unit_tile(a.tiles_m, a.tiles_n, u - (long long)s * tiles, &tm, &tn);
     x.m0 = (tm * a.pair + rank) * BM;
@@ -122,6 +92,63 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, long long u, int 
     x.ldo = a.ldo;
     x.direct = a.split == 1;
     return x;
+}
+
+// Stream-K tail arithmetic.  The tail's T = tail_units * nkb K blocks are laid
+// end to end (tail unit q holds blocks [q*nkb, (q+1)*nkb)); lane v of the
+// tail_lanes runs blocks [v*T/tail_lanes, (v+1)*T/tail_lanes).
+__host__ __device__ __forceinline__ long long tail_run_begin(long long v, long long T, long long lanes) {
+    return v * T / lanes;
+}
+// The lane whose run holds K block x of the tail (the last v with begin <= x).
+__host__ __device__ __forceinline__ long long tail_lane_of(long long x, long long T, long long lanes) {
+    return ((x + 1) * lanes + T - 1) / T - 1;
+}
+
+// Work item j of one lane (a CTA, or a CTA pair) of `lanes`, in the order
+// the lane runs them: first the whole units lane, lane + lanes, ... below
+// full_units; then, for each tail lane v = lane, lane + lanes, ..., the
+// pieces of v's run, one per tail unit it meets.  Returns false past the last
+// item.  Every role of the CTA walks j = 0, 1, ... and so sees the same
+// sequence; only j is carried between items.
+__device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, long long lanes, long long j,
+                                          int rank, int BM, int BN, Unit* x) {
+    const long long nfull = a.full_units > lane ? (a.full_units - lane + lanes - 1) / lanes : 0;
+    if (j < nfull) {
+        *x = decode_unit(a, lane + j * lanes, rank, BM, BN);
+        return true;
+    }
+    j -= nfull;
+    const long long T = a.tail_units * a.nkb;
+    for (long long v = lane; v < a.tail_lanes; v += lanes) {
+        const long long s = tail_run_begin(v, T, a.tail_lanes);
+        const long long e = tail_run_begin(v + 1, T, a.tail_lanes);
+        if (s >= e) continue;
+        const long long q0 = s / a.nkb, pieces = (e - 1) / a.nkb - q0 + 1;
+        if (j >= pieces) {
+            j -= pieces;
+            continue;
+        }
+        const long long q = q0 + j, b0 = q * a.nkb;
+        int tm, tn;
+        unit_tile(a.tiles_m, a.tiles_n, a.full_units + q, &tm, &tn);
+        x->m0 = (tm * a.pair + rank) * BM;
+        x->n0 = tn * BN;
+        x->kb0 = (int)((s > b0 ? s : b0) - b0);
+        x->kb1 = (int)((e < b0 + a.nkb ? e : b0 + a.nkb) - b0);
+        x->direct = x->kb0 == 0 && x->kb1 == a.nkb;
+        if (x->direct) {  // the run holds the whole unit: C itself
+            x->out = a.out;
+            x->ldo = a.ldo;
+        } else {  // this slot's [pair*BM][BN] block, addressed with global row/column
+            const long long blk = (long long)a.pair * BM * BN;
+            const long long slot = 2 * v + (j == 0 ? 0 : 1);
+            x->out = a.tail + slot * blk - (long long)tm * blk - x->n0;
+            x->ldo = BN;
+        }
+        return true;
+    }
+    return false;
 }
 
 // Store 4 consecutive values of one output row starting at column `col`,
@@ -233,8 +260,8 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-                const Unit t = decode_unit(args, u, 0, BM, BN);
+            Unit t;
+            for (long long j = 0; ok && work_item(args, blockIdx.x, gridDim.x, j, 0, BM, BN, &t); ++j) {
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteFfmaProducer)) {
                         ok = false;
@@ -265,8 +292,8 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
     const int lm = lane & 3, ln = lane >> 2;  // thread rows wm*32 + lm + 4i, columns 32j + 4ln + q
     int stage = 0;
     uint32_t phase = 0;
-    for (long long u = blockIdx.x; u < args.units; u += gridDim.x) {
-        const Unit t = decode_unit(args, u, 0, BM, BN);
+    Unit t;
+    for (long long j = 0; work_item(args, blockIdx.x, gridDim.x, j, 0, BM, BN, &t); ++j) {
         // acc[i][p] holds columns 32*(p/2) + 4ln + 2*(p%2) + {0, 1} of row i
         unsigned long long acc[8][8];
 #pragma unroll
@@ -456,8 +483,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
-            for (long long u = first_unit; ok && u < args.units; u += unit_stride) {
-                const Unit t = decode_unit(args, u, rank, BM, BN);
+            Unit t;
+            for (long long j = 0; ok && work_item(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     // with a pair, "empty" completes only when both CTAs are done
                     // with the stage, since this CTA's B half lands in both
@@ -495,8 +522,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             int stage = 0;
             uint32_t phase = 0, chunk = 0;
             bool ok = true;
-            for (long long u = first_unit; ok && u < args.units; u += unit_stride) {
-                const Unit t = decode_unit(args, u, rank, BM, BN);
+            Unit t;
+            for (long long j = 0; ok && work_item(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
                 for (int c0 = t.kb0; ok && c0 < t.kb1; c0 += kTfChunkKB, ++chunk) {
                     const int c1 = min(c0 + kTfChunkKB, t.kb1);
                     const uint32_t buf = chunk & 1u, par = (chunk >> 1) & 1u;
@@ -554,8 +581,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         const bool vec = args.vec_out != 0;
         uint32_t chunk = 0;
         bool ok = true;
-        for (long long u = first_unit; ok && u < args.units; u += unit_stride) {
-            const Unit t = decode_unit(args, u, rank, BM, BN);
+        Unit t;
+        for (long long j = 0; ok && work_item(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
@@ -771,31 +798,41 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Last-round tile units: C = sum of their tail_split K-slice partials, in
-// slice order (deterministic), float4 per thread.
+// Stream-K tail: every tail unit that more than one lane ran is the sum of
+// its pieces' partials, added in lane order (deterministic), float4 per
+// thread.  A unit run whole by one lane was stored by the GEMM kernel.
 __global__ void __launch_bounds__(256)
     tail_reduce_kernel(GemmArgs a, float* C, long long ldc, int BM, int BN, int vec_c) {
-    const long long tail_units = (a.units - a.full_units) / a.tail_split;
     const int rows = a.pair * BM, q4 = BN / 4;
     const long long block = (long long)rows * BN;
-    const long long total = tail_units * rows * q4;
+    const long long T = a.tail_units * a.nkb, lanes = a.tail_lanes;
+    const long long total = a.tail_units * rows * q4;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const long long q = i / ((long long)rows * q4);
         const int rem = (int)(i - q * rows * q4);
         const int r = rem / q4, c = (rem % q4) * 4;
+        const long long v0 = tail_lane_of(q * a.nkb, T, lanes);
+        const long long v1 = tail_lane_of((q + 1) * a.nkb - 1, T, lanes);
+        if (v0 == v1) continue;
         int tm, tn;
         unit_tile(a.tiles_m, a.tiles_n, a.full_units + q, &tm, &tn);
         const int m = tm * rows + r, n = tn * BN + c;
         if (m >= a.M || n >= a.N) continue;
-        const float* p = a.tail + q * a.tail_split * block + (long long)r * BN + c;
-        float4 s = *reinterpret_cast<const float4*>(p);
-        for (int t = 1; t < a.tail_split; ++t) {
-            const float4 v = *reinterpret_cast<const float4*>(p + t * block);
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (long long v = v0; v <= v1; ++v) {
+            // slot 2v holds lane v's first piece, 2v + 1 its last
+            const long long first_q = tail_run_begin(v, T, lanes) / a.nkb;
+            const long long slot = 2 * v + (first_q == q ? 0 : 1);
+            const float4 x = *reinterpret_cast<const float4*>(a.tail + slot * block + (long long)r * BN + c);
+            if (v == v0) {
+                s = x;
+            } else {
+                s.x += x.x;
+                s.y += x.y;
+                s.z += x.z;
+                s.w += x.w;
+            }
         }
         if (a.scaled)
             store_row4_scaled(C + (long long)m * ldc, n, a.N, s, vec_c != 0, a.alpha, a.beta);
@@ -953,8 +990,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     ga.nkb = p.nkb;
     ga.units = p.units;
     ga.full_units = p.full_units;
-    ga.tail_split = p.tail_split;
-    ga.tail = p.tail_split > 1 ? reinterpret_cast<float*>(w + p.off_tail) : nullptr;
+    ga.tail_units = p.tail_units;
+    ga.tail_lanes = p.tail_lanes;
+    ga.tail = p.tail_lanes > 0 ? reinterpret_cast<float*>(w + p.off_tail) : nullptr;
     ga.alpha = p.alpha;
     ga.beta = p.beta;
     ga.scaled = (p.alpha != 1.0f || p.beta != 0.0f) ? 1 : 0;
@@ -1065,7 +1103,7 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
     }
 
-    if (p.tail_split > 1) {
+    if (p.tail_lanes > 0) {
         const long long work = p.tail_units * p.pair * p.bm * (p.bn / 4);
         tail_reduce_kernel<<<elementwise_grid(work, 256), 256, 0, stream>>>(ga, C, p.ldc, p.bm, p.bn,
                                                                            p.vec_c ? 1 : 0);

@@ -89,8 +89,8 @@ extern "C" tg_status tg_sgemm_noalloc(int M, int N, int K, const float* A, int l
     Plan p;
     make_plan(TG_OP_N, TG_OP_N, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, TG_PATH_TF32X3, 0,
               d->num_sms, &p);
-    if (p.ws_bytes > TG_SGEMM_NOALLOC_SCRATCH_BYTES && (p.split > 1 || p.tail_split > 1))
-        // drop the split and last-round partials
+    if (p.ws_bytes > TG_SGEMM_NOALLOC_SCRATCH_BYTES && (p.split > 1 || p.tail_lanes > 0))
+        // drop the split and stream-K tail partials
         make_plan(TG_OP_N, TG_OP_N, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, TG_PATH_TF32X3, 1,
                   d->num_sms, &p);
     if (p.ws_bytes > TG_SGEMM_NOALLOC_SCRATCH_BYTES) return TG_ERR_WORKSPACE_TOO_SMALL;

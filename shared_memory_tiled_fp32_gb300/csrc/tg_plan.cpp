@@ -13,6 +13,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <vector>
 
 #include "tg_internal.h"
 
@@ -25,6 +26,28 @@ inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
 bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
     return a0 < b1 && b0 < a1;
+}
+
+// Bytes of the 3xTF32 operand copies (A_hi, A_lo rows; B_hi, B_lo columns)
+// that the last `rem` tile units of the raster read.
+long long tail_operand_bytes(const Plan& p, long long rem) {
+    const int prow = (int)cdiv(p.tiles_m, p.pair);
+    const long long units = (long long)prow * p.tiles_n;
+    std::vector<int> rows_seen, cols_seen;
+    for (long long t = units - rem; t < units; ++t) {
+        int tm = 0, tn = 0;
+        unit_tile(prow, p.tiles_n, t, &tm, &tn);
+        rows_seen.push_back(tm);
+        cols_seen.push_back(tn);
+    }
+    std::sort(rows_seen.begin(), rows_seen.end());
+    std::sort(cols_seen.begin(), cols_seen.end());
+    rows_seen.erase(std::unique(rows_seen.begin(), rows_seen.end()), rows_seen.end());
+    cols_seen.erase(std::unique(cols_seen.begin(), cols_seen.end()), cols_seen.end());
+    long long rows = 0, cols = 0;
+    for (int i : rows_seen) rows += std::min<long long>((long long)p.pair * p.bm, p.M - (long long)i * p.pair * p.bm);
+    for (int j : cols_seen) cols += std::min<long long>(p.bn, p.N - (long long)j * p.bn);
+    return (rows + cols) * p.k4 * 8;
 }
 
 }  // namespace
@@ -116,25 +139,42 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     const bool pair_off = pair_env != nullptr && std::strcmp(pair_env, "0") == 0;
     p->pair = (p->path == TG_PATH_TF32X3 && p->tiles_m >= 2 && num_sms >= 2 && !pair_off) ? 2 : 1;
     p->units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n * S;
-    p->grid = p->pair * (int)std::min<long long>(p->units, num_sms / p->pair);
+    const long long cap = num_sms / p->pair;  // units in flight at once (lanes)
+    p->grid = p->pair * (int)std::min<long long>(p->units, cap);
     p->full_units = p->units;
 
-    // Last-round balancing.  When the units do not divide into whole rounds of
-    // the resident CTAs (or pairs), the last round would leave most of them
-    // idle; instead its tile units are cut into tail_split K slices (at most
-    // 4, each at least 8 K blocks), so more CTAs share the last round.  Only
-    // with the automatic split and no K split.
-    const long long lanes = p->grid / p->pair;  // units in flight at once
-    if (split_k == 0 && S == 1 && p->units > lanes) {
-        const long long rem = p->units % lanes;
-        if (rem > 0 && 2 * rem <= lanes) {
-            int ts = (int)std::min<long long>(lanes / rem, 4);
-            while (ts > 1 && p->nkb < 8 * ts) --ts;
-            if (ts > 1) {
+    // Balancing the last round.  When the units do not divide into whole
+    // rounds of the lanes (or there are fewer units than lanes), the last
+    // round would leave lanes idle.  Instead its rem units (the tail) are
+    // shared out over L lanes: lane v runs K blocks [v*T/L, (v+1)*T/L) of the
+    // tail's T = rem * nkb K blocks laid end to end.  A run that holds a whole
+    // unit stores it to C; a part of a unit goes to a partial slot that the
+    // tail reduce adds up in lane order.
+    //  * stream-K (FFMA, and 3xTF32 while the tail's A and B rows fit in L2):
+    //    L = every lane, each share at least kTailMinK of K;
+    //  * equal K slices (3xTF32, larger tails): L = rem * ts, so each run is
+    //    one of ts equal K slices of one unit and the runs of a slice stay
+    //    at the same K across units (ts <= 4, each slice >= 8 K blocks, only
+    //    when that at least halves the last round).
+    // Taken when it shortens the last round by at least 10 %; only with the
+    // automatic split and no K split.
+    if (split_k == 0 && S == 1) {
+        const long long rem = p->units % cap;
+        if (rem > 0) {
+            long long L = 0;
+            if (p->path == TG_PATH_FFMA || tail_operand_bytes(*p, rem) <= kTailL2Bytes) {
+                const long long min_share = std::max<long long>(1, kTailMinK / p->bk);
+                L = std::min<long long>(cap, rem * p->nkb / min_share);
+            } else if (2 * rem <= cap) {
+                long long ts = std::min<long long>(cap / rem, 4);
+                while (ts > 1 && p->nkb < 8 * ts) --ts;
+                L = rem * ts;
+            }
+            if (L > rem && 10 * rem <= 9 * L) {
                 p->full_units = p->units - rem;
                 p->tail_units = rem;
-                p->tail_split = ts;
-                p->units = p->full_units + rem * ts;
+                p->tail_lanes = (int)L;
+                p->grid = p->pair * (int)std::max<long long>(std::min<long long>(p->units, cap), L);
             }
         }
     }
@@ -171,11 +211,11 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->part_stride = (long long)M * p->n4;
         p->off_part = take(4ull * S * M * p->n4);
     }
-    if (p->tail_split > 1)
-        p->off_tail = take(4ull * p->tail_units * p->tail_split * p->pair * p->bm * p->bn);
+    if (p->tail_lanes > 0)  // two partial slots per lane: its first and its last piece
+        p->off_tail = take(4ull * 2 * p->tail_lanes * p->pair * p->bm * p->bn);
     p->ws_bytes = off;
     const bool prepass = p->path == TG_PATH_TF32X3 || p->pack_a || p->pack_b;
-    p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_split > 1 ? 1 : 0);
+    p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_lanes > 0 ? 1 : 0);
 }
 
 }  // namespace tg

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import shared_memory_tiled_fp32_gb300 as tg
@@ -31,7 +32,7 @@ def test_library_exports_header_symbols():
 
 
 def test_version_and_status_strings():
-    assert tg.lib().tg_sgemm_version() == 100
+    assert tg.lib().tg_sgemm_version() == 101
     for code, name in tg.STATUS.items():
         assert tg.status_string(code).startswith(name)
 
@@ -71,15 +72,31 @@ def test_plan_tiles_split_and_workspace():
     p = tg.plan(8192, 8192, 8192, num_sms=sms)
     assert (p["path"], p["tiles_m"], p["tiles_n"], p["split_k"]) == ("tf32x3", 64, 32, 1)
     # pairs of vertically adjacent tiles share B (cluster of 2 CTAs); 1024 pair
-    # units on 76 pairs leave 36 for a last round, which is cut into 2 K slices
+    # units on 76 pairs leave 36 after 13 whole rounds.  Their A and B rows
+    # (2048 rows + 1280 columns of K = 8192, hi and lo) exceed L2, so each is
+    # cut into 2 equal K slices: 72 lanes, half a round
     assert p["pair"] == 2 and p["grid"] == sms and p["launches"] == 3
-    assert (p["tail_units"], p["tail_split"]) == (36, 2)
-    assert p["units"] == (32 * 32 - 36) + 36 * 2
-    # A_hi, A_lo, B_hi^T, B_lo^T, plus the tail partials: 36 units x 2 slices x 256 x 256
-    assert p["workspace_bytes"] == 4 * 8192 * 8192 * 4 + 36 * 2 * 256 * 256 * 4
-    # an explicit split turns the last-round balancing off
+    assert (p["tail_units"], p["tail_lanes"]) == (36, 72)
+    assert p["units"] == 32 * 32
+    # A_hi, A_lo, B_hi^T, B_lo^T, plus two partial slots of 256 x 256 per lane
+    assert p["workspace_bytes"] == 4 * 8192 * 8192 * 4 + 2 * 72 * 256 * 256 * 4
+    # 4096^3: the 28-unit tail's rows fit in L2 -> stream-K over all 76 pairs
+    m = tg.plan(4096, 4096, 4096, num_sms=sms)
+    assert (m["units"], m["tail_units"], m["tail_lanes"]) == (256, 28, 76)
+    # an explicit split turns the tail balancing off
     q = tg.plan(8192, 8192, 8192, num_sms=sms, split_k=1)
     assert q["tail_units"] == 0 and q["units"] == 1024 and q["launches"] == 2
+    # long K, fewer units than lanes: FFMA (128 units, 152 CTAs) runs all of it
+    # stream-K on every CTA; 3xTF32 (64 pair units, rows far past L2, more
+    # than half a round) keeps whole units
+    lk = tg.plan(2048, 2048, 16384, num_sms=sms, path="ffma")
+    assert (lk["units"], lk["tail_units"], lk["tail_lanes"], lk["grid"]) == (128, 128, 152, sms)
+    lt = tg.plan(2048, 2048, 16384, num_sms=sms)
+    assert (lt["units"], lt["tail_units"], lt["grid"]) == (64, 0, 128)
+    # a tail that fills 90 % of a round or more is left alone
+    assert tg.plan(128 * 2 * 70, 256, 4096, num_sms=sms)["tail_units"] == 0
+    # a short K gives too little work per lane to share out
+    assert tg.plan(4096, 4096, 128, num_sms=sms)["tail_units"] == 0
     # ragged: ceil(777/128) x ceil(1029/256) tiles, split to fill the SMs
     p = tg.plan(777, 1029, 513, num_sms=sms)
     assert (p["tiles_m"], p["tiles_n"]) == (7, 5)
@@ -105,6 +122,66 @@ def test_plan_tiles_split_and_workspace():
     # K = 0 is one fill kernel
     z = tg.plan(10, 10, 0, num_sms=sms)
     assert z["launches"] == 1 and z["workspace_bytes"] == 0
+
+
+def _tail_pieces(tail_units, nkb, lanes):
+    """The stream-K tail as the GEMM kernels walk it: lane v runs K blocks
+    [v*T/lanes, (v+1)*T/lanes) of the T = tail_units * nkb blocks laid end to
+    end, one piece per tail unit it meets; a piece short of its whole unit
+    writes partial slot 2v (the lane's first piece) or 2v + 1 (its last)."""
+    T = tail_units * nkb
+    for v in range(lanes):
+        s, e = v * T // lanes, (v + 1) * T // lanes
+        q = q0 = s // nkb
+        while q * nkb < e and s < e:
+            lo, hi = max(s, q * nkb) - q * nkb, min(e, (q + 1) * nkb) - q * nkb
+            direct = lo == 0 and hi == nkb
+            yield v, q, lo, hi, None if direct else 2 * v + (0 if q == q0 else 1)
+            q += 1
+
+
+@pytest.mark.parametrize("M,N,K,path,sliced", [
+    (8192, 8192, 8192, "tf32x3", True), (4000, 3900, 8000, "tf32x3", True), (4096, 4096, 4096, "tf32x3", False),
+    (1000, 3000, 1100, "tf32x3", False), (8192, 8192, 8192, "ffma", False), (2048, 2048, 16384, "ffma", False),
+    (400, 8000, 20000, "ffma", False)])
+def test_tail_runs_cover_every_unit_once(M, N, K, path, sliced):
+    """Host model of the balanced last round of a plan: every K block of
+    every tail unit is run exactly once, a lane writes at most its two slots,
+    and the reduce's lookup (lanes holding the unit's first to last K block,
+    slot 2v when the unit is the lane's first) finds exactly the pieces
+    written.  With equal K slices every run lies inside one unit."""
+    p = tg.plan(M, N, K, num_sms=152, path=path)
+    tu, L, nkb = p["tail_units"], p["tail_lanes"], -(-K // p["block_k"])
+    assert tu > 0 and L > tu and 10 * tu <= 9 * L
+    assert (p["units"] - tu) % (p["grid"] // p["pair"]) == 0 or p["units"] < L
+    T = tu * nkb
+    if sliced:
+        assert L % tu == 0 and 2 <= L // tu <= 4 and nkb >= 8 * (L // tu)
+    else:
+        assert T // L >= 512 // p["block_k"]  # every lane's share is at least 512 of K
+    pieces = list(_tail_pieces(tu, nkb, L))
+    covered = np.zeros((tu, nkb), np.int32)
+    slots = {}
+    for v, q, lo, hi, slot in pieces:
+        assert 0 <= lo < hi <= nkb
+        covered[q, lo:hi] += 1
+        if slot is not None:
+            assert slot // 2 == v and slot not in slots
+            slots[slot] = q
+    assert np.all(covered == 1)
+    lane_of = lambda x: ((x + 1) * L + T - 1) // T - 1
+    for q in range(tu):
+        v0, v1 = lane_of(q * nkb), lane_of((q + 1) * nkb - 1)
+        mine = [pc for pc in pieces if pc[1] == q]
+        assert [pc[0] for pc in mine] == list(range(v0, v1 + 1))
+        if v0 == v1:
+            assert mine[0][4] is None
+        else:
+            want = sorted(2 * v + (0 if (v * T // L) // nkb == q else 1) for v in range(v0, v1 + 1))
+            assert sorted(pc[4] for pc in mine) == want and all(slots[w] == q for w in want)
+    assert 2 * L * p["pair"] * p["block_m"] * p["block_n"] * 4 <= p["workspace_bytes"]
+    if sliced:
+        assert len(pieces) == L and all(slot in (None, 2 * v) for v, _, _, _, slot in pieces)
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (300, 7, 5000), (2048, 2048, 16384), (129, 257, 17)])

@@ -234,3 +234,44 @@ def test_tf32x3_cluster_pairs_on_and_off(tg, pair, monkeypatch):
         assert p["tiles_m"] == -(-M // 128)
         for split in (0, 1, 2):
             assert_close(run(tg, A, B, path="tf32x3", split_k=split), ref, K, f"pair={pair} {M}x{N}x{K} s{split}")
+
+
+TAIL_CASES = [(1000, 3000, 1100, "uniform", "tf32x3"), (1000, 3000, 1100, "int", "tf32x3"),
+              (4000, 3900, 8000, "uniform", "tf32x3"), (1000, 3000, 1100, "uniform", "ffma"),
+              (1000, 3000, 1100, "int", "ffma"), (400, 8000, 20000, "normal", "ffma")]
+
+
+@pytest.mark.parametrize("M,N,K,dist,path", TAIL_CASES)
+def test_balanced_tail(tg, M, N, K, dist, path):
+    """Shapes whose last round is shared out over more lanes than it has units
+    (pieces of a unit added by the tail reduce in lane order), with ragged
+    edges: stream-K runs on both paths, with fewer units than lanes and runs
+    shorter than a unit (some units spread over three lanes); equal K slices
+    on the 3xTF32 path when the tail's rows exceed L2 (4000 x 3900 x 8000).
+    Every output is checked; integer inputs bit-exactly."""
+    A, B = make_inputs(M, N, K, dist, 700 + K % 97)
+    p = tg.plan(M, N, K, path=path)
+    assert p["tail_units"] > 0 and p["tail_lanes"] > p["tail_units"]
+    ref = oracle.sgemm(A.numpy(), B.numpy())
+    got = run(tg, A, B, path=path)
+    if dist == "int":
+        assert_bitexact(got, ref, f"stream-K {path} {M}x{N}x{K}")
+    else:
+        assert_close(got, ref, K, f"stream-K {path} {M}x{N}x{K}")
+    again = run(tg, A, B, path=path)  # the fixed-order reduce gives the same bits
+    assert np.array_equal(got.view(np.uint32), again.view(np.uint32))
+
+
+@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+def test_balanced_tail_scaled(tg, path):
+    """alpha and beta on a stream-K plan: applied by the GEMM epilogue for
+    units one lane ran whole and by the tail reduce for the others."""
+    M, N, K = 1000, 3000, 1100
+    A, B = make_inputs(M, N, K, "uniform", 731)
+    C0 = np.random.default_rng(732).uniform(-1, 1, (M, N)).astype(np.float32)
+    Cd = torch.from_numpy(C0.copy()).cuda()
+    tg.matmul_general(A.cuda(), B.cuda(), Cd, alpha=0.5, beta=-1.5, path=path)
+    torch.cuda.synchronize()
+    assert tg.sync_status() == 0
+    ref = oracle.sgemm_general(0, 0, 0.5, A.numpy(), B.numpy(), -1.5, C0.copy())
+    assert_close(Cd.cpu().numpy(), ref, K, f"stream-K scaled {path}")
