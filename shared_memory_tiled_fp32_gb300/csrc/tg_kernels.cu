@@ -20,7 +20,9 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "tg_internal.h"
 #include "tg_ptx.cuh"
@@ -251,6 +253,8 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dep_wait();  // the operands (or their packed copies) are complete
+    grid_dep_launch();
 
     if (warp < 4) {  // ---------------------------------------- producer
         regs_dec<kFfmaProducerRegs>();
@@ -472,6 +476,9 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     if (kPair > 1) cluster_sync_all();  // the peer's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // the set-up above overlaps the end of the pre-pass; its output is read below
+    grid_dep_wait();
+    grid_dep_launch();
 
     if (warp < 4) {
         regs_dec<kTfIssueRegs>();
@@ -757,6 +764,7 @@ __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*til
 template <bool SPLIT>
 __global__ void __launch_bounds__(256) prepass_kernel(PrepassArgs a) {
     __shared__ float tile[64][65];
+    grid_dep_launch();  // the GEMM may start its set-up as this pass drains
 #pragma unroll 1
     for (int k = 0; k < 2; ++k) {
         const OperandPass& p = a.op[k];
@@ -777,6 +785,7 @@ __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ part, long long ldp, long long slice, int S,
                          float* C, long long ldc, int M, int N, int vec_c, int scaled, float alpha,
                          float beta) {
+    grid_dep_wait();  // every partial is written
     const int n4g = (N + 3) / 4;
     const long long total = (long long)M * n4g;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -803,6 +812,7 @@ __global__ void __launch_bounds__(256)
 // thread.  A unit run whole by one lane was stored by the GEMM kernel.
 __global__ void __launch_bounds__(256)
     tail_reduce_kernel(GemmArgs a, float* C, long long ldc, int BM, int BN, int vec_c) {
+    grid_dep_wait();  // every partial is written
     const int rows = a.pair * BM, q4 = BN / 4;
     const long long block = (long long)rows * BN;
     const long long T = a.tail_units * a.nkb, lanes = a.tail_lanes;
@@ -918,6 +928,49 @@ int elementwise_grid(long long work, int per_block) {
 
 tg_status last_launch_status() {
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+// Kernels after the first of a call are launched with programmatic stream
+// serialization (programmatic dependent launch), so their launch and set-up
+// overlap the end of the kernel before them; each waits (grid_dep_wait)
+// before it reads that kernel's output.  TG_PDL=0 launches them plainly.
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("TG_PDL");
+        return !(e != nullptr && std::strcmp(e, "0") == 0);
+    }();
+    return on;
+}
+
+template <typename... KArgs, typename... Args>
+tg_status launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           unsigned cluster, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_CUDA;
+    }
+    return TG_OK;
 }
 
 }  // namespace
@@ -1053,24 +1106,14 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         if (p.pair == 2) {
             int clusters = p.grid / 2;
             if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
-            cudaLaunchConfig_t cfg{};
-            cfg.gridDim = dim3(2 * clusters);
-            cfg.blockDim = dim3(kTfThreads);
-            cfg.dynamicSmemBytes = kTfSmemBytes;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr{};
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = 2;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            if (cudaLaunchKernelEx(&cfg, tf32x3_gemm_kernel<2>, mAhi, mAlo, mBhi, mBlo, ga) != cudaSuccess)
+            if (launch_dependent(tf32x3_gemm_kernel<2>, dim3(2 * clusters), dim3(kTfThreads), kTfSmemBytes, stream, 2,
+                                 mAhi, mAlo, mBhi, mBlo, ga) != TG_OK)
                 return TG_ERR_CUDA;
         } else {
-            tf32x3_gemm_kernel<1><<<p.grid, kTfThreads, kTfSmemBytes, stream>>>(mAhi, mAlo, mBhi, mBlo, ga);
+            if (launch_dependent(tf32x3_gemm_kernel<1>, dim3(p.grid), dim3(kTfThreads), kTfSmemBytes, stream, 1,
+                                 mAhi, mAlo, mBhi, mBlo, ga) != TG_OK)
+                return TG_ERR_CUDA;
         }
-        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
     } else {
         const float* a_src = A;
@@ -1098,23 +1141,24 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
             !make_map(&mB, b_src, p.N, p.K, 4ull * b_row, kFfmaBN, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))
             return TG_ERR_CUDA;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
-        ffma_gemm_kernel<<<p.grid, kFfmaThreads, kFfmaSmemBytes, stream>>>(mA, mB, ga);
-        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+        if (launch_dependent(ffma_gemm_kernel, dim3(p.grid), dim3(kFfmaThreads), kFfmaSmemBytes, stream, 1, mA, mB,
+                             ga) != TG_OK)
+            return TG_ERR_CUDA;
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
     }
 
     if (p.tail_lanes > 0) {
         const long long work = p.tail_units * p.pair * p.bm * (p.bn / 4);
-        tail_reduce_kernel<<<elementwise_grid(work, 256), 256, 0, stream>>>(ga, C, p.ldc, p.bm, p.bn,
-                                                                           p.vec_c ? 1 : 0);
-        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+        if (launch_dependent(tail_reduce_kernel, dim3(elementwise_grid(work, 256)), dim3(256), 0, stream, 1, ga, C,
+                             (long long)p.ldc, p.bm, p.bn, p.vec_c ? 1 : 0) != TG_OK)
+            return TG_ERR_CUDA;
     }
     if (p.split > 1) {
         const long long work = (long long)p.M * ((p.N + 3) / 4);
-        splitk_reduce_kernel<<<elementwise_grid(work, 256), 256, 0, stream>>>(
-            ga.out, p.ldp, p.part_stride, p.split, C, p.ldc, p.M, p.N, p.vec_c ? 1 : 0, ga.scaled, p.alpha,
-            p.beta);
-        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+        if (launch_dependent(splitk_reduce_kernel, dim3(elementwise_grid(work, 256)), dim3(256), 0, stream, 1,
+                             (const float*)ga.out, p.ldp, p.part_stride, p.split, C, (long long)p.ldc, p.M, p.N,
+                             p.vec_c ? 1 : 0, ga.scaled, p.alpha, p.beta) != TG_OK)
+            return TG_ERR_CUDA;
     }
     return TG_OK;
 }

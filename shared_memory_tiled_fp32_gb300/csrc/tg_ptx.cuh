@@ -143,6 +143,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may begin while the kernel before it in the stream is still
+// running; grid_dep_wait() returns once that kernel has completed and its
+// memory operations are visible (a no-op without the launch attribute), and
+// grid_dep_launch() allows the next such kernel to begin launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Every thread of every CTA in the cluster must execute this.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
