@@ -160,9 +160,26 @@ size_t tg_sgemm_workspace_bytes(int M, int N, int K, const void* A, int lda, con
  * gives asynchronous copies).  Copies A and B to device memory allocated
  * stream-ordered on `stream`, computes C = A x B there, copies C back and
  * synchronises `stream` before returning, so C is ready on return.  Also
- * returns TG_ERR_TIMEOUT if a kernel of this call gave up a wait. */
+ * returns TG_ERR_TIMEOUT if a kernel of this call gave up a wait.
+ * Large products are pipelined: C is cut into row x column blocks (see
+ * tg_sgemm_host_blocks), the first product starts once its A row block and
+ * B column block are on the device, and the copies of the other blocks (in
+ * on one copy stream, C out on another) overlap the products.  opts->split_k
+ * and path apply to every block's product; workspace, main_begin and main_end
+ * are ignored.  Below 2^33 multiply-adds (M*N*K) there is one block and C is
+ * bit-identical to tg_sgemm's; above, each block's product is planned on its
+ * own, so the K split and the order of the partial sums (the low bits) may
+ * differ, within the same error bounds. */
 tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                         float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts);
+
+/* The output blocks tg_sgemm_host would use (host arithmetic only): C is cut
+ * into *row_blocks x *col_blocks blocks of *block_rows x *block_cols (the last
+ * ones ragged), chosen to minimise a modelled pipeline time, returned in
+ * *model_ms (copies at the rates measured on GB300).  path as in
+ * tg_sgemm_opts; num_sms = SMs planned for (0 = the current device). */
+tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* row_blocks,
+                               int* col_blocks, int* block_rows, int* block_cols, double* model_ms);
 
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns TG_ERR_TIMEOUT if any kernel of this library on this device gave up

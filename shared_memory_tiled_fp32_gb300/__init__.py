@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     STATUS,
     TgError,
     error_site,
+    host_blocks,
     lib,
     matmul,
     matmul_general,

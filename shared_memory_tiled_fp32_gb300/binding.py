@@ -34,6 +34,7 @@ EXPORTS = (
     "tg_sgemm_plan_general",
     "tg_sgemm_workspace_bytes",
     "tg_sgemm_host",
+    "tg_sgemm_host_blocks",
     "tg_sgemm_noalloc",
     "tg_sgemm_sync_status",
     "tg_sgemm_error_site",
@@ -113,6 +114,9 @@ def lib():
         L.tg_sgemm_host.restype = i
         L.tg_sgemm_noalloc.argtypes = gemm
         L.tg_sgemm_noalloc.restype = i
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.tg_sgemm_host_blocks.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ctypes.POINTER(ctypes.c_double)]
+        L.tg_sgemm_host_blocks.restype = i
         L.tg_sgemm_plan.argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
         L.tg_sgemm_plan.restype = i
         f = ctypes.c_float
@@ -332,6 +336,17 @@ def sgemm_host(A, B, out, *, path="auto", split_k=0, stream=None):
                              _stream_handle(stream), ctypes.byref(o))
     _check(st, "tg_sgemm_host")
     return out
+
+
+def host_blocks(M, N, K, *, path="auto", num_sms=0) -> dict:
+    """The row x column output blocks sgemm_host pipelines (host arithmetic)."""
+    r = [ctypes.c_int() for _ in range(4)]
+    ms = ctypes.c_double()
+    st = lib().tg_sgemm_host_blocks(M, N, K, PATHS[path] if isinstance(path, str) else int(path), num_sms,
+                                    *[ctypes.byref(x) for x in r], ctypes.byref(ms))
+    _check(st, "tg_sgemm_host_blocks")
+    return {"row_blocks": r[0].value, "col_blocks": r[1].value, "block_rows": r[2].value,
+            "block_cols": r[3].value, "model_ms": ms.value}
 
 
 def plan(M, N, K, lda=None, ldb=None, ldc=None, *, A=0, B=0, C=0, path="auto", split_k=0,

@@ -24,12 +24,14 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 
-// Copy streams and events of the host-buffer entry point, per device.
-constexpr int kMaxHostBlocks = 8;
+// Copy streams and events of the host-buffer entry point, per device: one
+// event per copy in (8 row + 8 column blocks at most), one per output block
+// (64 at most), and three for the start and the end of a call.
+constexpr int kMaxHostEvents = 3 + 16 + 64;
 struct HostPipe {
     bool ready = false;
     cudaStream_t s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev[3 + 2 * kMaxHostBlocks] = {};
+    cudaEvent_t ev[kMaxHostEvents] = {};
     std::mutex mu;
 };
 HostPipe g_host[kMaxDevices];
@@ -243,28 +245,31 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     const int path = o.path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3;
     const bool tf32 = path == TG_PATH_TF32X3;
     const long long k4 = ((long long)std::max(K, 1) + 3) / 4 * 4, n4 = ((long long)N + 3) / 4 * 4;
-    // Row blocks: on large products the copies of one block overlap the
-    // product of another (A in, C out on two copy streams).
-    int P = 1;
-    if ((double)M * N * K >= 8589934592.0 && M >= 2048) P = std::min(kMaxHostBlocks, std::min(4, M / 1024));
-    const int mb = ((M + P - 1) / P + 127) / 128 * 128;
-    P = (M + mb - 1) / mb;
+    // Output blocks: C is cut into pm x pn blocks (A row blocks x B column
+    // blocks) so the first product needs only A_0 and B_0 on the device; the
+    // copies of later blocks (in on s_in, out on s_out) overlap the products
+    // of earlier ones.  A and B are split once, by the first product that
+    // reads each block, into shared hi/lo regions.
+    const HostBlocks hb = choose_host_blocks(M, N, K, path, d->num_sms);
+    const int pm = hb.pm, pn = hb.pn, mb = hb.mb, nb = hb.nb;
 
     // device copies: 16-byte row pitches, so TMA reads them in place
     const size_t a_bytes = 4ull * M * k4, b_bytes = 4ull * (size_t)std::max(K, 1) * n4,
                  c_bytes = 4ull * M * n4;
-    const size_t b_split = tf32 ? (4ull * N * k4 + kWsAlign - 1) / kWsAlign * kWsAlign : 0;
+    auto align = [](size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; };
+    const size_t b_split = tf32 ? align(4ull * N * k4) : 0;   // B_hi^T, B_lo^T: [N][k4] each
+    const size_t a_split = tf32 ? align(4ull * mb * k4) : 0;  // A_i hi, lo: [mb][k4] each
     // placeholder pointers with the alignment the real ones will have
     const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
-    size_t ws_max = 0;
-    for (int i = 0; i < P; ++i) {
-        const int Mi = std::min(mb, M - i * mb);
-        Plan pl;
-        make_plan(TG_OP_N, TG_OP_N, Mi, N, K, 1.0f, al, (int)k4, al, (int)n4, 0.0f, al, (int)n4, path,
-                  o.split_k, d->num_sms, &pl, tf32);
-        ws_max = std::max(ws_max, pl.ws_bytes);
-    }
-    const size_t ws_total = 2 * b_split + ws_max;
+    size_t ws_max = 0;  // over the (at most 4) block shapes: whole or ragged rows x columns
+    for (int i : {0, pm - 1})
+        for (int j : {0, pn - 1}) {
+            Plan pl;
+            make_plan(TG_OP_N, TG_OP_N, std::min(mb, M - i * mb), std::min(nb, N - j * nb), K, 1.0f, al, (int)k4,
+                      al, (int)n4, 0.0f, al, (int)n4, path, o.split_k, d->num_sms, &pl, tf32, tf32);
+            ws_max = std::max(ws_max, pl.ws_bytes);
+        }
+    const size_t ws_total = 2 * b_split + 2 * a_split + ws_max;
 
     void *dA = nullptr, *dB = nullptr, *dC = nullptr, *W = nullptr;
     if (cudaMallocFromPoolAsync(&dA, a_bytes, d->pool, stream) != cudaSuccess ||
@@ -281,50 +286,71 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     float* fB = static_cast<float*>(dB);
     float* fC = static_cast<float*>(dC);
     uint8_t* w8 = static_cast<uint8_t*>(W);
-    cudaEvent_t* ev = hp->ev;  // [0] alloc, [1] B in, [2+i] A_i in, [2+P+i] C_i done, [2+2P] out
+    float* bhi = reinterpret_cast<float*>(w8);
+    float* blo = reinterpret_cast<float*>(w8 + b_split);
+    float* ahi = reinterpret_cast<float*>(w8 + 2 * b_split);
+    float* alo = reinterpret_cast<float*>(w8 + 2 * b_split + a_split);
+    uint8_t* wplan = w8 + 2 * b_split + 2 * a_split;
+    // events: [0] start, [1] end of the copies in, [2] end of the copies
+    // out, [3 + i] A_i in, [11 + j] B_j in, [19 + i*pn + j] C_ij computed
+    cudaEvent_t* ev = hp->ev;
     bool ok = cudaEventRecord(ev[0], stream) == cudaSuccess &&
               cudaStreamWaitEvent(hp->s_in, ev[0], 0) == cudaSuccess &&
               cudaStreamWaitEvent(hp->s_out, ev[0], 0) == cudaSuccess;
-    if (ok && K > 0) {
-        ok = cudaMemcpy2DAsync(fB, 4ull * n4, B, 4ull * ldb, 4ull * N, K, cudaMemcpyHostToDevice, hp->s_in) ==
-                 cudaSuccess &&
-             cudaEventRecord(ev[1], hp->s_in) == cudaSuccess;
-        for (int i = 0; ok && i < P; ++i) {
-            const int i0 = i * mb, Mi = std::min(mb, M - i0);
-            ok = cudaMemcpy2DAsync(fA + (size_t)i0 * k4, 4ull * k4, A + (size_t)i0 * lda, 4ull * lda, 4ull * K, Mi,
-                                   cudaMemcpyHostToDevice, hp->s_in) == cudaSuccess &&
-                 cudaEventRecord(ev[2 + i], hp->s_in) == cudaSuccess;
-        }
+    auto copy_a = [&](int i) {
+        const int i0 = i * mb, Mi = std::min(mb, M - i0);
+        ok = ok &&
+             cudaMemcpy2DAsync(fA + (size_t)i0 * k4, 4ull * k4, A + (size_t)i0 * lda, 4ull * lda, 4ull * K, Mi,
+                               cudaMemcpyHostToDevice, hp->s_in) == cudaSuccess &&
+             cudaEventRecord(ev[3 + i], hp->s_in) == cudaSuccess;
+    };
+    auto copy_b = [&](int j) {
+        const int j0 = j * nb, Nj = std::min(nb, N - j0);
+        ok = ok &&
+             cudaMemcpy2DAsync(fB + j0, 4ull * n4, B + j0, 4ull * ldb, 4ull * Nj, K, cudaMemcpyHostToDevice,
+                               hp->s_in) == cudaSuccess &&
+             cudaEventRecord(ev[11 + j], hp->s_in) == cudaSuccess;
+    };
+    if (K > 0) {  // in the order the products first need them
+        copy_a(0);
+        for (int j = 0; j < pn; ++j) copy_b(j);
+        for (int i = 1; i < pm; ++i) copy_a(i);
     }
     st = ok ? TG_OK : TG_ERR_CUDA;
-    for (int i = 0; st == TG_OK && i < P; ++i) {
-        const int i0 = i * mb, Mi = std::min(mb, M - i0);
-        if (K > 0 && ((i == 0 && cudaStreamWaitEvent(stream, ev[1], 0) != cudaSuccess) ||
-                      cudaStreamWaitEvent(stream, ev[2 + i], 0) != cudaSuccess)) {
-            st = TG_ERR_CUDA;
-            break;
+    for (int i = 0; st == TG_OK && i < pm; ++i) {
+        for (int j = 0; st == TG_OK && j < pn; ++j) {
+            const int i0 = i * mb, Mi = std::min(mb, M - i0), j0 = j * nb, Nj = std::min(nb, N - j0);
+            if (K > 0 && ((j == 0 && cudaStreamWaitEvent(stream, ev[3 + i], 0) != cudaSuccess) ||
+                          (i == 0 && cudaStreamWaitEvent(stream, ev[11 + j], 0) != cudaSuccess))) {
+                st = TG_ERR_CUDA;
+                break;
+            }
+            const float* Ai = fA + (size_t)i0 * k4;
+            const float* Bj = fB + j0;
+            float* Cij = fC + (size_t)i0 * n4 + j0;
+            Plan pl;
+            make_plan(TG_OP_N, TG_OP_N, Mi, Nj, K, 1.0f, Ai, (int)k4, Bj, (int)n4, 0.0f, Cij, (int)n4, path,
+                      o.split_k, d->num_sms, &pl, tf32, tf32);
+            if (tf32) {  // A_i split by its first product (j == 0), B_j by its first (i == 0)
+                pl.ext_a0 = ahi;
+                pl.ext_a1 = alo;
+                pl.a_ready = j > 0;
+                pl.ext_b0 = bhi + (size_t)j0 * k4;
+                pl.ext_b1 = blo + (size_t)j0 * k4;
+                pl.b_ready = i > 0;
+            }
+            st = launch_plan(pl, Ai, Bj, Cij, wplan, stream, nullptr, nullptr);
+            if (st != TG_OK) break;
+            cudaEvent_t done = ev[19 + i * pn + j];
+            if (cudaEventRecord(done, stream) != cudaSuccess || cudaStreamWaitEvent(hp->s_out, done, 0) != cudaSuccess ||
+                cudaMemcpy2DAsync(C + (size_t)i0 * ldc + j0, 4ull * ldc, Cij, 4ull * n4, 4ull * Nj, Mi,
+                                  cudaMemcpyDeviceToHost, hp->s_out) != cudaSuccess)
+                st = TG_ERR_CUDA;
         }
-        const float* Ai = fA + (size_t)i0 * k4;
-        float* Ci = fC + (size_t)i0 * n4;
-        Plan pl;
-        make_plan(TG_OP_N, TG_OP_N, Mi, N, K, 1.0f, Ai, (int)k4, fB, (int)n4, 0.0f, Ci, (int)n4, path, o.split_k,
-                  d->num_sms, &pl, tf32);
-        if (tf32) {  // B is split once, by the first block, into the shared region
-            pl.ext_b0 = reinterpret_cast<float*>(w8);
-            pl.ext_b1 = reinterpret_cast<float*>(w8 + b_split);
-            pl.b_ready = i > 0;
-        }
-        st = launch_plan(pl, Ai, fB, Ci, w8 + 2 * b_split, stream, nullptr, nullptr);
-        if (st != TG_OK) break;
-        if (cudaEventRecord(ev[2 + P + i], stream) != cudaSuccess ||
-            cudaStreamWaitEvent(hp->s_out, ev[2 + P + i], 0) != cudaSuccess ||
-            cudaMemcpy2DAsync(C + (size_t)i0 * ldc, 4ull * ldc, Ci, 4ull * n4, 4ull * N, Mi, cudaMemcpyDeviceToHost,
-                              hp->s_out) != cudaSuccess)
-            st = TG_ERR_CUDA;
     }
     // the buffers are released on `stream` once both copy streams are done
-    cudaEventRecord(ev[2 + 2 * P], hp->s_out);
-    cudaStreamWaitEvent(stream, ev[2 + 2 * P], 0);
+    cudaEventRecord(ev[2], hp->s_out);
+    cudaStreamWaitEvent(stream, ev[2], 0);
     cudaEventRecord(ev[1], hp->s_in);
     cudaStreamWaitEvent(stream, ev[1], 0);
     for (void* q : {dA, dB, dC, W})
@@ -335,6 +361,28 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     st = read_error_word(stream, true, &word);
     if (st != TG_OK) return st;
     return word != 0 ? TG_ERR_TIMEOUT : TG_OK;
+}
+
+tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* row_blocks, int* col_blocks,
+                               int* block_rows, int* block_cols, double* model_ms) {
+    using namespace tg;
+    if (M < 0 || N < 0 || K < 0 || row_blocks == nullptr || col_blocks == nullptr || block_rows == nullptr ||
+        block_cols == nullptr)
+        return TG_ERR_INVALID_VALUE;
+    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3) return TG_ERR_INVALID_VALUE;
+    if (num_sms <= 0) {
+        DeviceState* d = nullptr;
+        const tg_status st = current_device(&d);
+        if (st != TG_OK) return st;
+        num_sms = d->num_sms;
+    }
+    const HostBlocks hb = choose_host_blocks(M, N, K, path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3, num_sms);
+    *row_blocks = hb.pm;
+    *col_blocks = hb.pn;
+    *block_rows = hb.mb;
+    *block_cols = hb.nb;
+    if (model_ms != nullptr) *model_ms = hb.model_ms;
+    return TG_OK;
 }
 
 tg_status tg_sgemm_sync_status(cudaStream_t stream) {

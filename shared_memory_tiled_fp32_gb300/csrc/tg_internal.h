@@ -84,11 +84,15 @@ struct Plan {
     long long part_stride = 0;   // elements between two K-slice partials
     size_t ws_bytes = 0;
     int launches = 0;
-    // 3xTF32 only: B_hi^T / B_lo^T live outside the workspace at ext_b0 /
-    // ext_b1 (planned with external_b); b_ready = they already hold op(B)'s
-    // split, so the pre-pass skips B
+    // 3xTF32 only: A_hi / A_lo (B_hi^T / B_lo^T) live outside the workspace
+    // at ext_a0 / ext_a1 (ext_b0 / ext_b1), planned with external_a
+    // (external_b); a_ready (b_ready) = they already hold that operand's
+    // split, so the pre-pass skips it (and is not launched if both are)
+    float* ext_a0 = nullptr;
+    float* ext_a1 = nullptr;
     float* ext_b0 = nullptr;
     float* ext_b1 = nullptr;
+    bool a_ready = false;
     bool b_ready = false;
 };
 
@@ -97,10 +101,20 @@ struct Plan {
 tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int lda, const void* B,
                    int ldb, const void* C, int ldc, int path, int split_k, bool need_pointers = true);
 
+// Output blocks of the host-buffer entry point: C is cut into pm x pn blocks
+// of mb rows (a multiple of 128) and nb columns (a multiple of 256); the
+// choice minimises a modelled pipeline time (copies in, products, copies
+// out).  Host arithmetic only.
+struct HostBlocks {
+    int pm = 1, pn = 1, mb = 0, nb = 0;
+    double model_ms = 0.0;
+};
+HostBlocks choose_host_blocks(int M, int N, int K, int path, int num_sms);
+
 // Fill `p` for the given call; num_sms > 0.  Assumes validate() passed.
 void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
                const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
-               int num_sms, Plan* p, bool external_b = false);
+               int num_sms, Plan* p, bool external_b = false, bool external_a = false);
 
 // Enqueue every kernel of plan `p` on `stream` (defined in tg_kernels.cu).
 tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, void* ws,

@@ -1085,15 +1085,17 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     const int prepass_grid = g_prepass_blocks_per_sm[p.path == TG_PATH_TF32X3 ? 1 : 0] * p.num_sms;
 
     if (p.path == TG_PATH_TF32X3) {
-        float* ahi = reinterpret_cast<float*>(w + p.off_a0);
-        float* alo = reinterpret_cast<float*>(w + p.off_a1);
+        float* ahi = p.ext_a0 ? p.ext_a0 : reinterpret_cast<float*>(w + p.off_a0);
+        float* alo = p.ext_a1 ? p.ext_a1 : reinterpret_cast<float*>(w + p.off_a1);
         float* bhi = p.ext_b0 ? p.ext_b0 : reinterpret_cast<float*>(w + p.off_b0);
         float* blo = p.ext_b1 ? p.ext_b1 : reinterpret_cast<float*>(w + p.off_b1);
         // A_hi/A_lo [M][k4] from op(A); B_hi/B_lo [N][k4] from op(B)^T
-        pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, ahi, alo);
+        pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, p.a_ready ? nullptr : ahi, alo);
         pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k4, p.op_b == TG_OP_N, p.b_ready ? nullptr : bhi, blo);
-        prepass_kernel<true><<<prepass_grid, 256, 0, stream>>>(pa);
-        if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+        if (!(p.a_ready && p.b_ready)) {
+            prepass_kernel<true><<<prepass_grid, 256, 0, stream>>>(pa);
+            if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
+        }
 
         CUtensorMap mAhi, mAlo, mBhi, mBlo;
         const uint64_t row = 4ull * p.k4;

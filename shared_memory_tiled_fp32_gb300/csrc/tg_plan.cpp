@@ -13,6 +13,9 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "tg_internal.h"
@@ -85,7 +88,7 @@ tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int l
 
 void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
                const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
-               int num_sms, Plan* p, bool external_b) {
+               int num_sms, Plan* p, bool external_b, bool external_a) {
     *p = Plan{};
     p->M = M;
     p->N = N;
@@ -188,8 +191,10 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     if (p->path == TG_PATH_TF32X3) {
         // hi/lo copies: A as [M][k4], B transposed as [N][k4] (both K-major)
         const size_t a_bytes = 4ull * M * p->k4, b_bytes = 4ull * N * p->k4;
-        p->off_a0 = take(a_bytes);
-        p->off_a1 = take(a_bytes);
+        if (!external_a) {  // else the caller provides A's hi/lo copies
+            p->off_a0 = take(a_bytes);
+            p->off_a1 = take(a_bytes);
+        }
         if (!external_b) {  // else the caller provides B's hi/lo copies
             p->off_b0 = take(b_bytes);
             p->off_b1 = take(b_bytes);
@@ -216,6 +221,122 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     p->ws_bytes = off;
     const bool prepass = p->path == TG_PATH_TF32X3 || p->pack_a || p->pack_b;
     p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_lanes > 0 ? 1 : 0);
+}
+
+// Modelled duration (seconds) of one planned product: its rounds of work
+// units over the lanes (whole rounds, plus the tail's share of a unit per
+// lane), each unit taking its tile's flops at the path's per-lane rate, plus
+// a fixed 25 us per product (pipeline fill and drain, reduce, launch gaps;
+// measured on GB300 for products of one to a few rounds).
+double product_seconds(const Plan& p, double rate) {
+    if (p.M == 0 || p.N == 0 || p.K == 0) return 5e-6;
+    const long long lanes = std::max(1, p.grid / p.pair);
+    double rounds;
+    if (p.tail_lanes > 0)
+        rounds = (double)(p.full_units / lanes) + (double)p.tail_units / p.tail_lanes;
+    else
+        rounds = (double)cdiv(p.units, lanes);
+    const double unit_flops = 2.0 * p.pair * p.bm * p.bn * ((double)p.K / p.split);
+    return rounds * unit_flops / (rate / std::max(1, p.num_sms / p.pair)) + 25e-6;
+}
+
+// Host-buffer pipeline model.  Copies in run on one copy stream in the order
+// the products first need them (A_0, B_0, B_1, ..., A_1, ...), the products
+// run in row-block-major order (i, j) on the compute stream, and each C block
+// is copied out on a second copy stream once its product is done.  Rates are
+// the ones measured on GB300: pinned host memory over NVLink-C2C about 200
+// GB/s in and 190 GB/s out, the split pre-pass about 5.7 TB/s, and a full
+// round of work units 355 (3xTF32) or 62 (FFMA) useful TFLOP/s.
+HostBlocks model_host_blocks(int M, int N, int K, int path, int num_sms) {
+    const bool tf32 = path != TG_PATH_FFMA;
+    const double bw_in = 200e9, bw_out = 190e9, bw_split = 5.7e12;
+    const double rate = tf32 ? 355e12 : 62e12;
+    const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
+    const int k4 = (int)round_up((size_t)std::max(K, 1), 4), n4 = (int)round_up((size_t)std::max(N, 1), 4);
+    HostBlocks best;
+    best.mb = (int)round_up((size_t)std::max(M, 1), 128);
+    best.nb = (int)round_up((size_t)std::max(N, 1), 256);
+    best.model_ms = -1.0;
+    if (M == 0 || N == 0) return best;
+    // below 2^33 multiply-adds one block: the launches would cost more than
+    // the copies they hide, and the result is then bit-identical to tg_sgemm's
+    const int max_blocks = (double)M * N * K >= 8589934592.0 ? 8 : 1;
+    for (int pm = 1; pm <= max_blocks; ++pm) {
+        for (int pn = 1; pn <= max_blocks; ++pn) {
+            const int mb = (int)round_up((size_t)cdiv(M, pm), 128), nb = (int)round_up((size_t)cdiv(N, pn), 256);
+            const int qm = (int)cdiv(M, mb), qn = (int)cdiv(N, nb);
+            if (qm != pm || qn != pn) continue;  // same blocks as a smaller count
+            if (pm > 1 && mb < 512) continue;
+            if (pn > 1 && nb < 512) continue;
+            // copies in
+            std::vector<double> a_ready(pm), b_ready(pn);
+            double t_in = 0.0;
+            auto copy_a = [&](int i) {
+                const int rows = std::min(mb, M - i * mb);
+                t_in += 4.0 * rows * K / bw_in;
+                a_ready[i] = t_in;
+            };
+            auto copy_b = [&](int j) {
+                const int cols = std::min(nb, N - j * nb);
+                t_in += 4.0 * cols * K / bw_in;
+                b_ready[j] = t_in;
+            };
+            copy_a(0);
+            for (int j = 0; j < pn; ++j) copy_b(j);
+            for (int i = 1; i < pm; ++i) copy_a(i);
+            // products and copies out; the blocks have at most 4 shapes
+            // (whole or ragged rows x whole or ragged columns)
+            double shape_s[2][2] = {{-1.0, -1.0}, {-1.0, -1.0}};
+            double t_gpu = 0.0, t_out = 0.0;
+            for (int i = 0; i < pm; ++i) {
+                for (int j = 0; j < pn; ++j) {
+                    const int rows = std::min(mb, M - i * mb), cols = std::min(nb, N - j * nb);
+                    double t = std::max({t_gpu, a_ready[i], b_ready[j]});
+                    if (tf32) {
+                        if (j == 0) t += 12.0 * rows * K / bw_split;
+                        if (i == 0) t += 12.0 * cols * K / bw_split;
+                    }
+                    double& ps = shape_s[i == pm - 1][j == pn - 1];
+                    if (ps < 0.0) {
+                        Plan pl;
+                        make_plan(TG_OP_N, TG_OP_N, rows, cols, K, 1.0f, al, k4, al, n4, 0.0f, al, n4, path, 0,
+                                  num_sms, &pl, tf32, tf32);
+                        ps = product_seconds(pl, rate);
+                    }
+                    t += ps;
+                    t_gpu = t;
+                    t_out = std::max(t_out, t) + 4.0 * rows * cols / bw_out;
+                }
+            }
+            const double ms = t_out * 1e3;
+            if (best.model_ms < 0.0 || ms < best.model_ms * 0.98) {  // prefer fewer blocks on near ties
+                best.pm = pm;
+                best.pn = pn;
+                best.mb = mb;
+                best.nb = nb;
+                best.model_ms = ms;
+            }
+        }
+    }
+    return best;
+}
+
+// The model's answer is remembered per shape (a few hundred plans are
+// evaluated on first use; later calls with the same shape only look it up).
+HostBlocks choose_host_blocks(int M, int N, int K, int path, int num_sms) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int>, HostBlocks> memo;
+    const auto key = std::make_tuple(M, N, K, path, num_sms);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = memo.find(key);
+        if (it != memo.end()) return it->second;
+    }
+    const HostBlocks hb = model_host_blocks(M, N, K, path, num_sms);
+    std::lock_guard<std::mutex> lock(mu);
+    if (memo.size() > 4096) memo.clear();
+    memo[key] = hb;
+    return hb;
 }
 
 }  // namespace tg

@@ -226,3 +226,35 @@ def test_general_plan_packs_transposed_operands():
          for a in (0, 1) for b in (0, 1)]
     assert len({x["workspace_bytes"] for x in t}) == 1
 
+
+
+@pytest.mark.parametrize("M,N,K,path", [(8192, 8192, 8192, "tf32x3"), (8192, 8192, 8192, "ffma"),
+                                        (4096, 4096, 4096, "tf32x3"), (2048, 2048, 16384, "tf32x3"),
+                                        (4100, 1030, 2050, "tf32x3"), (777, 1029, 513, "ffma"), (1, 1, 1, "tf32x3"),
+                                        (5000, 300, 0, "tf32x3")])
+def test_host_blocks_cover_c(M, N, K, path):
+    """The host entry's output blocks: rows in multiples of 128, columns in
+    multiples of 256, exactly covering C (the last ones ragged), at most 8 x 8."""
+    h = tg.host_blocks(M, N, K, path=path, num_sms=152)
+    pm, pn, mb, nb = h["row_blocks"], h["col_blocks"], h["block_rows"], h["block_cols"]
+    assert 1 <= pm <= 8 and 1 <= pn <= 8
+    assert mb % 128 == 0 and nb % 256 == 0
+    assert -(-M // mb) == pm and -(-N // nb) == pn
+    assert h["model_ms"] >= 0
+    if pm > 1:
+        assert mb >= 512
+    if pn > 1:
+        assert nb >= 512
+
+
+def test_host_blocks_pipeline_large_products():
+    """A large product is cut so that the first block's operands are a small
+    part of A and B, and the modelled time beats a single block."""
+    h = tg.host_blocks(8192, 8192, 8192, path="tf32x3", num_sms=152)
+    assert h["row_blocks"] * h["col_blocks"] >= 4
+    assert 4 * 8192 * (h["block_rows"] + h["block_cols"]) <= 0.5 * 4 * 8192 * 16384
+    assert tg.lib().tg_sgemm_host_blocks(-1, 4, 4, 0, 152, *[ctypes.byref(ctypes.c_int()) for _ in range(4)],
+                                         None) == 1
+    # below 2^33 multiply-adds: one block (bit-identical to the device entry)
+    small = tg.host_blocks(777, 1029, 513, path="tf32x3", num_sms=152)
+    assert (small["row_blocks"], small["col_blocks"]) == (1, 1)

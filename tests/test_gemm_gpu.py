@@ -205,6 +205,31 @@ def test_host_buffer_entry_row_blocks(tg, path):
     assert np.all(np.isnan(Cbig.numpy()[:, N:])), "host entry wrote past column N"
 
 
+@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+def test_host_buffer_entry_2d_blocks(tg, path):
+    """The host entry point with C cut into row x column blocks (ragged last
+    ones): every block's product waits for its own A row block and B column
+    block, A and B are split once and reused, C blocks are copied out as they
+    finish.  Sampled rows at and around every row-block edge, all columns."""
+    M, N, K = 4100, 3000, 1500
+    hb = tg.host_blocks(M, N, K, path=path)
+    assert hb["row_blocks"] > 1 and hb["col_blocks"] > 1
+    A, B = make_inputs(M, N, K, "uniform", 322)
+    Ap, Bp = A.pin_memory(), B.pin_memory()
+    Cbig = torch.full((M, N + 3), float("nan")).pin_memory()
+    C = Cbig[:, :N]
+    tg.sgemm_host(Ap, Bp, C, path=path)
+    mb = hb["block_rows"]
+    edges = [r for i in range(1, hb["row_blocks"]) for r in (i * mb - 1, i * mb)]
+    rows = np.sort(np.random.default_rng(4).choice(M, 120, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, M - 1], edges]))
+    ref = oracle.sgemm_rows(A.numpy(), B.numpy(), rows)
+    assert_close(C.numpy()[rows], ref, K, f"host 2-D blocks {path}")
+    assert np.all(np.isnan(Cbig.numpy()[:, N:])), "host entry wrote past column N"
+    dev = run(tg, A, B, path=path)  # same products as the device entry, block by block
+    assert_close(C.numpy(), dev, K, f"host vs device {path}")
+
+
 def test_side_stream(tg):
     A, B, _, ref = workload_case("sq256_uniform")
     s = torch.cuda.Stream()
