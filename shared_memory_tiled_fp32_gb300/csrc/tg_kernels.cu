@@ -659,10 +659,11 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 // Each operand is either copied row by row (its stored rows already run along
 // the destination rows) or transposed.  Memory-bound: the row-wise pass moves
 // 4 values per item with 16-byte stores (and 16-byte loads when the source
-// rows are 16-byte aligned), four items in flight per thread; the transpose
+// rows are 16-byte aligned), eight items in flight per thread; the transpose
 // runs on 64 x 64 tiles through a [64][65] shared tile, 16 values per thread
-// in flight; the padded row makes the column read conflict-free ("Bank
-// Conflict", padding: gcd(65, 32) = 1).  Loads and stores are row-coalesced.
+// in flight, the next tile's loads overlapping the current tile's stores;
+// the padded row makes the column read conflict-free ("Bank Conflict",
+// padding: gcd(65, 32) = 1).  Loads and stores are row-coalesced.
 
 struct OperandPass {
     const float* src;
@@ -708,13 +709,14 @@ __device__ __forceinline__ void store_split4(float* d0, float* d1, long long o, 
 
 template <bool SPLIT>
 __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
+    constexpr int kInFlight = 8;  // 16-byte loads issued before the first store
     const long long stride = (long long)gridDim.x * blockDim.x;
     const int groups = p.pitch / 4;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < p.items; i += 4 * stride) {
-        float4 v[4];
-        long long o[4];
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < p.items; i += kInFlight * stride) {
+        float4 v[kInFlight];
+        long long o[kInFlight];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kInFlight; ++u) {
             const long long it = i + u * stride;
             o[u] = -1;
             if (it < p.items) {
@@ -724,23 +726,38 @@ __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < kInFlight; ++u)
             if (o[u] >= 0) store_split4<SPLIT>(p.d0, p.d1, o[u], v[u]);
     }
 }
 
+// Source tile (r0, c0) of a transpose: this thread's 16 values, rows c0 + ty
+// + 4j of the source (destination columns), column r0 + tx (coalesced).
+__device__ __forceinline__ void transpose_load(const OperandPass& p, long long t, int tx, int ty, float* v) {
+    const int r0 = (int)(t / p.tiles_c) * 64, c0 = (int)(t % p.tiles_c) * 64;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int c = c0 + ty + 4 * j, r = r0 + tx;
+        v[j] = (c < p.cols && r < p.rows) ? p.src[(long long)c * p.ld + r] : 0.0f;
+    }
+}
+
+// The tiles are software-pipelined: the loads of a block's next tile are
+// issued before the stores of the current one, so reads stay in flight while
+// the block writes.
 template <bool SPLIT>
 __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*tile)[65]) {
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4 threads
-    for (long long t = blockIdx.x; t < p.items; t += gridDim.x) {
+    long long t = blockIdx.x;
+    if (t >= p.items) return;
+    float v[16];
+    transpose_load(p, t, tx, ty, v);
+    for (; t < p.items; t += gridDim.x) {
         const int r0 = (int)(t / p.tiles_c) * 64, c0 = (int)(t % p.tiles_c) * 64;
-        // source row c, column r: coalesced along r
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int c = c0 + ty + 4 * j, r = r0 + tx;
-            tile[ty + 4 * j][tx] = (c < p.cols && r < p.rows) ? p.src[(long long)c * p.ld + r] : 0.0f;
-        }
+        for (int j = 0; j < 16; ++j) tile[ty + 4 * j][tx] = v[j];
         __syncthreads();
+        if (t + gridDim.x < p.items) transpose_load(p, t + gridDim.x, tx, ty, v);
         // destination row r, column c: coalesced along c
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
