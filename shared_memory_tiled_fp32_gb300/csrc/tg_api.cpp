@@ -257,8 +257,9 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     const size_t a_bytes = 4ull * M * k4, b_bytes = 4ull * (size_t)std::max(K, 1) * n4,
                  c_bytes = 4ull * M * n4;
     auto align = [](size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; };
-    const size_t b_split = tf32 ? align(4ull * N * k4) : 0;   // B_hi^T, B_lo^T: [N][k4] each
-    const size_t a_split = tf32 ? align(4ull * mb * k4) : 0;  // A_i hi, lo: [mb][k4] each
+    const long long k16 = ((long long)std::max(K, 1) + 15) / 16 * 16;
+    const size_t b_split = tf32 ? align(8ull * N * k16) : 0;   // B^T's interleaved hi/lo: [N][2*k16]
+    const size_t a_split = tf32 ? align(8ull * mb * k16) : 0;  // A_i's interleaved hi/lo: [mb][2*k16]
     // placeholder pointers with the alignment the real ones will have
     const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
     size_t ws_max = 0;  // over the (at most 4) block shapes: whole or ragged rows x columns
@@ -269,7 +270,7 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
                       al, (int)n4, 0.0f, al, (int)n4, path, o.split_k, d->num_sms, &pl, tf32, tf32);
             ws_max = std::max(ws_max, pl.ws_bytes);
         }
-    const size_t ws_total = 2 * b_split + 2 * a_split + ws_max;
+    const size_t ws_total = b_split + a_split + ws_max;
 
     void *dA = nullptr, *dB = nullptr, *dC = nullptr, *W = nullptr;
     if (cudaMallocFromPoolAsync(&dA, a_bytes, d->pool, stream) != cudaSuccess ||
@@ -286,11 +287,9 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     float* fB = static_cast<float*>(dB);
     float* fC = static_cast<float*>(dC);
     uint8_t* w8 = static_cast<uint8_t*>(W);
-    float* bhi = reinterpret_cast<float*>(w8);
-    float* blo = reinterpret_cast<float*>(w8 + b_split);
-    float* ahi = reinterpret_cast<float*>(w8 + 2 * b_split);
-    float* alo = reinterpret_cast<float*>(w8 + 2 * b_split + a_split);
-    uint8_t* wplan = w8 + 2 * b_split + 2 * a_split;
+    float* b_cat = reinterpret_cast<float*>(w8);
+    float* a_cat = reinterpret_cast<float*>(w8 + b_split);
+    uint8_t* wplan = w8 + b_split + a_split;
     // events: [0] start, [1] end of the copies in, [2] end of the copies
     // out, [3 + i] A_i in, [11 + j] B_j in, [19 + i*pn + j] C_ij computed
     cudaEvent_t* ev = hp->ev;
@@ -332,11 +331,9 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
             make_plan(TG_OP_N, TG_OP_N, Mi, Nj, K, 1.0f, Ai, (int)k4, Bj, (int)n4, 0.0f, Cij, (int)n4, path,
                       o.split_k, d->num_sms, &pl, tf32, tf32);
             if (tf32) {  // A_i split by its first product (j == 0), B_j by its first (i == 0)
-                pl.ext_a0 = ahi;
-                pl.ext_a1 = alo;
+                pl.ext_a = a_cat;
                 pl.a_ready = j > 0;
-                pl.ext_b0 = bhi + (size_t)j0 * k4;
-                pl.ext_b1 = blo + (size_t)j0 * k4;
+                pl.ext_b = b_cat + (size_t)j0 * 2 * k16;
                 pl.b_ready = i > 0;
             }
             st = launch_plan(pl, Ai, Bj, Cij, wplan, stream, nullptr, nullptr);

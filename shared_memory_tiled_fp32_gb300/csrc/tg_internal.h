@@ -75,23 +75,22 @@ struct Plan {
     int num_sms = 0;     // SMs planned for
     int nkb = 0;         // K blocks of bk
     int k4 = 0, n4 = 0;  // K and N rounded up to a multiple of 4 (16-byte rows)
+    int k16 = 0;         // K rounded up to a multiple of 16 (3xTF32 split rows)
     bool zero_fill = false;  // K == 0: C = beta * C, nothing else runs
     bool pack_a = false, pack_b = false;  // FFMA: copy an operand to a 16-byte-pitched buffer
     bool vec_c = false;  // C rows start on 16-byte boundaries
     // workspace layout (byte offsets; a region absent from the plan has size 0)
-    size_t off_a0 = 0, off_a1 = 0, off_b0 = 0, off_b1 = 0, off_part = 0, off_tail = 0;
+    size_t off_a0 = 0, off_b0 = 0, off_part = 0, off_tail = 0;
     long long ldp = 0;           // partial-product row stride (elements)
     long long part_stride = 0;   // elements between two K-slice partials
     size_t ws_bytes = 0;
     int launches = 0;
-    // 3xTF32 only: A_hi / A_lo (B_hi^T / B_lo^T) live outside the workspace
-    // at ext_a0 / ext_a1 (ext_b0 / ext_b1), planned with external_a
-    // (external_b); a_ready (b_ready) = they already hold that operand's
-    // split, so the pre-pass skips it (and is not launched if both are)
-    float* ext_a0 = nullptr;
-    float* ext_a1 = nullptr;
-    float* ext_b0 = nullptr;
-    float* ext_b1 = nullptr;
+    // 3xTF32 only: A's interleaved hi/lo copy [M][2*k16] (B^T's, [N][2*k16])
+    // lives outside the workspace at ext_a (ext_b), planned with external_a
+    // (external_b); a_ready (b_ready) = it already holds that operand's split,
+    // so the pre-pass skips it (and is not launched if both are)
+    float* ext_a = nullptr;
+    float* ext_b = nullptr;
     bool a_ready = false;
     bool b_ready = false;
 };

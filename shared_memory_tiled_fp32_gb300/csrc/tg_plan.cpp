@@ -50,7 +50,7 @@ long long tail_operand_bytes(const Plan& p, long long rem) {
     long long rows = 0, cols = 0;
     for (int i : rows_seen) rows += std::min<long long>((long long)p.pair * p.bm, p.M - (long long)i * p.pair * p.bm);
     for (int j : cols_seen) cols += std::min<long long>(p.bn, p.N - (long long)j * p.bn);
-    return (rows + cols) * p.k4 * 8;
+    return (rows + cols) * p.k16 * 8;
 }
 
 }  // namespace
@@ -109,6 +109,7 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->bm = kFfmaBM; p->bn = kFfmaBN; p->bk = kFfmaBK; p->stages = kFfmaStages;
     }
     p->k4 = (int)round_up((size_t)K, 4);
+    p->k16 = (int)round_up((size_t)K, 16);
     p->n4 = (int)round_up((size_t)N, 4);
     if (M == 0 || N == 0) {
         p->launches = 0;
@@ -189,16 +190,9 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         return at;
     };
     if (p->path == TG_PATH_TF32X3) {
-        // hi/lo copies: A as [M][k4], B transposed as [N][k4] (both K-major)
-        const size_t a_bytes = 4ull * M * p->k4, b_bytes = 4ull * N * p->k4;
-        if (!external_a) {  // else the caller provides A's hi/lo copies
-            p->off_a0 = take(a_bytes);
-            p->off_a1 = take(a_bytes);
-        }
-        if (!external_b) {  // else the caller provides B's hi/lo copies
-            p->off_b0 = take(b_bytes);
-            p->off_b1 = take(b_bytes);
-        }
+        // interleaved hi/lo copies: A as [M][2*k16], B transposed as [N][2*k16]
+        if (!external_a) p->off_a0 = take(8ull * M * p->k16);  // else the caller provides them
+        if (!external_b) p->off_b0 = take(8ull * N * p->k16);
     } else {
         // TMA reads the operands in place when they are stored untransposed,
         // their base is 16-byte aligned and their row pitch a multiple of 16
