@@ -258,8 +258,9 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
                  c_bytes = 4ull * M * n4;
     auto align = [](size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; };
     const long long k16 = ((long long)std::max(K, 1) + 15) / 16 * 16;
-    const size_t b_split = tf32 ? align(8ull * N * k16) : 0;   // B^T's interleaved hi/lo: [N][2*k16]
-    const size_t a_split = tf32 ? align(8ull * mb * k16) : 0;  // A_i's interleaved hi/lo: [mb][2*k16]
+    // split tiles (rows padded to 256): all of B^T's, and one A row block's
+    const size_t b_split = tf32 ? align(8ull * ((N + 255) / 256 * 256) * k16) : 0;
+    const size_t a_split = tf32 ? align(8ull * ((mb + 255) / 256 * 256) * k16) : 0;
     // placeholder pointers with the alignment the real ones will have
     const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
     size_t ws_max = 0;  // over the (at most 4) block shapes: whole or ragged rows x columns

@@ -76,6 +76,7 @@ struct Plan {
     int nkb = 0;         // K blocks of bk
     int k4 = 0, n4 = 0;  // K and N rounded up to a multiple of 4 (16-byte rows)
     int k16 = 0;         // K rounded up to a multiple of 16 (3xTF32 split rows)
+    int a_rows = 0, b_rows = 0;  // 3xTF32: rows of the split tiles (M, N padded to whole tiles)
     bool zero_fill = false;  // K == 0: C = beta * C, nothing else runs
     bool pack_a = false, pack_b = false;  // FFMA: copy an operand to a 16-byte-pitched buffer
     bool vec_c = false;  // C rows start on 16-byte boundaries
@@ -85,8 +86,8 @@ struct Plan {
     long long part_stride = 0;   // elements between two K-slice partials
     size_t ws_bytes = 0;
     int launches = 0;
-    // 3xTF32 only: A's interleaved hi/lo copy [M][2*k16] (B^T's, [N][2*k16])
-    // lives outside the workspace at ext_a (ext_b), planned with external_a
+    // 3xTF32 only: A's split tiles (a_rows x 2*k16 floats; B^T's, b_rows x
+    // 2*k16) live outside the workspace at ext_a (ext_b), planned with external_a
     // (external_b); a_ready (b_ready) = it already holds that operand's split,
     // so the pre-pass skips it (and is not launched if both are)
     float* ext_a = nullptr;

@@ -52,6 +52,10 @@ struct GemmArgs {
     int split, nkb;
     long long units;
     float* out;              // C (split == 1) or the first K-slice partial
+    // 3xTF32: the operands' split copies as 16 KiB tiles (see the pre-pass)
+    const float* a_tiles;
+    const float* b_tiles;
+    int kbs;                 // K blocks per tile row of tiles
     long long ldo;           // row stride of `out`
     long long slice_stride;  // elements between K-slice partials
     int vec_out;             // rows of `out` start on 16-byte boundaries
@@ -386,17 +390,16 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 
 // -------------------------------------------------------------- 3xTF32 path
 //
-// Operands come from the split pre-pass, K-major and with hi and lo
-// interleaved: A as [M][2*k16] and B transposed as [N][2*k16], where each
-// 16-wide K block of a row holds 16 hi values then the same 16 lo values.
-// One K block of a tile row is thus one 128-byte row, which TMA writes with
-// the 128-byte swizzle of the tensor core's K-major layout; a stage takes two
-// boxes (A: 128 rows, B: 256 rows, or one 128-row half per CTA of a pair)
-// instead of four boxes of 64-byte rows, half the row requests for the same
-// bytes (measured on GB300: the MMA thread waited for data 12 % of the time
-// instead of 19 %, 8192^3 348 -> 368 TFLOP/s).  Within a stage the hi slice
-// ks (8 values) starts ks * 32 bytes into each row and the lo slice 64 bytes
-// after it.
+// Operands come from the split pre-pass as 16 KiB tiles: 128 rows of A (or
+// of B transposed) x one 16-wide K block, each row 16 hi values then the same
+// 16 lo values (128 bytes), already in the 128-byte-swizzled order of the
+// tensor core's K-major layout.  A stage is then one contiguous bulk copy per
+// 128-row tile (A, and B's two halves: one per CTA of a pair, multicast to
+// both) rather than a TMA box of 128 or 256 separate rows.  Measured on
+// GB300 with cycle counters: four boxes of 64-byte rows per stage left the
+// MMA thread waiting for data 19 % of the time, two boxes of 128-byte rows
+// 12 %.  Within a stage the hi slice ks (8 values) starts ks * 32 bytes into
+// each row and the lo slice 64 bytes after it.
 //
 // Per 8-wide K slice the MMA thread issues
 //     D += A_hi B_lo;  D += A_hi B_hi;  D += A_lo B_hi
@@ -433,6 +436,7 @@ constexpr uint32_t kTfBStage = kTf32BN * kTfRowBytes;              // 32 KiB
 constexpr uint32_t kTfStageBytes = kTfAStage + kTfBStage;          // 48 KiB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSwRowGroupBytes = 8 * kTfRowBytes;  // 8 rows of the 128-byte swizzle atom
+constexpr long long kTileFloats = kTfAStage / 4;        // one 128-row tile: 4096 floats
 constexpr uint32_t kDescSwizzle128 = 2;
 static_assert(kTfRowBytes == 128, "one K block of hi and lo must fill one 128-byte swizzle row");
 constexpr int kTfBars = 2 * kTf32Stages + 5;
@@ -440,8 +444,7 @@ constexpr size_t kTfSmemBytes = 1024 + (size_t)kTf32Stages * kTfStageBytes + kTf
 
 template <int kPair>
 __global__ void __launch_bounds__(kTfThreads, 1)
-    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       GemmArgs args) {
+    tf32x3_gemm_kernel(GemmArgs args) {
     constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK, ST = kTf32Stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
@@ -460,7 +463,6 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     const long long first_unit = blockIdx.x / kPair, unit_stride = gridDim.x / kPair;
     constexpr uint16_t kPairMask = (uint16_t)((1u << kPair) - 1u);
     constexpr uint32_t kBHalf = kTfBStage / kPair;  // bytes of the B tile one CTA loads
-    constexpr int kBRows = BN / kPair;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
@@ -490,8 +492,6 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     if (warp < 4) {
         regs_dec<kTfIssueRegs>();
         if (warp == 0 && lane == 0) {  // ------------------------- producer
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
@@ -506,15 +506,20 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                     }
                     uint8_t* st = smem + stage * kTfStageBytes;
                     // this CTA receives the whole A and B tiles (48 KiB), half
-                    // of B from its own load and half from the peer's
+                    // of B from its own copy and half from the peer's
                     mbar_arrive_expect_tx(&full[stage], kTfStageBytes);
-                    const int x = kb * 2 * BK;  // K block kb: 32 floats of the interleaved rows
-                    tma_load_2d(st, &tmA, &full[stage], x, t.m0);
-                    if (kPair > 1)
-                        tma_load_2d_multicast(st + kTfAStage + rank * kBHalf, &tmB, &full[stage], x,
-                                              t.n0 + rank * kBRows, kPairMask);
-                    else
-                        tma_load_2d(st + kTfAStage, &tmB, &full[stage], x, t.n0);
+                    const float* a_src = args.a_tiles + ((long long)(t.m0 >> 7) * args.kbs + kb) * kTileFloats;
+                    const float* b_src = args.b_tiles + ((long long)(t.n0 >> 7) * args.kbs + kb) * kTileFloats;
+                    bulk_load(st, a_src, kTfAStage, &full[stage]);
+                    if (kPair > 1) {
+                        bulk_load_multicast(st + kTfAStage + rank * kBHalf,
+                                            b_src + (long long)rank * args.kbs * kTileFloats, kBHalf, &full[stage],
+                                            kPairMask);
+                    } else {
+                        bulk_load(st + kTfAStage, b_src, kTfAStage, &full[stage]);
+                        bulk_load(st + 2 * kTfAStage, b_src + (long long)args.kbs * kTileFloats, kTfAStage,
+                                  &full[stage]);
+                    }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == ST) {
@@ -653,10 +658,11 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 //
 // Lays each operand out K-major for the GEMM kernels, zero-padding columns
 // past the valid extent (ghost elements):
-//   SPLIT (3xTF32): op(A) -> [M][2*k16];  op(B)^T -> [N][2*k16], hi and lo
-//     interleaved per 16-wide block of K: destination column c of row r goes
-//     to r*2*k16 + (c/16)*32 + c%16 (hi) and 16 further on (lo), with
-//     hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32).
+//   SPLIT (3xTF32): op(A) and op(B)^T as 16 KiB tiles of 128 rows x one
+//     16-wide K block, [row tile][K block], with rows padded to whole tiles
+//     (zeros).  Tile row r holds 16 hi then 16 lo values, each 4-value group
+//     (16 bytes) j of the 8 stored at position j ^ (r % 8): the 128-byte
+//     swizzle.  hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32).
 //   PACK (FFMA, operand not TMA-legal or transposed): op(A) -> [M][k4],
 //     op(B) -> [K][n4].
 // Each operand is either copied row by row (its stored rows already run along
@@ -671,7 +677,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 struct OperandPass {
     const float* src;
     long long ld;    // source row stride (elements)
-    int rows;        // destination rows
+    int rows;        // destination rows written (SPLIT: padded to whole tiles)
+    int rows_valid;  // destination rows that exist in the source (the rest are zeros)
     int cols;        // valid destination columns (source extent)
     int pitch;       // padded destination columns (multiple of 16 for SPLIT, of 4 for PACK)
     int trans;       // 1: dst[r][c] = src[c*ld + r]; 0: dst[r][c] = src[r*ld + c]
@@ -699,20 +706,25 @@ __device__ __forceinline__ float4 load_row4(const float* src, long long ld, int 
 
 // Offset of destination element (r, c): hi of the interleaved layout (SPLIT)
 // or the plain padded row (PACK).
+// Offset of destination element (r, c): hi in its swizzled tile (SPLIT; the
+// lo value sits at offset ^ 16, its 16-byte group j + 4 swizzled the same
+// way) or the plain padded row (PACK).
 template <bool SPLIT>
 __device__ __forceinline__ long long dst_offset(int pitch, int r, int c) {
-    if (SPLIT) return (long long)r * 2 * pitch + (c >> 4) * 32 + (c & 15);
+    if (SPLIT)
+        return ((long long)(r >> 7) * (pitch >> 4) + (c >> 4)) * 4096 + (r & 127) * 32 +
+               ((((c & 15) >> 2) ^ (r & 7)) << 2) + (c & 3);
     return (long long)r * pitch + c;
 }
 
-// Store destination columns c..c+3 of a row (c a multiple of 4, so they share
-// one 16-wide block) at offset o.
+// Store destination columns c..c+3 of a row (c a multiple of 4: one 16-byte
+// group) at offset o.
 template <bool SPLIT>
 __device__ __forceinline__ void store_split4(float* d0, long long o, float4 x) {
     if (SPLIT) {
         const float4 hi = make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
         *reinterpret_cast<float4*>(d0 + o) = hi;
-        *reinterpret_cast<float4*>(d0 + o + 16) =
+        *reinterpret_cast<float4*>(d0 + (o ^ 16)) =
             make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
     } else {
         *reinterpret_cast<float4*>(d0 + o) = x;
@@ -733,7 +745,8 @@ __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
             o[u] = -1;
             if (it < p.items) {
                 const int r = (int)(it / groups), c = (int)(it % groups) * 4;
-                v[u] = load_row4(p.src, p.ld, r, c, p.cols, p.vec != 0);
+                v[u] = r < p.rows_valid ? load_row4(p.src, p.ld, r, c, p.cols, p.vec != 0)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                 o[u] = dst_offset<SPLIT>(p.pitch, r, c);
             }
         }
@@ -750,7 +763,7 @@ __device__ __forceinline__ void transpose_load(const OperandPass& p, long long t
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int c = c0 + ty + 4 * j, r = r0 + tx;
-        v[j] = (c < p.cols && r < p.rows) ? p.src[(long long)c * p.ld + r] : 0.0f;
+        v[j] = (c < p.cols && r < p.rows_valid) ? p.src[(long long)c * p.ld + r] : 0.0f;
     }
 }
 
@@ -780,7 +793,7 @@ __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*til
                 if (SPLIT) {
                     const float hi = to_tf32(x);
                     p.d0[o] = hi;
-                    p.d0[o + 16] = to_tf32(x - hi);
+                    p.d0[o ^ 16] = to_tf32(x - hi);
                 } else {
                     p.d0[o] = x;
                 }
@@ -1097,18 +1110,20 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
 
     // Operand passes of the pre-pass.  A is stored M x K (op N) or K x M
     // (op T); B is stored K x N (op N) or N x K (op T).
-    auto pass = [](const float* src, long long ld, int rows, int cols, int pitch, bool trans, float* d0) {
+    auto pass = [](const float* src, long long ld, int rows, int cols, int pitch, bool trans, float* d0,
+                   int rows_out) {
         OperandPass o{};
         o.src = src;
         o.ld = ld;
-        o.rows = rows;
+        o.rows = rows_out;
+        o.rows_valid = rows;
         o.cols = cols;
         o.pitch = pitch;
         o.trans = trans ? 1 : 0;
         o.vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && ld % 4 == 0) ? 1 : 0;
         o.d0 = d0;
         o.tiles_c = (pitch + 63) / 64;
-        o.items = trans ? (long long)((rows + 63) / 64) * o.tiles_c : (long long)rows * (pitch / 4);
+        o.items = trans ? (long long)((rows_out + 63) / 64) * o.tiles_c : (long long)rows_out * (pitch / 4);
         return o;
     };
     PrepassArgs pa{};
@@ -1116,33 +1131,28 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     const int prepass_grid = g_prepass_blocks_per_sm[p.path == TG_PATH_TF32X3 ? 1 : 0] * p.num_sms;
 
     if (p.path == TG_PATH_TF32X3) {
-        float* a_cat = p.ext_a ? p.ext_a : reinterpret_cast<float*>(w + p.off_a0);
-        float* b_cat = p.ext_b ? p.ext_b : reinterpret_cast<float*>(w + p.off_b0);
-        // interleaved hi/lo: A [M][2*k16] from op(A); B [N][2*k16] from op(B)^T
-        pa.op[0] = pass(A, p.lda, p.M, p.K, p.k16, p.op_a == TG_OP_T, p.a_ready ? nullptr : a_cat);
-        pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, p.b_ready ? nullptr : b_cat);
+        float* a_tiles = p.ext_a ? p.ext_a : reinterpret_cast<float*>(w + p.off_a0);
+        float* b_tiles = p.ext_b ? p.ext_b : reinterpret_cast<float*>(w + p.off_b0);
+        // split tiles: A [a_rows/128][k16/16] from op(A); B [b_rows/128][k16/16] from op(B)^T
+        pa.op[0] = pass(A, p.lda, p.M, p.K, p.k16, p.op_a == TG_OP_T, p.a_ready ? nullptr : a_tiles, p.a_rows);
+        pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, p.b_ready ? nullptr : b_tiles, p.b_rows);
         if (!(p.a_ready && p.b_ready)) {
             prepass_kernel<true><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
         }
-
-        // the pre-pass writes every column of the padded rows; rows past M
-        // (N) read as zero
-        CUtensorMap mA, mB;
-        const uint64_t cols = 2ull * p.k16, row = 4 * cols;
-        if (!make_map(&mA, a_cat, cols, p.M, row, 2 * kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map(&mB, b_cat, cols, p.N, row, 2 * kTf32BK, kTf32BN / p.pair, CU_TENSOR_MAP_SWIZZLE_128B))
-            return TG_ERR_CUDA;
+        ga.a_tiles = a_tiles;
+        ga.b_tiles = b_tiles;
+        ga.kbs = p.k16 / 16;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
         if (p.pair == 2) {
             int clusters = p.grid / 2;
             if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
             if (launch_dependent(tf32x3_gemm_kernel<2>, dim3(2 * clusters), dim3(kTfThreads), kTfSmemBytes, stream, 2,
-                                 mA, mB, ga) != TG_OK)
+                                 ga) != TG_OK)
                 return TG_ERR_CUDA;
         } else {
             if (launch_dependent(tf32x3_gemm_kernel<1>, dim3(p.grid), dim3(kTfThreads), kTfSmemBytes, stream, 1,
-                                 mA, mB, ga) != TG_OK)
+                                 ga) != TG_OK)
                 return TG_ERR_CUDA;
         }
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
@@ -1154,8 +1164,8 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
             // A_pack [M][k4] from op(A); B_pack [K][n4] from op(B)
             float* ap = p.pack_a ? reinterpret_cast<float*>(w + p.off_a0) : nullptr;
             float* bp = p.pack_b ? reinterpret_cast<float*>(w + p.off_b0) : nullptr;
-            pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, ap);
-            pa.op[1] = pass(B, p.ldb, p.K, p.N, p.n4, p.op_b == TG_OP_T, bp);
+            pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, ap, p.M);
+            pa.op[1] = pass(B, p.ldb, p.K, p.N, p.n4, p.op_b == TG_OP_T, bp, p.K);
             prepass_kernel<false><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
             if (p.pack_a) {

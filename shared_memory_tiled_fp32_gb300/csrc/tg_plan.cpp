@@ -190,9 +190,12 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         return at;
     };
     if (p->path == TG_PATH_TF32X3) {
-        // interleaved hi/lo copies: A as [M][2*k16], B transposed as [N][2*k16]
-        if (!external_a) p->off_a0 = take(8ull * M * p->k16);  // else the caller provides them
-        if (!external_b) p->off_b0 = take(8ull * N * p->k16);
+        // split tiles of 128 rows x (16 hi + 16 lo): A's rows padded to whole
+        // units (pair x 128), B^T's to whole 256-row B tiles
+        p->a_rows = (int)round_up((size_t)M, 128 * (size_t)p->pair);
+        p->b_rows = (int)round_up((size_t)N, 256);
+        if (!external_a) p->off_a0 = take(8ull * p->a_rows * p->k16);  // else the caller provides them
+        if (!external_b) p->off_b0 = take(8ull * p->b_rows * p->k16);
     } else {
         // TMA reads the operands in place when they are stored untransposed,
         // their base is 16-byte aligned and their row pitch a multiple of 16

@@ -135,6 +135,28 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUte
         : "memory");
 }
 
+// 1-D bulk copy of `bytes` contiguous bytes (16-byte aligned, a multiple of
+// 16) from global to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// The same, delivered to the same shared-memory offset of every CTA in
+// `cta_mask` (cluster ranks), each signalling its own mbarrier at `bar`'s
+// offset.
+__device__ __forceinline__ void bulk_load_multicast(void* smem_dst, const void* src, uint32_t bytes,
+                                                    uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "h"(cta_mask)
+        : "memory");
+}
+
 // ------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
