@@ -532,6 +532,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                 if ((issued >> s) & 1u) mbar_drain(&full[s], (last_par >> s) & 1u, args.timeout_ns);
         } else if (warp == 1 && lane == 0) {  // ---------------- MMA issuer
             constexpr uint32_t idesc = idesc_tf32(BM, BN);
+            static_assert(BK == 16 && kTfRowBytes == 128, "the issue loop below is written for two 8-wide slices");
+            const uint64_t desc_stage0 = smem_desc_kmajor(smem_addr(smem), kSwRowGroupBytes, kDescSwizzle128);
             int stage = 0;
             uint32_t phase = 0, chunk = 0;
             bool ok = true;
@@ -552,23 +554,24 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint32_t a_hi = smem_addr(smem + stage * kTfStageBytes);
-                        const uint32_t a_lo = a_hi + 4 * BK;  // lo half of each 128-byte row
-                        const uint32_t b_hi = a_hi + kTfAStage;
-                        const uint32_t b_lo = b_hi + 4 * BK;
-#pragma unroll
-                        for (int ks = 0; ks < BK / 8; ++ks) {
-                            const uint32_t ko = ks * 32;  // 8 tf32 values along K
-                            const uint64_t dahi = smem_desc_kmajor(a_hi + ko, kSwRowGroupBytes, kDescSwizzle128);
-                            const uint64_t dalo = smem_desc_kmajor(a_lo + ko, kSwRowGroupBytes, kDescSwizzle128);
-                            const uint64_t dbhi = smem_desc_kmajor(b_hi + ko, kSwRowGroupBytes, kDescSwizzle128);
-                            const uint64_t dblo = smem_desc_kmajor(b_lo + ko, kSwRowGroupBytes, kDescSwizzle128);
-                            // A_hi is read from shared memory once and kept in the
-                            // tensor core's A collector for its second product
-                            mma_tf32_ss_fill_a(d_tmem, dahi, dblo, idesc, (kb > c0 || ks > 0) ? 1u : 0u);
-                            mma_tf32_ss_lastuse_a(d_tmem, dahi, dbhi, idesc, 1u);
-                            mma_tf32_ss(d_tmem, dalo, dbhi, idesc, 1u);
-                        }
+                        // descriptors of this stage's tiles; their address field
+                        // counts 16-byte units, so the lo half of each 128-byte row
+                        // is +4 and the second 8-wide K slice +2
+                        const uint64_t da = desc_stage0 + (uint64_t)stage * (kTfStageBytes >> 4);
+                        const uint64_t db = da + (kTfAStage >> 4);
+                        // A_hi is read from shared memory once per slice and kept in
+                        // the tensor core's A collector for its second product.  The
+                        // chunk's first K block starts the accumulator.  No branch
+                        // separates the MMAs: a branch in the issue sequence cost
+                        // the single issuing thread about 10 % of its rate
+                        // (measured), a flag computed per block does not.
+                        const uint32_t acc = kb > c0 ? 1u : 0u;
+                        mma_tf32_ss_fill_a(d_tmem, da, db + 4, idesc, acc);
+                        mma_tf32_ss_lastuse_a(d_tmem, da, db, idesc, 1u);
+                        mma_tf32_ss(d_tmem, da + 4, db, idesc, 1u);
+                        mma_tf32_ss_fill_a(d_tmem, da + 2, db + 6, idesc, 1u);
+                        mma_tf32_ss_lastuse_a(d_tmem, da + 2, db + 2, idesc, 1u);
+                        mma_tf32_ss(d_tmem, da + 6, db + 2, idesc, 1u);
                         // frees the stage (in both CTAs of a pair) once these MMAs are done
                         if (kPair > 1)
                             mma_commit_multicast(&empty[stage], kPairMask);

@@ -57,22 +57,33 @@ __global__ void __launch_bounds__(128, 1) probe_tf32_mma_kernel(int iters, int u
     if (threadIdx.x == 0) {
         constexpr uint32_t idesc = idesc_tf32(kProbeM, kProbeN);
         const uint32_t sa = smem_addr(smem), sb = sa + kProbeA;
-        for (int it = 0; it < iters; ++it) {
+        // the MMA sequence inside the loop has no branch, as in the GEMM's
+        // issue loop (a branch between MMAs costs the single issuing thread
+        // about 10 % of the rate)
+        if (use_collector) {
+            for (int it = 0; it < iters; ++it) {
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const uint64_t da = smem_desc_kmajor(sa + ks * 32, 512, 4);
-                const uint64_t db = smem_desc_kmajor(sb + ks * 32, 512, 4);
-                const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
-                if (use_collector) {
-                    mma_tf32_ss_fill_a(tmem, da, db, idesc, acc);
+                for (int ks = 0; ks < 2; ++ks) {
+                    const uint64_t da = smem_desc_kmajor(sa + ks * 32, 512, 4);
+                    const uint64_t db = smem_desc_kmajor(sb + ks * 32, 512, 4);
+                    mma_tf32_ss_fill_a(tmem, da, db, idesc, (it > 0 || ks > 0) ? 1u : 0u);
                     mma_tf32_ss_lastuse_a(tmem, da, db, idesc, 1u);
-                } else {
-                    mma_tf32_ss(tmem, da, db, idesc, acc);
                     mma_tf32_ss(tmem, da, db, idesc, 1u);
                 }
-                mma_tf32_ss(tmem, da, db, idesc, 1u);
+                mma_commit(&bars[0]);  // one commit per six MMAs, like the GEMM's stages
             }
-            mma_commit(&bars[0]);  // one commit per six MMAs, like the GEMM's stages
+        } else {
+            for (int it = 0; it < iters; ++it) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const uint64_t da = smem_desc_kmajor(sa + ks * 32, 512, 4);
+                    const uint64_t db = smem_desc_kmajor(sb + ks * 32, 512, 4);
+                    mma_tf32_ss(tmem, da, db, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_tf32_ss(tmem, da, db, idesc, 1u);
+                    mma_tf32_ss(tmem, da, db, idesc, 1u);
+                }
+                mma_commit(&bars[0]);
+            }
         }
         mma_commit(&bars[1]);
         mbar_drain(&bars[1], 0, timeout_ns);
