@@ -105,8 +105,11 @@ typedef struct tg_plan_info {
     size_t workspace_bytes;
     int pair;          /* 3xTF32: CTAs per cluster sharing one B tile by TMA multicast (1 or 2);
                           a unit is then `pair` vertically adjacent tiles */
-    long long tail_units; /* units after the last whole round of lanes, run stream-K (0 = none) */
+    long long tail_units; /* units after the last whole round of lanes, balanced (0 = none) */
     int tail_lanes;       /* lanes (CTAs, or CTA pairs) sharing those units' K blocks equally */
+    int tail_kx;          /* 0: the lanes run the units' K blocks laid end to end (stream-K) or
+                             equal K slices; > 0: unit q's first tail_kx K blocks run on lane q,
+                             all in step, the rest of every unit over the other lanes */
 } tg_plan_info;
 
 /* C = A x B with automatic path and split choice (see the file comment for

@@ -84,6 +84,7 @@ class PlanInfo(ctypes.Structure):
         ("pair", ctypes.c_int),
         ("tail_units", ctypes.c_longlong),
         ("tail_lanes", ctypes.c_int),
+        ("tail_kx", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -113,6 +113,7 @@ void fill_info(const Plan& p, tg_plan_info* out) {
     out->pair = p.pair;
     out->tail_units = p.tail_units;
     out->tail_lanes = p.tail_lanes;
+    out->tail_kx = p.tail_kx;
 }
 
 }  // namespace

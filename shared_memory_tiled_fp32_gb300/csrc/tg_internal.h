@@ -71,6 +71,12 @@ struct Plan {
     long long full_units = 0;
     long long tail_units = 0;
     int tail_lanes = 0;
+    // split point (3xTF32, tails larger than L2 with more than half the lanes
+    // busy): the first tail_kx K blocks of tail unit q run on lane q, all
+    // units in step; the remaining K blocks of every unit are shared out over
+    // the other lanes; tail_slots partial slots per unit (0: runs as above)
+    int tail_kx = 0;
+    int tail_slots = 0;
     int grid = 0;
     int num_sms = 0;     // SMs planned for
     int nkb = 0;         // K blocks of bk

@@ -59,12 +59,15 @@ struct GemmArgs {
     long long ldo;           // row stride of `out`
     long long slice_stride;  // elements between K-slice partials
     int vec_out;             // rows of `out` start on 16-byte boundaries
-    // stream-K tail: the tail_units tile units after full_units are shared
-    // out over tail_lanes lanes (see work_item); pieces of a unit go to
-    // partial slot 2*lane (a lane's first piece) or 2*lane + 1 (its last) of
-    // `tail` ([slot][pair*BM][BN] floats)
+    // balanced last round: the tail_units tile units after full_units are
+    // shared out over tail_lanes lanes (see work_item).  tail_kx == 0: runs
+    // of the units laid end to end, pieces to partial slot 2*lane (a lane's
+    // first piece) or 2*lane + 1 (its last); tail_kx > 0: unit q's first
+    // tail_kx K blocks on lane q (slot q*tail_slots), the rest of every unit
+    // over the other lanes (slots q*tail_slots + 1 + i).  Slots are
+    // [pair*BM][BN] floats of `tail`.
     long long full_units, tail_units;
-    int tail_lanes;
+    int tail_lanes, tail_kx, tail_slots;
     float* tail;
     // C = alpha * op(A) op(B) + beta * C, applied where C is written (scaled
     // = 0: a plain store of the product; beta == 0: C is not read)
@@ -125,6 +128,48 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, lon
         return true;
     }
     j -= nfull;
+    const long long blk = (long long)a.pair * BM * BN;
+    int tm, tn;
+    if (a.tail_kx > 0) {  // split point: lockstep first parts, the rest spread out
+        const long long U = a.tail_units, E = a.tail_lanes - U, rl = a.nkb - a.tail_kx, R = U * rl;
+        for (long long v = lane; v < a.tail_lanes; v += lanes) {
+            if (v < U) {
+                if (j > 0) {
+                    --j;
+                    continue;
+                }
+                unit_tile(a.tiles_m, a.tiles_n, a.full_units + v, &tm, &tn);
+                x->m0 = (tm * a.pair + rank) * BM;
+                x->n0 = tn * BN;
+                x->kb0 = 0;
+                x->kb1 = a.tail_kx;
+                x->direct = false;
+                x->out = a.tail + v * a.tail_slots * blk - (long long)tm * blk - x->n0;
+                x->ldo = BN;
+                return true;
+            }
+            const long long e = v - U;
+            const long long s = tail_run_begin(e, R, E), t = tail_run_begin(e + 1, R, E);
+            if (s >= t) continue;
+            const long long q0 = s / rl, pieces = (t - 1) / rl - q0 + 1;
+            if (j >= pieces) {
+                j -= pieces;
+                continue;
+            }
+            const long long q = q0 + j, b0 = q * rl;
+            unit_tile(a.tiles_m, a.tiles_n, a.full_units + q, &tm, &tn);
+            x->m0 = (tm * a.pair + rank) * BM;
+            x->n0 = tn * BN;
+            x->kb0 = a.tail_kx + (int)((s > b0 ? s : b0) - b0);
+            x->kb1 = a.tail_kx + (int)((t < b0 + rl ? t : b0 + rl) - b0);
+            x->direct = false;
+            const long long slot = q * a.tail_slots + 1 + (e - tail_lane_of(b0, R, E));
+            x->out = a.tail + slot * blk - (long long)tm * blk - x->n0;
+            x->ldo = BN;
+            return true;
+        }
+        return false;
+    }
     const long long T = a.tail_units * a.nkb;
     for (long long v = lane; v < a.tail_lanes; v += lanes) {
         const long long s = tail_run_begin(v, T, a.tail_lanes);
@@ -136,7 +181,6 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, lon
             continue;
         }
         const long long q = q0 + j, b0 = q * a.nkb;
-        int tm, tn;
         unit_tile(a.tiles_m, a.tiles_n, a.full_units + q, &tm, &tn);
         x->m0 = (tm * a.pair + rank) * BM;
         x->n0 = tn * BN;
@@ -147,7 +191,6 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, lon
             x->out = a.out;
             x->ldo = a.ldo;
         } else {  // this slot's [pair*BM][BN] block, addressed with global row/column
-            const long long blk = (long long)a.pair * BM * BN;
             const long long slot = 2 * v + (j == 0 ? 0 : 1);
             x->out = a.tail + slot * blk - (long long)tm * blk - x->n0;
             x->ldo = BN;
@@ -856,35 +899,57 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Stream-K tail: every tail unit that more than one lane ran is the sum of
-// its pieces' partials, added in lane order (deterministic), float4 per
-// thread.  A unit run whole by one lane was stored by the GEMM kernel.
+// Balanced last round: every tail unit that more than one lane ran is the
+// sum of its pieces' partials, added in a fixed order (deterministic), float4
+// per thread.  Stream-K runs: lane order; a unit run whole by one lane was
+// stored by the GEMM kernel.  Split point: the unit's first part, then the
+// pieces of its remainder in lane order.
 __global__ void __launch_bounds__(256)
     tail_reduce_kernel(GemmArgs a, float* C, long long ldc, int BM, int BN, int vec_c) {
     grid_dep_wait();  // every partial is written
     const int rows = a.pair * BM, q4 = BN / 4;
     const long long block = (long long)rows * BN;
-    const long long T = a.tail_units * a.nkb, lanes = a.tail_lanes;
     const long long total = a.tail_units * rows * q4;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const long long q = i / ((long long)rows * q4);
         const int rem = (int)(i - q * rows * q4);
         const int r = rem / q4, c = (rem % q4) * 4;
-        const long long v0 = tail_lane_of(q * a.nkb, T, lanes);
-        const long long v1 = tail_lane_of((q + 1) * a.nkb - 1, T, lanes);
-        if (v0 == v1) continue;
+        long long v0, v1, T, lanes, base;
+        if (a.tail_kx > 0) {
+            const long long rl = a.nkb - a.tail_kx;
+            T = a.tail_units * rl;
+            lanes = a.tail_lanes - a.tail_units;
+            v0 = tail_lane_of(q * rl, T, lanes);
+            v1 = tail_lane_of((q + 1) * rl - 1, T, lanes);
+            base = q * a.tail_slots;
+        } else {
+            T = a.tail_units * a.nkb;
+            lanes = a.tail_lanes;
+            v0 = tail_lane_of(q * a.nkb, T, lanes);
+            v1 = tail_lane_of((q + 1) * a.nkb - 1, T, lanes);
+            if (v0 == v1) continue;
+            base = 0;
+        }
         int tm, tn;
         unit_tile(a.tiles_m, a.tiles_n, a.full_units + q, &tm, &tn);
         const int m = tm * rows + r, n = tn * BN + c;
         if (m >= a.M || n >= a.N) continue;
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* tile = a.tail + (long long)r * BN + c;
+        float4 s;
+        if (a.tail_kx > 0) s = *reinterpret_cast<const float4*>(tile + base * block);
         for (long long v = v0; v <= v1; ++v) {
-            // slot 2v holds lane v's first piece, 2v + 1 its last
-            const long long first_q = tail_run_begin(v, T, lanes) / a.nkb;
-            const long long slot = 2 * v + (first_q == q ? 0 : 1);
-            const float4 x = *reinterpret_cast<const float4*>(a.tail + slot * block + (long long)r * BN + c);
-            if (v == v0) {
+            // stream-K: slot 2v holds lane v's first piece, 2v + 1 its last;
+            // split point: slot base + 1 + (v - v0)
+            long long slot;
+            if (a.tail_kx > 0) {
+                slot = base + 1 + (v - v0);
+            } else {
+                const long long first_q = tail_run_begin(v, T, lanes) / a.nkb;
+                slot = 2 * v + (first_q == q ? 0 : 1);
+            }
+            const float4 x = *reinterpret_cast<const float4*>(tile + slot * block);
+            if (v == v0 && a.tail_kx == 0) {
                 s = x;
             } else {
                 s.x += x.x;
@@ -1094,6 +1159,8 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     ga.full_units = p.full_units;
     ga.tail_units = p.tail_units;
     ga.tail_lanes = p.tail_lanes;
+    ga.tail_kx = p.tail_kx;
+    ga.tail_slots = p.tail_slots;
     ga.tail = p.tail_lanes > 0 ? reinterpret_cast<float*>(w + p.off_tail) : nullptr;
     ga.alpha = p.alpha;
     ga.beta = p.beta;

@@ -159,25 +159,46 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     //  * equal K slices (3xTF32, larger tails): L = rem * ts, so each run is
     //    one of ts equal K slices of one unit and the runs of a slice stay
     //    at the same K across units (ts <= 4, each slice >= 8 K blocks, only
-    //    when that at least halves the last round).
+    //    when that at least halves the last round);
+    //  * split point (3xTF32, larger tails filling more than half the lanes):
+    //    lane q < rem runs the first kx = rem * nkb / L K blocks of unit q,
+    //    all in step, and the other E = L - rem lanes share the remaining
+    //    nkb - kx blocks of every unit as runs laid end to end (each share at
+    //    least kTailMinK of K), so every lane gets about kx blocks.  The
+    //    reduce adds each unit's first part and its remainder's pieces.
     // Taken when it shortens the last round by at least 10 %; only with the
     // automatic split and no K split.
     if (split_k == 0 && S == 1) {
         const long long rem = p->units % cap;
+        const long long min_share = std::max<long long>(1, kTailMinK / p->bk);
         if (rem > 0) {
-            long long L = 0;
+            long long L = 0, kx = 0, slots = 0;
             if (p->path == TG_PATH_FFMA || tail_operand_bytes(*p, rem) <= kTailL2Bytes) {
-                const long long min_share = std::max<long long>(1, kTailMinK / p->bk);
                 L = std::min<long long>(cap, rem * p->nkb / min_share);
             } else if (2 * rem <= cap) {
                 long long ts = std::min<long long>(cap / rem, 4);
                 while (ts > 1 && p->nkb < 8 * ts) --ts;
                 L = rem * ts;
+            } else {
+                for (long long E = cap - rem; E > 0; --E) {
+                    const long long l = rem + E, x = rem * p->nkb / l;
+                    const long long share = rem * (p->nkb - x) / E;
+                    if (x > 0 && x < p->nkb && share >= min_share) {
+                        L = l;
+                        kx = x;
+                        // lanes meeting one unit's remainder: at most ceil(rl / share) + 1
+                        slots = 1 + (p->nkb - x + share - 1) / share + 1;
+                        break;
+                    }
+                }
             }
-            if (L > rem && 10 * rem <= 9 * L) {
+            const bool better = kx > 0 ? 10 * kx <= 9 * p->nkb : (L > rem && 10 * rem <= 9 * L);
+            if (L > 0 && better) {
                 p->full_units = p->units - rem;
                 p->tail_units = rem;
                 p->tail_lanes = (int)L;
+                p->tail_kx = (int)kx;
+                p->tail_slots = (int)slots;
                 p->grid = p->pair * (int)std::max<long long>(std::min<long long>(p->units, cap), L);
             }
         }
@@ -213,8 +234,10 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->part_stride = (long long)M * p->n4;
         p->off_part = take(4ull * S * M * p->n4);
     }
-    if (p->tail_lanes > 0)  // two partial slots per lane: its first and its last piece
-        p->off_tail = take(4ull * 2 * p->tail_lanes * p->pair * p->bm * p->bn);
+    if (p->tail_lanes > 0) {  // stream-K: two slots per lane (its first and last piece)
+        const size_t slots = p->tail_kx > 0 ? (size_t)p->tail_units * p->tail_slots : 2ull * p->tail_lanes;
+        p->off_tail = take(4ull * slots * p->pair * p->bm * p->bn);
+    }
     p->ws_bytes = off;
     const bool prepass = p->path == TG_PATH_TF32X3 || p->pack_a || p->pack_b;
     p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_lanes > 0 ? 1 : 0);

@@ -87,12 +87,14 @@ def test_plan_tiles_split_and_workspace():
     q = tg.plan(8192, 8192, 8192, num_sms=sms, split_k=1)
     assert q["tail_units"] == 0 and q["units"] == 1024 and q["launches"] == 2
     # long K, fewer units than lanes: FFMA (128 units, 152 CTAs) runs all of it
-    # stream-K on every CTA; 3xTF32 (64 pair units, rows far past L2, more
-    # than half a round) keeps whole units
+    # stream-K on every CTA
     lk = tg.plan(2048, 2048, 16384, num_sms=sms, path="ffma")
     assert (lk["units"], lk["tail_units"], lk["tail_lanes"], lk["grid"]) == (128, 128, 152, sms)
     lt = tg.plan(2048, 2048, 16384, num_sms=sms)
-    assert (lt["units"], lt["tail_units"], lt["grid"]) == (64, 0, 128)
+    # 3xTF32 (64 pair units, rows far past L2, more than half the lanes):
+    # split point, lane q runs the first 862 of unit q's 1024 K blocks in step
+    # with the others, the 12 remaining pairs share the rest
+    assert (lt["units"], lt["tail_units"], lt["tail_lanes"], lt["tail_kx"], lt["grid"]) == (64, 64, 76, 862, sms)
     # a tail that fills 90 % of a round or more is left alone
     assert tg.plan(128 * 2 * 70, 256, 4096, num_sms=sms)["tail_units"] == 0
     # a short K gives too little work per lane to share out
@@ -122,6 +124,54 @@ def test_plan_tiles_split_and_workspace():
     # K = 0 is one fill kernel
     z = tg.plan(10, 10, 0, num_sms=sms)
     assert z["launches"] == 1 and z["workspace_bytes"] == 0
+
+
+def _split_point_pieces(U, nkb, L, kx, slots):
+    """The split-point tail as the 3xTF32 kernel walks it: lane q < U runs the
+    first kx K blocks of unit q (slot q*slots); the other E = L - U lanes run
+    the remaining blocks of all units laid end to end, one piece per unit
+    they meet (slot q*slots + 1 + i, i counted from the first lane meeting
+    unit q's remainder)."""
+    E, rl = L - U, nkb - kx
+    R = U * rl
+    lane_of = lambda x: ((x + 1) * E + R - 1) // R - 1
+    for q in range(U):
+        yield q, q, 0, kx, q * slots
+    for e in range(E):
+        s, t = e * R // E, (e + 1) * R // E
+        q = s // rl
+        while s < t and q * rl < t:
+            b0 = q * rl
+            lo, hi = max(s, b0) - b0, min(t, b0 + rl) - b0
+            yield U + e, q, kx + lo, kx + hi, q * slots + 1 + (e - lane_of(b0))
+            q += 1
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 16384), (400, 8000, 20000)])
+def test_split_point_tail_covers_every_unit_once(M, N, K):
+    """Host model of the split-point tail (3xTF32 tails larger than L2 that
+    fill more than half the lanes): every K block of every tail unit runs
+    exactly once, the lockstep first parts and the remainder pieces give every
+    lane a similar share, and no two pieces share a partial slot."""
+    p = tg.plan(M, N, K, num_sms=152)
+    U, L, kx, nkb = p["tail_units"], p["tail_lanes"], p["tail_kx"], -(-K // p["block_k"])
+    assert kx > 0 and U < L and 10 * kx <= 9 * nkb
+    E = L - U
+    rl = nkb - kx
+    share = U * rl // E
+    slots = 1 + -(-rl // share) + 1
+    pieces = list(_split_point_pieces(U, nkb, L, kx, slots))
+    covered = np.zeros((U, nkb), np.int32)
+    used = set()
+    work = np.zeros(L, np.int64)
+    for lane, q, lo, hi, slot in pieces:
+        assert 0 <= lo < hi <= nkb and slot not in used and q * slots <= slot < (q + 1) * slots
+        used.add(slot)
+        covered[q, lo:hi] += 1
+        work[lane] += hi - lo
+    assert np.all(covered == 1)
+    assert work.max() - work.min() <= max(2, nkb // 50)  # balanced lanes
+    assert U * slots * p["pair"] * p["block_m"] * p["block_n"] * 4 <= p["workspace_bytes"]
 
 
 def _tail_pieces(tail_units, nkb, lanes):

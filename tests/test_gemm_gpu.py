@@ -262,7 +262,8 @@ def test_tf32x3_cluster_pairs_on_and_off(tg, pair, monkeypatch):
 
 
 TAIL_CASES = [(1000, 3000, 1100, "uniform", "tf32x3"), (1000, 3000, 1100, "int", "tf32x3"),
-              (4000, 3900, 8000, "uniform", "tf32x3"), (1000, 3000, 1100, "uniform", "ffma"),
+              (4000, 3900, 8000, "uniform", "tf32x3"), (400, 8000, 20000, "normal", "tf32x3"),
+              (400, 8000, 20000, "int", "tf32x3"), (1000, 3000, 1100, "uniform", "ffma"),
               (1000, 3000, 1100, "int", "ffma"), (400, 8000, 20000, "normal", "ffma")]
 
 
@@ -272,8 +273,11 @@ def test_balanced_tail(tg, M, N, K, dist, path):
     (pieces of a unit added by the tail reduce in lane order), with ragged
     edges: stream-K runs on both paths, with fewer units than lanes and runs
     shorter than a unit (some units spread over three lanes); equal K slices
-    on the 3xTF32 path when the tail's rows exceed L2 (4000 x 3900 x 8000).
-    Every output is checked; integer inputs bit-exactly."""
+    on the 3xTF32 path when the tail's rows exceed L2 (4000 x 3900 x 8000),
+    or a split point when such a tail fills more than half the lanes
+    (400 x 8000 x 20000: every unit's first K blocks on its own lane, the
+    rest spread over the others).  Every output is checked; integer inputs
+    bit-exactly."""
     A, B = make_inputs(M, N, K, dist, 700 + K % 97)
     p = tg.plan(M, N, K, path=path)
     assert p["tail_units"] > 0 and p["tail_lanes"] > p["tail_units"]
