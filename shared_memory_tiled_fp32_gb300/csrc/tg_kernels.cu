@@ -120,6 +120,10 @@ __host__ __device__ __forceinline__ long long tail_lane_of(long long x, long lon
 // pieces of v's run, one per tail unit it meets.  Returns false past the last
 // item.  Every role of the CTA walks j = 0, 1, ... and so sees the same
 // sequence; only j is carried between items.
+// kSplitPoint: the kernel may run a split-point tail (3xTF32); kOut: fill
+// out/ldo/direct too (the roles that store; the copy and MMA threads only
+// need the tile and its K range).
+template <bool kSplitPoint, bool kOut = true>
 __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, long long lanes, long long j,
                                           int rank, int BM, int BN, Unit* x) {
     const long long nfull = a.full_units > lane ? (a.full_units - lane + lanes - 1) / lanes : 0;
@@ -130,7 +134,7 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, lon
     j -= nfull;
     const long long blk = (long long)a.pair * BM * BN;
     int tm, tn;
-    if (a.tail_kx > 0) {  // split point: lockstep first parts, the rest spread out
+    if (kSplitPoint && a.tail_kx > 0) {  // split point: lockstep first parts, the rest spread out
         const long long U = a.tail_units, E = a.tail_lanes - U, rl = a.nkb - a.tail_kx, R = U * rl;
         for (long long v = lane; v < a.tail_lanes; v += lanes) {
             if (v < U) {
@@ -143,9 +147,11 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, lon
                 x->n0 = tn * BN;
                 x->kb0 = 0;
                 x->kb1 = a.tail_kx;
-                x->direct = false;
-                x->out = a.tail + v * a.tail_slots * blk - (long long)tm * blk - x->n0;
-                x->ldo = BN;
+                if (kOut) {
+                    x->direct = false;
+                    x->out = a.tail + v * a.tail_slots * blk - (long long)tm * blk - x->n0;
+                    x->ldo = BN;
+                }
                 return true;
             }
             const long long e = v - U;
@@ -162,10 +168,12 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, lon
             x->n0 = tn * BN;
             x->kb0 = a.tail_kx + (int)((s > b0 ? s : b0) - b0);
             x->kb1 = a.tail_kx + (int)((t < b0 + rl ? t : b0 + rl) - b0);
-            x->direct = false;
-            const long long slot = q * a.tail_slots + 1 + (e - tail_lane_of(b0, R, E));
-            x->out = a.tail + slot * blk - (long long)tm * blk - x->n0;
-            x->ldo = BN;
+            if (kOut) {
+                x->direct = false;
+                const long long slot = q * a.tail_slots + 1 + (e - tail_lane_of(b0, R, E));
+                x->out = a.tail + slot * blk - (long long)tm * blk - x->n0;
+                x->ldo = BN;
+            }
             return true;
         }
         return false;
@@ -186,14 +194,16 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, long long lane, lon
         x->n0 = tn * BN;
         x->kb0 = (int)((s > b0 ? s : b0) - b0);
         x->kb1 = (int)((e < b0 + a.nkb ? e : b0 + a.nkb) - b0);
-        x->direct = x->kb0 == 0 && x->kb1 == a.nkb;
-        if (x->direct) {  // the run holds the whole unit: C itself
-            x->out = a.out;
-            x->ldo = a.ldo;
-        } else {  // this slot's [pair*BM][BN] block, addressed with global row/column
-            const long long slot = 2 * v + (j == 0 ? 0 : 1);
-            x->out = a.tail + slot * blk - (long long)tm * blk - x->n0;
-            x->ldo = BN;
+        if (kOut) {
+            x->direct = x->kb0 == 0 && x->kb1 == a.nkb;
+            if (x->direct) {  // the run holds the whole unit: C itself
+                x->out = a.out;
+                x->ldo = a.ldo;
+            } else {  // this slot's [pair*BM][BN] block, addressed with global row/column
+                const long long slot = 2 * v + (j == 0 ? 0 : 1);
+                x->out = a.tail + slot * blk - (long long)tm * blk - x->n0;
+                x->ldo = BN;
+            }
         }
         return true;
     }
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
             Unit t;
-            for (long long j = 0; ok && work_item(args, blockIdx.x, gridDim.x, j, 0, BM, BN, &t); ++j) {
+            for (long long j = 0; ok && work_item<false, false>(args, blockIdx.x, gridDim.x, j, 0, BM, BN, &t); ++j) {
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteFfmaProducer)) {
                         ok = false;
@@ -344,7 +354,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     Unit t;
-    for (long long j = 0; work_item(args, blockIdx.x, gridDim.x, j, 0, BM, BN, &t); ++j) {
+    for (long long j = 0; work_item<false>(args, blockIdx.x, gridDim.x, j, 0, BM, BN, &t); ++j) {
         // acc[i][p] holds columns 32*(p/2) + 4ln + 2*(p%2) + {0, 1} of row i
         unsigned long long acc[8][8];
 #pragma unroll
@@ -469,7 +479,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 // epilogue drain one chunk while the MMAs fill the next.
 
 constexpr int kTfThreads = 384;
-constexpr int kTfLaunchRegs = 168, kTfIssueRegs = 56, kTfEpiRegs = 224;
+constexpr int kTfLaunchRegs = 168, kTfIssueRegs = 72, kTfEpiRegs = 216;
 static_assert(4 * 32 * kTfIssueRegs + 8 * 32 * kTfEpiRegs == kTfThreads * kTfLaunchRegs,
               "setmaxnreg split must balance the launch allocation");
 constexpr int kTfChunkKB = 16;                                     // K blocks per chunk (256 of K)
@@ -539,7 +549,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
             Unit t;
-            for (long long j = 0; ok && work_item(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
+            for (long long j = 0; ok && work_item<true, false>(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     // with a pair, "empty" completes only when both CTAs are done
                     // with the stage, since this CTA's B half lands in both
@@ -581,7 +591,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             uint32_t phase = 0, chunk = 0;
             bool ok = true;
             Unit t;
-            for (long long j = 0; ok && work_item(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
+            for (long long j = 0; ok && work_item<true, false>(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
                 for (int c0 = t.kb0; ok && c0 < t.kb1; c0 += kTfChunkKB, ++chunk) {
                     const int c1 = min(c0 + kTfChunkKB, t.kb1);
                     const uint32_t buf = chunk & 1u, par = (chunk >> 1) & 1u;
@@ -641,7 +651,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         uint32_t chunk = 0;
         bool ok = true;
         Unit t;
-        for (long long j = 0; ok && work_item(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
+        for (long long j = 0; ok && work_item<true>(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
