@@ -291,11 +291,12 @@ def test_balanced_tail(tg, M, N, K, dist, path):
     assert np.array_equal(got.view(np.uint32), again.view(np.uint32))
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
-def test_balanced_tail_scaled(tg, path):
-    """alpha and beta on a stream-K plan: applied by the GEMM epilogue for
-    units one lane ran whole and by the tail reduce for the others."""
-    M, N, K = 1000, 3000, 1100
+@pytest.mark.parametrize("path,M,N,K", [("tf32x3", 1000, 3000, 1100), ("ffma", 1000, 3000, 1100),
+                                        ("tf32x3", 400, 8000, 20000), ("tf32x3", 4000, 3900, 8000)])
+def test_balanced_tail_scaled(tg, path, M, N, K):
+    """alpha and beta on balanced last rounds (stream-K, split point, equal K
+    slices): applied by the GEMM epilogue for units one lane ran whole and by
+    the tail reduce for the others."""
     A, B = make_inputs(M, N, K, "uniform", 731)
     C0 = np.random.default_rng(732).uniform(-1, 1, (M, N)).astype(np.float32)
     Cd = torch.from_numpy(C0.copy()).cuda()
@@ -303,4 +304,4 @@ def test_balanced_tail_scaled(tg, path):
     torch.cuda.synchronize()
     assert tg.sync_status() == 0
     ref = oracle.sgemm_general(0, 0, 0.5, A.numpy(), B.numpy(), -1.5, C0.copy())
-    assert_close(Cd.cpu().numpy(), ref, K, f"stream-K scaled {path}")
+    assert_close(Cd.cpu().numpy(), ref, K, f"balanced tail scaled {path} {M}x{N}x{K}")
