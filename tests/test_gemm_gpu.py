@@ -305,3 +305,16 @@ def test_balanced_tail_scaled(tg, path, M, N, K):
     assert tg.sync_status() == 0
     ref = oracle.sgemm_general(0, 0, 0.5, A.numpy(), B.numpy(), -1.5, C0.copy())
     assert_close(Cd.cpu().numpy(), ref, K, f"balanced tail scaled {path} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+@pytest.mark.parametrize("M,N,K", [(3, 5, 1 << 22), (2, 1 << 24, 3), (1 << 22, 7, 9)])
+def test_extreme_aspect_ratios(tg, path, M, N, K):
+    """Products of hundreds of MB with one dimension in the millions and the
+    others tiny: a K split over 2^18 K blocks, 65,536 tile columns, 32,768
+    tile rows (64-bit tile and row offsets, ghost-heavy edge tiles), every
+    output checked against the oracle."""
+    A, B = make_inputs(M, N, K, "uniform", 40 + (M % 7))
+    C = run(tg, A, B, path=path)
+    ref = oracle.sgemm(A.numpy(), B.numpy())  # at most 2^25 outputs, 2^28 multiply-adds
+    assert_close(C, ref, K, f"{M}x{N}x{K} {path}")
