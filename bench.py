@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "tf32x3", "ffma"])
+    ap.add_argument("--path", default="auto", choices=["auto", "tf32x3", "ffma", "tiled"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--op-a", default="N", choices=["N", "T"], help="A stored transposed (K x M)")
     ap.add_argument("--op-b", default="N", choices=["N", "T"], help="B stored transposed (N x K)")
@@ -344,7 +344,8 @@ def run_reduce(args, world, rank, local):
 
 
 def run_all_configs(args, local):
-    """Step and GEMM-kernel throughput of every workload on both paths."""
+    """Step and GEMM-kernel throughput of every workload on each path (the
+    tiled path only where the automatic choice would take it)."""
     import shared_memory_tiled_fp32_gb300 as tg
 
     torch.cuda.set_device(local)
@@ -353,7 +354,8 @@ def run_all_configs(args, local):
     for name, w in WORKLOADS.items():
         A, B = (t.to(dev) for t in make_inputs(w.M, w.N, w.K, w.dist, w.seed))
         C = torch.empty(w.M, w.N, device=dev)
-        for path in ("tf32x3", "ffma"):
+        auto = tg.plan(w.M, w.N, w.K, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())["path"]
+        for path in ("tf32x3", "ffma") + (("tiled",) if auto == "tiled" else ()):
             plan = tg.plan(w.M, w.N, w.K, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr(), path=path)
             ws = torch.empty(max(1, plan["workspace_bytes"] // 4 + 64), device=dev)
             steps = max(3, min(args.steps, int(2e12 / w.flop) + 3))

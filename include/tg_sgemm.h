@@ -60,16 +60,21 @@ typedef enum tg_status {
  * transposed (the stored matrix is op(X)^T). */
 typedef enum tg_op { TG_OP_N = 0, TG_OP_T = 1 } tg_op;
 
-/* Math paths.  Both are hand-written sm_103a kernels fed by TMA through an
- * mbarrier pipeline with warp-specialised producer and consumer warps.
+/* Math paths, all hand-written sm_103a kernels.
  *  - TG_PATH_TF32X3: tensor cores (tcgen05.mma kind::tf32, accumulator in
- *    tensor memory).  Each float is split into hi = tf32(x) and
- *    lo = tf32(x - hi); the product is lo*hi + hi*lo + hi*hi.  A pre-pass
- *    writes hi/lo copies of A and of B transposed.
+ *    tensor memory), fed through an mbarrier pipeline by a producer warp.
+ *    Each float is split into hi = tf32(x) and lo = tf32(x - hi); the product
+ *    is lo*hi + hi*lo + hi*hi.  A pre-pass writes hi/lo tiles of A and of B
+ *    transposed.
  *  - TG_PATH_FFMA: register-blocked fused multiply-add on the CUDA cores, fp32
- *    throughout.
- *  - TG_PATH_AUTO: TG_PATH_TF32X3. */
-typedef enum tg_path { TG_PATH_AUTO = 0, TG_PATH_FFMA = 1, TG_PATH_TF32X3 = 2 } tg_path;
+ *    throughout, TMA-fed through the same kind of pipeline.
+ *  - TG_PATH_TILED: the shared-memory tiled kernel for small products: one
+ *    launch (no pre-pass, no split), 64 x 64 tiles, fp32 fused multiply-adds;
+ *    operands read in place with any alignment.  A block of 256 threads
+ *    handles one tile, so large products run it far below the other paths.
+ *  - TG_PATH_AUTO: TG_PATH_TILED for small products (where one launch beats
+ *    the three of the 3xTF32 path; see tg_sgemm_plan), else TG_PATH_TF32X3. */
+typedef enum tg_path { TG_PATH_AUTO = 0, TG_PATH_FFMA = 1, TG_PATH_TF32X3 = 2, TG_PATH_TILED = 3 } tg_path;
 
 /* Options for tg_sgemm_ex.  Zero-initialise and set what you need.
  *  path            tg_path value.
@@ -94,7 +99,7 @@ typedef struct tg_sgemm_opts {
 
 /* What one call would launch (filled by tg_sgemm_plan). */
 typedef struct tg_plan_info {
-    int path;          /* TG_PATH_FFMA or TG_PATH_TF32X3 */
+    int path;          /* TG_PATH_FFMA, TG_PATH_TF32X3 or TG_PATH_TILED */
     int split_k;       /* K slices */
     int block_m, block_n, block_k, stages; /* CTA tile and pipeline depth */
     int tiles_m, tiles_n;

@@ -20,6 +20,16 @@ constexpr int kTf32BM = 128, kTf32BN = 256, kTf32BK = 16, kTf32Stages = 4;
 // register block, K staged 32 floats at a time, 4 stages of 48 KiB.
 constexpr int kFfmaBM = 128, kFfmaBN = 256, kFfmaBK = 32, kFfmaStages = 4;
 
+// Tiled path (small products): 64 x 64 tiles, K staged 16 at a time.
+constexpr int kTiledBM = 64, kTiledBN = 64, kTiledBK = 16;
+// The automatic path takes the tiled kernel up to 2^26 multiply-adds with K
+// at most 512 (one block per tile: its time grows with K, and past that size
+// the 3xTF32 path's three launches cost less than the tiled path's math;
+// measured on GB300: 256^3 15.9 vs 21.2 us, 384^3 21.0 vs 23.6, 512^3 27.9
+// vs 22.2, 128 x 128 x 8192 416 vs 35).
+constexpr double kTiledMaxMacs = 67108864.0;  // 2^26
+constexpr int kTiledMaxK = 512;
+
 constexpr size_t kWsAlign = 256;
 
 #ifdef __CUDACC__

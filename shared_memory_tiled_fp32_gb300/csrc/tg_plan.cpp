@@ -53,6 +53,13 @@ long long tail_operand_bytes(const Plan& p, long long rem) {
     return (rows + cols) * p.k16 * 8;
 }
 
+// Whether the one-launch tiled path beats the 3xTF32 path's pre-pass, GEMM
+// and reduce for this product (see its definition for the measured basis).
+bool tiled_is_faster(int M, int N, int K, int num_sms) {
+    (void)num_sms;
+    return (double)M * N * K <= kTiledMaxMacs && K <= kTiledMaxK;
+}
+
 }  // namespace
 
 tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int lda, const void* B,
@@ -65,7 +72,7 @@ tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int l
     const int b_rows = op_b == TG_OP_N ? K : N, b_cols = op_b == TG_OP_N ? N : K;
     if (lda < std::max(1, a_cols) || ldb < std::max(1, b_cols) || ldc < std::max(1, N))
         return TG_ERR_INVALID_VALUE;
-    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3)
+    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3 && path != TG_PATH_TILED)
         return TG_ERR_INVALID_VALUE;
     if (split_k < 0) return TG_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return TG_OK;  // nothing is read or written
@@ -101,12 +108,19 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     p->alpha = alpha;
     p->beta = beta;
     p->num_sms = num_sms;
-    p->path = (path == TG_PATH_FFMA) ? TG_PATH_FFMA : TG_PATH_TF32X3;
+    if (path == TG_PATH_FFMA || path == TG_PATH_TILED)
+        p->path = path;
+    else if (path == TG_PATH_AUTO && split_k <= 1 && tiled_is_faster(M, N, K, num_sms))
+        p->path = TG_PATH_TILED;
+    else
+        p->path = TG_PATH_TF32X3;
     p->vec_c = C != nullptr && (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
     if (p->path == TG_PATH_TF32X3) {
         p->bm = kTf32BM; p->bn = kTf32BN; p->bk = kTf32BK; p->stages = kTf32Stages;
-    } else {
+    } else if (p->path == TG_PATH_FFMA) {
         p->bm = kFfmaBM; p->bn = kFfmaBN; p->bk = kFfmaBK; p->stages = kFfmaStages;
+    } else {
+        p->bm = kTiledBM; p->bn = kTiledBN; p->bk = kTiledBK; p->stages = 2;
     }
     p->k4 = (int)round_up((size_t)K, 4);
     p->k16 = (int)round_up((size_t)K, 16);
@@ -125,6 +139,14 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     p->tiles_n = (int)cdiv(N, p->bn);
     p->nkb = (int)cdiv(K, p->bk);
     const long long tiles = (long long)p->tiles_m * p->tiles_n;
+    if (p->path == TG_PATH_TILED) {  // one block per tile, one launch, no workspace
+        p->split = 1;
+        p->units = tiles;
+        p->full_units = tiles;
+        p->grid = (int)std::min<long long>(tiles, 0x7fffffffLL);
+        p->launches = 1;
+        return;
+    }
 
     // Split K when the tiles alone would leave most SMs idle.  Every slice
     // keeps at least 4 K blocks, and there are at most 16 slices.

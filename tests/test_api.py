@@ -124,6 +124,15 @@ def test_plan_tiles_split_and_workspace():
     # K = 0 is one fill kernel
     z = tg.plan(10, 10, 0, num_sms=sms)
     assert z["launches"] == 1 and z["workspace_bytes"] == 0
+    # small products: the one-launch tiled path (64 x 64 tiles, no workspace,
+    # operands in place), unless a K split is asked for
+    t = tg.plan(256, 256, 256, num_sms=sms)
+    assert (t["path"], t["tiles_m"], t["tiles_n"], t["launches"], t["workspace_bytes"], t["prepass"]) == \
+        ("tiled", 4, 4, 1, 0, 0)
+    assert tg.plan(256, 256, 256, num_sms=sms, split_k=2)["path"] == "tf32x3"
+    assert tg.plan(512, 512, 512, num_sms=sms)["path"] == "tf32x3"    # 2^27 multiply-adds
+    assert tg.plan(64, 64, 8192, num_sms=sms)["path"] == "tf32x3"     # long K: split instead
+    assert tg.plan(777, 1029, 513, num_sms=sms, path="tiled")["tiles_m"] == 13
 
 
 def _split_point_pieces(U, nkb, L, kx, slots):

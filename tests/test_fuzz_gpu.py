@@ -33,7 +33,7 @@ def draw_case(rng):
     op_a, op_b = int(rng.integers(0, 2)), int(rng.integers(0, 2))
     alpha = float(rng.choice([1.0, 1.0, -0.5, 2.0, 0.3]))
     beta = float(rng.choice([0.0, 0.0, 1.0, -1.5]))
-    path = str(rng.choice(["tf32x3", "ffma"]))
+    path = str(rng.choice(["tf32x3", "ffma", "tiled"]))
     split = int(rng.choice([0, 0, 1, 2, 5]))
     pads = [int(rng.integers(0, 6)) for _ in range(3)]
     offs = [int(rng.integers(0, 4)) for _ in range(3)]

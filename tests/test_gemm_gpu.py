@@ -52,6 +52,8 @@ CASES = [
     ("sq8192_normal", "tf32x3", 0), ("sq8192_normal", "ffma", 0),
     ("longk_2048x2048x16384_normal", "tf32x3", 0), ("longk_2048x2048x16384_normal", "tf32x3", 2),
     ("longk_2048x2048x16384_normal", "tf32x3", 4), ("longk_2048x2048x16384_normal", "ffma", 0),
+    ("sq256_uniform", "tiled", 0), ("sq256_int", "tiled", 0), ("ragged_777x1029x513", "tiled", 0),
+    ("sq4096_int", "tiled", 0), ("sq4096_uniform", "auto", 0), ("sq256_uniform", "auto", 0),
 ]
 
 
@@ -67,7 +69,7 @@ def test_workload(tg, name, path, split):
         assert_close(got, ref, w.K, f"{name} {path} split {split}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
 def test_ragged_random_shapes(tg, path):
     """Shapes around tile edges and random shapes in [1, 300]^3."""
     rng = np.random.default_rng(7)
@@ -80,7 +82,7 @@ def test_ragged_random_shapes(tg, path):
         assert_close(run(tg, A, B, path=path), ref, K, f"{path} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
 def test_integer_random_shapes_bitexact(tg, path):
     rng = np.random.default_rng(8)
     for i in range(6):
@@ -91,7 +93,7 @@ def test_integer_random_shapes_bitexact(tg, path):
             assert_bitexact(run(tg, A, B, path=path, split_k=split), ref, f"{path} {M}x{N}x{K} s{split}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
 @pytest.mark.parametrize("split", [0, 1, 2])
 def test_strided_unaligned_views_and_canaries(tg, path, split):
     """Odd leading dimensions, unaligned base pointers (sub-views at odd
@@ -125,7 +127,7 @@ def test_strided_unaligned_views_and_canaries(tg, path, split):
 
 def test_k_zero_and_empty(tg):
     dev = torch.device("cuda")
-    for path in ("tf32x3", "ffma"):
+    for path in ("tf32x3", "ffma", "tiled"):
         C = torch.empty(5, 7, device=dev)
         fill_sentinel(C)
         tg.matmul(torch.empty(5, 0, device=dev), torch.empty(0, 7, device=dev), out=C, path=path)
@@ -143,7 +145,7 @@ def test_nan_row_propagates(tg):
     A[3, 17] = float("nan")
     ref = oracle.sgemm(A.numpy(), B.numpy())
     assert np.all(np.isnan(ref[3]))
-    for path in ("tf32x3", "ffma"):
+    for path in ("tf32x3", "ffma", "tiled"):
         C = run(tg, A, B, path=path)
         assert np.all(np.isnan(C[3])), path
         keep = np.arange(M) != 3
@@ -152,7 +154,7 @@ def test_nan_row_propagates(tg):
 
 def test_deterministic(tg):
     A, B, _, _ = workload_case("ragged_777x1029x513")
-    for path in ("tf32x3", "ffma"):
+    for path in ("tf32x3", "ffma", "tiled"):
         c1 = run(tg, A, B, path=path)
         c2 = run(tg, A, B, path=path)
         assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32)), path
