@@ -182,12 +182,15 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
                         float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts);
 
 /* The output blocks tg_sgemm_host would use (host arithmetic only): C is cut
- * into *row_blocks x *col_blocks blocks of *block_rows x *block_cols (the last
- * ones ragged), chosen to minimise a modelled pipeline time, returned in
- * *model_ms (copies at the rates measured on GB300).  path as in
- * tg_sgemm_opts; num_sms = SMs planned for (0 = the current device). */
+ * into *row_blocks x *col_blocks blocks; row block 0 has *first_block_rows
+ * rows (a short first block lets the first product start sooner), the others
+ * *block_rows, columns *block_cols (the last ones ragged), chosen to minimise
+ * a modelled pipeline time, returned in *model_ms (copies at the rates
+ * measured on GB300).  path as in tg_sgemm_opts; num_sms = SMs planned for
+ * (0 = the current device). */
 tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* row_blocks,
-                               int* col_blocks, int* block_rows, int* block_cols, double* model_ms);
+                               int* col_blocks, int* first_block_rows, int* block_rows, int* block_cols,
+                               double* model_ms);
 
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns TG_ERR_TIMEOUT if any kernel of this library on this device gave up

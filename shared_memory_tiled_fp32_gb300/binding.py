@@ -116,7 +116,7 @@ def lib():
         L.tg_sgemm_noalloc.argtypes = gemm
         L.tg_sgemm_noalloc.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
-        L.tg_sgemm_host_blocks.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ctypes.POINTER(ctypes.c_double)]
+        L.tg_sgemm_host_blocks.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ip, ctypes.POINTER(ctypes.c_double)]
         L.tg_sgemm_host_blocks.restype = i
         L.tg_sgemm_plan.argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
         L.tg_sgemm_plan.restype = i
@@ -341,13 +341,13 @@ def sgemm_host(A, B, out, *, path="auto", split_k=0, stream=None):
 
 def host_blocks(M, N, K, *, path="auto", num_sms=0) -> dict:
     """The row x column output blocks sgemm_host pipelines (host arithmetic)."""
-    r = [ctypes.c_int() for _ in range(4)]
+    r = [ctypes.c_int() for _ in range(5)]
     ms = ctypes.c_double()
     st = lib().tg_sgemm_host_blocks(M, N, K, PATHS[path] if isinstance(path, str) else int(path), num_sms,
                                     *[ctypes.byref(x) for x in r], ctypes.byref(ms))
     _check(st, "tg_sgemm_host_blocks")
-    return {"row_blocks": r[0].value, "col_blocks": r[1].value, "block_rows": r[2].value,
-            "block_cols": r[3].value, "model_ms": ms.value}
+    return {"row_blocks": r[0].value, "col_blocks": r[1].value, "first_block_rows": r[2].value,
+            "block_rows": r[3].value, "block_cols": r[4].value, "model_ms": ms.value}
 
 
 def plan(M, N, K, lda=None, ldb=None, ldc=None, *, A=0, B=0, C=0, path="auto", split_k=0,

@@ -252,7 +252,7 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     // of earlier ones.  A and B are split once, by the first product that
     // reads each block, into shared hi/lo regions.
     const HostBlocks hb = choose_host_blocks(M, N, K, path, d->num_sms);
-    const int pm = hb.pm, pn = hb.pn, mb = hb.mb, nb = hb.nb;
+    const int pm = hb.pm, pn = hb.pn, nb = hb.nb, mb_max = std::max(hb.first, hb.mb);
 
     // device copies: 16-byte row pitches, so TMA reads them in place
     const size_t a_bytes = 4ull * M * k4, b_bytes = 4ull * (size_t)std::max(K, 1) * n4,
@@ -261,14 +261,14 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     const long long k16 = ((long long)std::max(K, 1) + 15) / 16 * 16;
     // split tiles (rows padded to 256): all of B^T's, and one A row block's
     const size_t b_split = tf32 ? align(8ull * ((N + 255) / 256 * 256) * k16) : 0;
-    const size_t a_split = tf32 ? align(8ull * ((mb + 255) / 256 * 256) * k16) : 0;
+    const size_t a_split = tf32 ? align(8ull * ((mb_max + 255) / 256 * 256) * k16) : 0;
     // placeholder pointers with the alignment the real ones will have
     const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
     size_t ws_max = 0;  // over the (at most 4) block shapes: whole or ragged rows x columns
-    for (int i : {0, pm - 1})
+    for (int i : {0, std::min(1, pm - 1), pm - 1})
         for (int j : {0, pn - 1}) {
             Plan pl;
-            make_plan(TG_OP_N, TG_OP_N, std::min(mb, M - i * mb), std::min(nb, N - j * nb), K, 1.0f, al, (int)k4,
+            make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), std::min(nb, N - j * nb), K, 1.0f, al, (int)k4,
                       al, (int)n4, 0.0f, al, (int)n4, path, o.split_k, d->num_sms, &pl, tf32, tf32);
             ws_max = std::max(ws_max, pl.ws_bytes);
         }
@@ -299,7 +299,7 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
               cudaStreamWaitEvent(hp->s_in, ev[0], 0) == cudaSuccess &&
               cudaStreamWaitEvent(hp->s_out, ev[0], 0) == cudaSuccess;
     auto copy_a = [&](int i) {
-        const int i0 = i * mb, Mi = std::min(mb, M - i0);
+        const int i0 = hb.row0(i), Mi = hb.rows(i, M);
         ok = ok &&
              cudaMemcpy2DAsync(fA + (size_t)i0 * k4, 4ull * k4, A + (size_t)i0 * lda, 4ull * lda, 4ull * K, Mi,
                                cudaMemcpyHostToDevice, hp->s_in) == cudaSuccess &&
@@ -320,7 +320,7 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     st = ok ? TG_OK : TG_ERR_CUDA;
     for (int i = 0; st == TG_OK && i < pm; ++i) {
         for (int j = 0; st == TG_OK && j < pn; ++j) {
-            const int i0 = i * mb, Mi = std::min(mb, M - i0), j0 = j * nb, Nj = std::min(nb, N - j0);
+            const int i0 = hb.row0(i), Mi = hb.rows(i, M), j0 = j * nb, Nj = std::min(nb, N - j0);
             if (K > 0 && ((j == 0 && cudaStreamWaitEvent(stream, ev[3 + i], 0) != cudaSuccess) ||
                           (i == 0 && cudaStreamWaitEvent(stream, ev[11 + j], 0) != cudaSuccess))) {
                 st = TG_ERR_CUDA;
@@ -363,10 +363,10 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
 }
 
 tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* row_blocks, int* col_blocks,
-                               int* block_rows, int* block_cols, double* model_ms) {
+                               int* first_block_rows, int* block_rows, int* block_cols, double* model_ms) {
     using namespace tg;
-    if (M < 0 || N < 0 || K < 0 || row_blocks == nullptr || col_blocks == nullptr || block_rows == nullptr ||
-        block_cols == nullptr)
+    if (M < 0 || N < 0 || K < 0 || row_blocks == nullptr || col_blocks == nullptr || first_block_rows == nullptr ||
+        block_rows == nullptr || block_cols == nullptr)
         return TG_ERR_INVALID_VALUE;
     if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3) return TG_ERR_INVALID_VALUE;
     if (num_sms <= 0) {
@@ -378,6 +378,7 @@ tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* 
     const HostBlocks hb = choose_host_blocks(M, N, K, path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3, num_sms);
     *row_blocks = hb.pm;
     *col_blocks = hb.pn;
+    *first_block_rows = hb.first;
     *block_rows = hb.mb;
     *block_cols = hb.nb;
     if (model_ms != nullptr) *model_ms = hb.model_ms;

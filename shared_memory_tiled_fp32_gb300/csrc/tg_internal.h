@@ -117,13 +117,19 @@ struct Plan {
 tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int lda, const void* B,
                    int ldb, const void* C, int ldc, int path, int split_k, bool need_pointers = true);
 
-// Output blocks of the host-buffer entry point: C is cut into pm x pn blocks
-// of mb rows (a multiple of 128) and nb columns (a multiple of 256); the
-// choice minimises a modelled pipeline time (copies in, products, copies
+// Output blocks of the host-buffer entry point: C is cut into pm x pn blocks;
+// row block 0 has `first` rows, the others mb (multiples of 128, the last
+// ragged), column blocks nb columns (a multiple of 256, the last ragged).
+// The choice minimises a modelled pipeline time (copies in, products, copies
 // out).  Host arithmetic only.
 struct HostBlocks {
-    int pm = 1, pn = 1, mb = 0, nb = 0;
+    int pm = 1, pn = 1, first = 0, mb = 0, nb = 0;
     double model_ms = 0.0;
+    int row0(int i) const { return i == 0 ? 0 : first + (i - 1) * mb; }
+    int rows(int i, int M) const {
+        const int r = M - row0(i), cap = i == 0 ? first : mb;
+        return r < cap ? r : cap;
+    }
 };
 HostBlocks choose_host_blocks(int M, int N, int K, int path, int num_sms);
 

@@ -296,67 +296,78 @@ HostBlocks model_host_blocks(int M, int N, int K, int path, int num_sms) {
     const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
     const int k4 = (int)round_up((size_t)std::max(K, 1), 4), n4 = (int)round_up((size_t)std::max(N, 1), 4);
     HostBlocks best;
-    best.mb = (int)round_up((size_t)std::max(M, 1), 128);
+    best.mb = best.first = (int)round_up((size_t)std::max(M, 1), 128);
     best.nb = (int)round_up((size_t)std::max(N, 1), 256);
     best.model_ms = -1.0;
     if (M == 0 || N == 0) return best;
     // below 2^33 multiply-adds one block: the launches would cost more than
     // the copies they hide, and the result is then bit-identical to tg_sgemm's
     const int max_blocks = (double)M * N * K >= 8589934592.0 ? 8 : 1;
+    auto evaluate = [&](int pm, int first, int mb, int pn, int nb) {
+        auto row0 = [&](int i) { return i == 0 ? 0 : first + (i - 1) * mb; };
+        auto rows_of = [&](int i) { return std::min(i == 0 ? first : mb, M - row0(i)); };
+        // copies in, in the order the products first need them
+        std::vector<double> a_ready(pm), b_ready(pn);
+        double t_in = 0.0;
+        auto copy_a = [&](int i) {
+            t_in += 4.0 * rows_of(i) * K / bw_in;
+            a_ready[i] = t_in;
+        };
+        auto copy_b = [&](int j) {
+            t_in += 4.0 * std::min(nb, N - j * nb) * K / bw_in;
+            b_ready[j] = t_in;
+        };
+        copy_a(0);
+        for (int j = 0; j < pn; ++j) copy_b(j);
+        for (int i = 1; i < pm; ++i) copy_a(i);
+        // products and copies out; the blocks have at most 6 shapes (first,
+        // whole or ragged rows x whole or ragged columns)
+        double shape_s[3][2] = {{-1.0, -1.0}, {-1.0, -1.0}, {-1.0, -1.0}};
+        double t_gpu = 0.0, t_out = 0.0;
+        for (int i = 0; i < pm; ++i) {
+            for (int j = 0; j < pn; ++j) {
+                const int rows = rows_of(i), cols = std::min(nb, N - j * nb);
+                double t = std::max({t_gpu, a_ready[i], b_ready[j]});
+                if (tf32) {
+                    if (j == 0) t += 12.0 * rows * K / bw_split;
+                    if (i == 0) t += 12.0 * cols * K / bw_split;
+                }
+                double& ps = shape_s[i == 0 ? 0 : (i == pm - 1 ? 2 : 1)][j == pn - 1];
+                if (ps < 0.0) {
+                    Plan pl;
+                    make_plan(TG_OP_N, TG_OP_N, rows, cols, K, 1.0f, al, k4, al, n4, 0.0f, al, n4, path, 0,
+                              num_sms, &pl, tf32, tf32);
+                    ps = product_seconds(pl, rate);
+                }
+                t += ps;
+                t_gpu = t;
+                t_out = std::max(t_out, t) + 4.0 * rows * cols / bw_out;
+            }
+        }
+        const double ms = t_out * 1e3;
+        if (best.model_ms < 0.0 || ms < best.model_ms * 0.98) {  // prefer earlier (fewer) blocks on near ties
+            best.pm = pm;
+            best.pn = pn;
+            best.first = first;
+            best.mb = mb;
+            best.nb = nb;
+            best.model_ms = ms;
+        }
+    };
     for (int pm = 1; pm <= max_blocks; ++pm) {
         for (int pn = 1; pn <= max_blocks; ++pn) {
-            const int mb = (int)round_up((size_t)cdiv(M, pm), 128), nb = (int)round_up((size_t)cdiv(N, pn), 256);
-            const int qm = (int)cdiv(M, mb), qn = (int)cdiv(N, nb);
-            if (qm != pm || qn != pn) continue;  // same blocks as a smaller count
-            if (pm > 1 && mb < 512) continue;
-            if (pn > 1 && nb < 512) continue;
-            // copies in
-            std::vector<double> a_ready(pm), b_ready(pn);
-            double t_in = 0.0;
-            auto copy_a = [&](int i) {
-                const int rows = std::min(mb, M - i * mb);
-                t_in += 4.0 * rows * K / bw_in;
-                a_ready[i] = t_in;
-            };
-            auto copy_b = [&](int j) {
-                const int cols = std::min(nb, N - j * nb);
-                t_in += 4.0 * cols * K / bw_in;
-                b_ready[j] = t_in;
-            };
-            copy_a(0);
-            for (int j = 0; j < pn; ++j) copy_b(j);
-            for (int i = 1; i < pm; ++i) copy_a(i);
-            // products and copies out; the blocks have at most 4 shapes
-            // (whole or ragged rows x whole or ragged columns)
-            double shape_s[2][2] = {{-1.0, -1.0}, {-1.0, -1.0}};
-            double t_gpu = 0.0, t_out = 0.0;
-            for (int i = 0; i < pm; ++i) {
-                for (int j = 0; j < pn; ++j) {
-                    const int rows = std::min(mb, M - i * mb), cols = std::min(nb, N - j * nb);
-                    double t = std::max({t_gpu, a_ready[i], b_ready[j]});
-                    if (tf32) {
-                        if (j == 0) t += 12.0 * rows * K / bw_split;
-                        if (i == 0) t += 12.0 * cols * K / bw_split;
-                    }
-                    double& ps = shape_s[i == pm - 1][j == pn - 1];
-                    if (ps < 0.0) {
-                        Plan pl;
-                        make_plan(TG_OP_N, TG_OP_N, rows, cols, K, 1.0f, al, k4, al, n4, 0.0f, al, n4, path, 0,
-                                  num_sms, &pl, tf32, tf32);
-                        ps = product_seconds(pl, rate);
-                    }
-                    t += ps;
-                    t_gpu = t;
-                    t_out = std::max(t_out, t) + 4.0 * rows * cols / bw_out;
-                }
-            }
-            const double ms = t_out * 1e3;
-            if (best.model_ms < 0.0 || ms < best.model_ms * 0.98) {  // prefer fewer blocks on near ties
-                best.pm = pm;
-                best.pn = pn;
-                best.mb = mb;
-                best.nb = nb;
-                best.model_ms = ms;
+            const int nb = (int)round_up((size_t)cdiv(N, pn), 256);
+            if (cdiv(N, nb) != pn || (pn > 1 && nb < 512)) continue;
+            // equal row blocks
+            const int mb = (int)round_up((size_t)cdiv(M, pm), 128);
+            if (cdiv(M, mb) == pm && (pm == 1 || mb >= 512)) evaluate(pm, mb, mb, pn, nb);
+            // a short first row block (the first product starts sooner), the
+            // rest of the rows in pm - 1 equal blocks
+            for (int first = 256; pm > 1 && first <= 2048; first *= 2) {
+                if (first >= M) break;
+                const int rest = (int)round_up((size_t)cdiv(M - first, pm - 1), 128);
+                if (rest <= first || rest < 512 || cdiv(M - first, rest) != pm - 1) continue;
+                evaluate(pm, first, rest, pn, nb);
             }
         }
     }

@@ -295,10 +295,12 @@ def test_host_blocks_cover_c(M, N, K, path):
     """The host entry's output blocks: rows in multiples of 128, columns in
     multiples of 256, exactly covering C (the last ones ragged), at most 8 x 8."""
     h = tg.host_blocks(M, N, K, path=path, num_sms=152)
-    pm, pn, mb, nb = h["row_blocks"], h["col_blocks"], h["block_rows"], h["block_cols"]
+    pm, pn, f, mb, nb = h["row_blocks"], h["col_blocks"], h["first_block_rows"], h["block_rows"], h["block_cols"]
     assert 1 <= pm <= 8 and 1 <= pn <= 8
-    assert mb % 128 == 0 and nb % 256 == 0
-    assert -(-M // mb) == pm and -(-N // nb) == pn
+    assert f % 128 == 0 and mb % 128 == 0 and nb % 256 == 0 and f <= mb
+    # row blocks: [0, f), then pm - 1 blocks of mb rows, the last ragged
+    assert (pm == 1 and f >= M) or (pm > 1 and f < M and -(-(M - f) // mb) == pm - 1)
+    assert -(-N // nb) == pn
     assert h["model_ms"] >= 0
     if pm > 1:
         assert mb >= 512
@@ -312,7 +314,7 @@ def test_host_blocks_pipeline_large_products():
     h = tg.host_blocks(8192, 8192, 8192, path="tf32x3", num_sms=152)
     assert h["row_blocks"] * h["col_blocks"] >= 4
     assert 4 * 8192 * (h["block_rows"] + h["block_cols"]) <= 0.5 * 4 * 8192 * 16384
-    assert tg.lib().tg_sgemm_host_blocks(-1, 4, 4, 0, 152, *[ctypes.byref(ctypes.c_int()) for _ in range(4)],
+    assert tg.lib().tg_sgemm_host_blocks(-1, 4, 4, 0, 152, *[ctypes.byref(ctypes.c_int()) for _ in range(5)],
                                          None) == 1
     # below 2^33 multiply-adds: one block (bit-identical to the device entry)
     small = tg.host_blocks(777, 1029, 513, path="tf32x3", num_sms=152)

@@ -221,8 +221,8 @@ def test_host_buffer_entry_2d_blocks(tg, path):
     Cbig = torch.full((M, N + 3), float("nan")).pin_memory()
     C = Cbig[:, :N]
     tg.sgemm_host(Ap, Bp, C, path=path)
-    mb = hb["block_rows"]
-    edges = [r for i in range(1, hb["row_blocks"]) for r in (i * mb - 1, i * mb)]
+    f, mb = hb["first_block_rows"], hb["block_rows"]
+    edges = [r for i in range(1, hb["row_blocks"]) for r in (f + (i - 1) * mb - 1, f + (i - 1) * mb)]
     rows = np.sort(np.random.default_rng(4).choice(M, 120, replace=False))
     rows = np.unique(np.concatenate([rows, [0, M - 1], edges]))
     ref = oracle.sgemm_rows(A.numpy(), B.numpy(), rows)
