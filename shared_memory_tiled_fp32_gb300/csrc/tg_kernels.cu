@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 // store the tile after its last chunk.  The remaining error is about
 // 7e-9 * 256 ~ 2e-6 relative, independent of K.
 //
-// Warp roles (384 threads, 3 warpgroups): warp 0 = TMA producer, warp 1 =
+// Warp roles (384 threads, 3 warpgroups): warp 0 = copy producer, warp 1 =
 // tensor-memory owner and MMA issuer (one thread), warps 2-3 idle; warps 4-11
 // = epilogue.  Epilogue warp e reads tensor-memory lanes 32*(e%4).. (a warp
 // may only touch the lane quarter of its warp index modulo 4) and columns
