@@ -122,19 +122,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
-// 2-D tiled load delivered to the same shared-memory offset of every CTA in
-// `cta_mask` (cluster ranks), each signalling its own mbarrier at `bar`'s
-// offset.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map,
-                                                      uint64_t* bar, int32_t x, int32_t y,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // 1-D bulk copy of `bytes` contiguous bytes (16-byte aligned, a multiple of
 // 16) from global to this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
