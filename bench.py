@@ -213,7 +213,30 @@ def cpu_baseline(w, A_np, B_np, target_s):
     value = 2.0 * len(rows) * w.N * w.K / t / 1e12
     return rows, ref, {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
                        "sample": f"{len(rows)} of {w.M} output rows (all {w.N} columns), seeded; "
-                                 f"{t:.1f} s of fp64 triple-loop work"}
+                                 f"{t:.1f} s of fp64 triple-loop work",
+                       "full_matrix_s_extrapolated": 2.0 * w.M * w.N * w.K / (value * 1e12),
+                       "single_thread_s": oracle_single_thread()}
+
+
+def oracle_single_thread(names=("sq256_uniform", "ragged_777x1029x513")):
+    """Whole products of the two small workloads on one host thread (each
+    well under a second), seconds per product."""
+    import oracle
+
+    n0 = oracle.threads()
+    out = {}
+    try:
+        oracle.set_threads(1)
+        for name in names:
+            w = WORKLOADS[name]
+            A, B = make_inputs(w.M, w.N, w.K, w.dist, w.seed)
+            A_np, B_np = A.numpy(), B.numpy()
+            t0 = time.perf_counter()
+            oracle.sgemm(A_np, B_np)
+            out[name] = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(n0)
+    return out
 
 
 def run_reference(args, w, world, rank):
@@ -566,6 +589,7 @@ def main():
     if not args.no_probes:
         probes = {"tf32_mma_tensor_tflops": tg.binding.probe_tf32_mma_tflops(use_collector=False),
                   "tf32_mma_tensor_tflops_collector": tg.binding.probe_tf32_mma_tflops(use_collector=True),
+                  "f16_mma_tensor_tflops": tg.binding.probe_f16_mma_tflops(),
                   "ffma_tflops": tg.binding.probe_ffma_tflops(),
                   "note": "tcgen05 kind::tf32 M128 N256 K8 issue loop with operands resident in shared "
                           "memory; 16 independent FMA chains per thread"}

@@ -64,6 +64,8 @@ def _declare(lib):
     lib.tg_oracle_sum.restype = ctypes.c_int
     lib.tg_oracle_threads.argtypes = []
     lib.tg_oracle_threads.restype = ctypes.c_int
+    lib.tg_oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.tg_oracle_set_threads.restype = ctypes.c_int
     return lib
 
 
@@ -161,3 +163,8 @@ def reduce_sum(x: np.ndarray, lib=None) -> np.float32:
 def threads(lib=None) -> int:
     """OpenMP threads the oracle uses."""
     return int((lib or load()).tg_oracle_threads())
+
+
+def set_threads(n: int, lib=None) -> int:
+    """Use n OpenMP threads in later calls (timing only); returns the count."""
+    return int((lib or load()).tg_oracle_set_threads(int(n)))

@@ -204,6 +204,19 @@ int tg_oracle_sum(int64_t n, const float* x, float* result) {
     return 0;
 }
 
+/* Set the number of threads later calls use (n >= 1); returns the new count.
+ * Only the timing of the oracle changes: every output is still one thread's
+ * ascending-k sum. */
+int tg_oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 /* Number of threads the two entry points above use. */
 int tg_oracle_threads(void) {
 #ifdef _OPENMP

@@ -42,6 +42,7 @@ EXPORTS = (
     "tg_status_string",
     "tg_sgemm_version",
     "tg_probe_tf32_mma",
+    "tg_probe_f16_mma",
     "tg_probe_ffma",
     "tg_transpose",
     "tg_reduce_sum",
@@ -139,6 +140,8 @@ def lib():
         L.tg_sgemm_version.restype = i
         L.tg_probe_tf32_mma.argtypes = [i, i, vp, ctypes.POINTER(ctypes.c_double)]
         L.tg_probe_tf32_mma.restype = i
+        L.tg_probe_f16_mma.argtypes = [i, vp, ctypes.POINTER(ctypes.c_double)]
+        L.tg_probe_f16_mma.restype = i
         L.tg_probe_ffma.argtypes = [i, p, vp, ctypes.POINTER(ctypes.c_double)]
         L.tg_probe_ffma.restype = i
         L.tg_transpose.argtypes = [i, i, i, p, i, p, i, vp]
@@ -412,6 +415,16 @@ def probe_tf32_mma_tflops(iters=100000, use_collector=True) -> float:
         f = ctypes.c_double()
         _check(lib().tg_probe_tf32_mma(iters, int(use_collector), _stream_handle(stream), ctypes.byref(f)),
                "tg_probe_tf32_mma")
+        return f.value
+    return _time_probe(launch)
+
+
+def probe_f16_mma_tflops(iters=100000) -> float:
+    """Tensor TFLOP/s of the same issue pattern with kind::f16 MMAs (K=16),
+    for comparison only: no GEMM path uses fp16 operands."""
+    def launch(stream):
+        f = ctypes.c_double()
+        _check(lib().tg_probe_f16_mma(iters, _stream_handle(stream), ctypes.byref(f)), "tg_probe_f16_mma")
         return f.value
     return _time_probe(launch)
 

@@ -5,6 +5,9 @@
 //    tcgen05.mma.cta_group::1.kind::tf32 M=128, N=256, K=8 from operand tiles
 //    that stay in shared memory, three per 8-wide K slice and a commit every
 //    six -- the issue pattern of the 3xTF32 GEMM's main loop.
+//    The same kernel with kind::f16 (M=128, N=256, K=16: the same 32 bytes
+//    of each operand row per MMA, twice the products) measures the rate a
+//    split into fp16 halves would run at.
 //  * probe_ffma_kernel: 16 independent fp32 FMA chains per thread, 2048
 //    threads per SM.
 //
@@ -28,8 +31,9 @@ constexpr uint32_t kProbeB = kProbeN * 16 * 4;  // 256 rows x 64 bytes
 // large enough that one CTA occupies an SM
 constexpr size_t kProbeSmem = 160 * 1024;
 
-__global__ void __launch_bounds__(128, 1) probe_tf32_mma_kernel(int iters, int use_collector,
-                                                              uint64_t timeout_ns) {
+template <bool kF16>
+__global__ void __launch_bounds__(128, 1) probe_mma_kernel(int iters, int use_collector,
+                                                         uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t a0 = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (a0 & 1023u)) & 1023u);
@@ -55,12 +59,24 @@ __global__ void __launch_bounds__(128, 1) probe_tf32_mma_kernel(int iters, int u
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     if (threadIdx.x == 0) {
-        constexpr uint32_t idesc = idesc_tf32(kProbeM, kProbeN);
+        constexpr uint32_t idesc = kF16 ? idesc_f16(kProbeM, kProbeN) : idesc_tf32(kProbeM, kProbeN);
         const uint32_t sa = smem_addr(smem), sb = sa + kProbeA;
         // the MMA sequence inside the loop has no branch, as in the GEMM's
         // issue loop (a branch between MMAs costs the single issuing thread
         // about 10 % of the rate)
-        if (use_collector) {
+        if (kF16) {
+            for (int it = 0; it < iters; ++it) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const uint64_t da = smem_desc_kmajor(sa + ks * 32, 512, 4);
+                    const uint64_t db = smem_desc_kmajor(sb + ks * 32, 512, 4);
+                    mma_f16_ss(tmem, da, db, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_f16_ss(tmem, da, db, idesc, 1u);
+                    mma_f16_ss(tmem, da, db, idesc, 1u);
+                }
+                mma_commit(&bars[0]);
+            }
+        } else if (use_collector) {
             for (int it = 0; it < iters; ++it) {
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
@@ -135,12 +151,27 @@ extern "C" tg_status tg_probe_tf32_mma(int iters, int use_collector, cudaStream_
     if (!probe_device_ok()) return TG_ERR_UNSUPPORTED_DEVICE;
     const int sms = probe_sms();
     if (sms <= 0) return TG_ERR_CUDA;
-    if (cudaFuncSetAttribute(probe_tf32_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(probe_mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kProbeSmem) != cudaSuccess)
         return TG_ERR_CUDA;
-    probe_tf32_mma_kernel<<<sms, 128, kProbeSmem, stream>>>(iters, use_collector, 4000000000ull);
+    probe_mma_kernel<false><<<sms, 128, kProbeSmem, stream>>>(iters, use_collector, 4000000000ull);
     if (cudaGetLastError() != cudaSuccess) return TG_ERR_CUDA;
     *tensor_flop = 2.0 * kProbeM * kProbeN * kProbeK * 6.0 * iters * sms;
+    return TG_OK;
+}
+
+extern "C" tg_status tg_probe_f16_mma(int iters, cudaStream_t stream, double* tensor_flop) {
+    using namespace tg;
+    if (iters < 1 || tensor_flop == nullptr) return TG_ERR_INVALID_VALUE;
+    if (!probe_device_ok()) return TG_ERR_UNSUPPORTED_DEVICE;
+    const int sms = probe_sms();
+    if (sms <= 0) return TG_ERR_CUDA;
+    if (cudaFuncSetAttribute(probe_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kProbeSmem) != cudaSuccess)
+        return TG_ERR_CUDA;
+    probe_mma_kernel<true><<<sms, 128, kProbeSmem, stream>>>(iters, 0, 4000000000ull);
+    if (cudaGetLastError() != cudaSuccess) return TG_ERR_CUDA;
+    *tensor_flop = 2.0 * kProbeM * kProbeN * (2 * kProbeK) * 6.0 * iters * sms;
     return TG_OK;
 }
 

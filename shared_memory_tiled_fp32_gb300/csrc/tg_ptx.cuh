@@ -228,6 +228,18 @@ __device__ __forceinline__ void mma_tf32_ss_lastuse_a(uint32_t d_tmem, uint64_t 
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] x B[smem]^T, both operands K-major, kind::f16 (used
+// only by the instruction-rate probe).
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -299,6 +311,16 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4)                          // D format: f32
            | (2u << 7)                        // A format: tf32
            | (2u << 10)                       // B format: tf32
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with fp16 A and B, fp32
+// accumulator, both K-major, dense, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4)                          // D format: f32
+           | (0u << 7)                        // A format: f16
+           | (0u << 10)                       // B format: f16
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }

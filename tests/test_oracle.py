@@ -406,6 +406,24 @@ def test_bad_shapes_rejected(oracle_lib):
     assert lib.tg_oracle_sgemm_rows(1, rows.ctypes.data, 2, 2, 2, p, 2, p, 2, p, 2) == 1
 
 
+def test_thread_count_does_not_change_results(oracle_lib):
+    """Each output is one thread's ascending-k sum, so the result is the same
+    bits whatever the number of OpenMP threads (the single-thread timing in
+    the bench relies on this)."""
+    rng = np.random.default_rng(11)
+    A = rng.standard_normal((37, 300)).astype(np.float32)
+    B = rng.standard_normal((300, 29)).astype(np.float32)
+    n0 = oracle.threads(oracle_lib)
+    try:
+        many = oracle.sgemm(A, B, lib=oracle_lib)
+        assert oracle.set_threads(1, oracle_lib) == 1
+        one = oracle.sgemm(A, B, lib=oracle_lib)
+    finally:
+        oracle.set_threads(n0, oracle_lib)
+    assert oracle.threads(oracle_lib) == n0
+    assert np.array_equal(many.view(np.uint32), one.view(np.uint32))
+
+
 def test_normal_inputs_statistics(oracle_lib):
     """RNG wiring: for i.i.d. N(0,1) operands each C element has mean 0 and
     variance K."""
