@@ -169,10 +169,13 @@ size_t tg_sgemm_workspace_bytes(int M, int N, int K, const void* A, int lda, con
  * stream-ordered on `stream`, computes C = A x B there, copies C back and
  * synchronises `stream` before returning, so C is ready on return.  Also
  * returns TG_ERR_TIMEOUT if a kernel of this call gave up a wait.
- * Large products are pipelined: C is cut into row x column blocks (see
- * tg_sgemm_host_blocks), the first product starts once its A row block and
- * B column block are on the device, and the copies of the other blocks (in
- * on one copy stream, C out on another) overlap the products.  opts->split_k
+ * Large products are pipelined: C is cut into row blocks, the first of them
+ * also into column blocks (see tg_sgemm_host_blocks); the first product
+ * starts once its A row block and B column block are on the device, later
+ * row blocks are computed full width once all of B is in, and the copies of
+ * the other blocks (in on one copy stream, C out on another) overlap the
+ * products.  TG_HOST_TRACE=1 in the environment prints the call's timeline
+ * (copies, products) to stderr.  opts->split_k
  * and path apply to every block's product; workspace, main_begin and main_end
  * are ignored.  Below 2^33 multiply-adds (M*N*K) there is one block and C is
  * bit-identical to tg_sgemm's; above, each block's product is planned on its
@@ -181,16 +184,32 @@ size_t tg_sgemm_workspace_bytes(int M, int N, int K, const void* A, int lda, con
 tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                         float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts);
 
-/* The output blocks tg_sgemm_host would use (host arithmetic only): C is cut
- * into *row_blocks x *col_blocks blocks; row block 0 has *first_block_rows
- * rows (a short first block lets the first product start sooner), the others
- * *block_rows, columns *block_cols (the last ones ragged), chosen to minimise
- * a modelled pipeline time, returned in *model_ms (copies at the rates
- * measured on GB300).  path as in tg_sgemm_opts; num_sms = SMs planned for
- * (0 = the current device). */
-tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* row_blocks,
-                               int* col_blocks, int* first_block_rows, int* block_rows, int* block_cols,
-                               double* model_ms);
+/* The output blocks tg_sgemm_host uses for a shape (host arithmetic only).
+ * C is cut into row_blocks row blocks: row block 0 has first_block_rows rows
+ * (a short first block lets the first product start sooner), the next ones
+ * block_rows, the last one the remaining rows (possibly fewer).  Row blocks
+ * 0 .. split_row_blocks - 1 are cut into col_blocks column blocks of
+ * block_cols columns (the last ragged); the later row blocks are one
+ * full-width product each.  With defer_copies_out != 0 the copies of C out
+ * wait until every copy in is done (the host link then carries one direction
+ * at a time).  model_ms is the modelled time of the call (copy rates measured
+ * on GB300). */
+typedef struct {
+    int row_blocks;
+    int col_blocks;
+    int first_block_rows;
+    int block_rows;
+    int block_cols;
+    int split_row_blocks;
+    int defer_copies_out;
+    double model_ms;
+} tg_host_blocks_info;
+
+/* Fill *out with the blocks tg_sgemm_host would use, chosen to minimise the
+ * modelled time.  path as in tg_sgemm_opts; num_sms = SMs planned for (0 =
+ * the current device).  TG_ERR_INVALID_VALUE on negative sizes, an unknown
+ * path or out == NULL. */
+tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, tg_host_blocks_info* out);
 
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns TG_ERR_TIMEOUT if any kernel of this library on this device gave up

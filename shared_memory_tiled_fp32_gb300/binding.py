@@ -67,6 +67,15 @@ class Opts(ctypes.Structure):
     ]
 
 
+class HostBlocksInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("row_blocks", "col_blocks", "first_block_rows", "block_rows",
+                                             "block_cols", "split_row_blocks", "defer_copies_out")] + [
+        ("model_ms", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
 class PlanInfo(ctypes.Structure):
     _fields_ = [
         ("path", ctypes.c_int),
@@ -117,7 +126,7 @@ def lib():
         L.tg_sgemm_noalloc.argtypes = gemm
         L.tg_sgemm_noalloc.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
-        L.tg_sgemm_host_blocks.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ip, ctypes.POINTER(ctypes.c_double)]
+        L.tg_sgemm_host_blocks.argtypes = [i, i, i, i, i, ctypes.POINTER(HostBlocksInfo)]
         L.tg_sgemm_host_blocks.restype = i
         L.tg_sgemm_plan.argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
         L.tg_sgemm_plan.restype = i
@@ -343,14 +352,14 @@ def sgemm_host(A, B, out, *, path="auto", split_k=0, stream=None):
 
 
 def host_blocks(M, N, K, *, path="auto", num_sms=0) -> dict:
-    """The row x column output blocks sgemm_host pipelines (host arithmetic)."""
-    r = [ctypes.c_int() for _ in range(5)]
-    ms = ctypes.c_double()
+    """The output blocks sgemm_host pipelines (host arithmetic): row blocks
+    [0, split_row_blocks) are cut into col_blocks column blocks, the later ones
+    are full width; see include/tg_sgemm.h."""
+    info = HostBlocksInfo()
     st = lib().tg_sgemm_host_blocks(M, N, K, PATHS[path] if isinstance(path, str) else int(path), num_sms,
-                                    *[ctypes.byref(x) for x in r], ctypes.byref(ms))
+                                    ctypes.byref(info))
     _check(st, "tg_sgemm_host_blocks")
-    return {"row_blocks": r[0].value, "col_blocks": r[1].value, "first_block_rows": r[2].value,
-            "block_rows": r[3].value, "block_cols": r[4].value, "model_ms": ms.value}
+    return info.as_dict()
 
 
 def plan(M, N, K, lda=None, ldb=None, ldc=None, *, A=0, B=0, C=0, path="auto", split_k=0,

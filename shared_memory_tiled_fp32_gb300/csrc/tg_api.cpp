@@ -5,7 +5,11 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "tg_internal.h"
 
@@ -150,7 +154,7 @@ const char* tg_status_string(tg_status s) {
     return "unknown tg_status";
 }
 
-int tg_sgemm_version(void) { return 101; }
+int tg_sgemm_version(void) { return 102; }
 
 tg_status tg_sgemm_plan_general(int op_a, int op_b, int M, int N, int K, const void* A, int lda,
                                 const void* B, int ldb, const void* C, int ldc, int path,
@@ -227,6 +231,36 @@ tg_status tg_sgemm(int M, int N, int K, const float* A, int lda, const float* B,
     return tg_sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
 }
 
+namespace {
+
+// TG_HOST_TRACE=1: tg_sgemm_host records a timing event after each copy in,
+// around each product and after each copy out, and prints them (ms after the
+// call's start) to stderr once the call has synchronised.
+struct HostTrace {
+    bool on = false;
+    std::vector<std::pair<std::string, cudaEvent_t>> marks;
+    explicit HostTrace(bool enable) : on(enable) {}
+    void mark(const std::string& what, cudaStream_t s) {
+        if (!on) return;
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return;
+        cudaEventRecord(e, s);
+        marks.emplace_back(what, e);
+    }
+    void print() {
+        for (auto& m : marks) {
+            float ms = 0.0f;
+            if (on && cudaEventElapsedTime(&ms, marks.front().second, m.second) == cudaSuccess)
+                std::fprintf(stderr, "tg_host_trace %8.3f ms %s\n", ms, m.first.c_str());
+        }
+    }
+    ~HostTrace() {
+        for (auto& m : marks) cudaEventDestroy(m.second);
+    }
+};
+
+}  // namespace
+
 tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                         float* C, int ldc, cudaStream_t stream, const tg_sgemm_opts* opts) {
     const tg_sgemm_opts o = opts ? *opts : default_opts();
@@ -246,13 +280,24 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     const int path = o.path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3;
     const bool tf32 = path == TG_PATH_TF32X3;
     const long long k4 = ((long long)std::max(K, 1) + 3) / 4 * 4, n4 = ((long long)N + 3) / 4 * 4;
-    // Output blocks: C is cut into pm x pn blocks (A row blocks x B column
-    // blocks) so the first product needs only A_0 and B_0 on the device; the
-    // copies of later blocks (in on s_in, out on s_out) overlap the products
-    // of earlier ones.  A and B are split once, by the first product that
-    // reads each block, into shared hi/lo regions.
+    // Output blocks: C is cut into row blocks, the first ones also into
+    // column blocks, so the first product needs only A_0 and B_0 on the
+    // device; the copies of later blocks (in on s_in, out on s_out) overlap
+    // the products of earlier ones.  Row blocks past hb.split are computed
+    // full width once all of B is in.  A and B are split once, by the first
+    // product that reads each block, into shared hi/lo regions.
     const HostBlocks hb = choose_host_blocks(M, N, K, path, d->num_sms);
     const int pm = hb.pm, pn = hb.pn, nb = hb.nb, mb_max = std::max(hb.first, hb.mb);
+    // the (row offset, rows, column offset, columns) of block j of row block i
+    auto block_cols = [&](int i, int j, int* j0, int* Nj) {
+        if (hb.col_blocks(i) == 1) {
+            *j0 = 0;
+            *Nj = N;
+        } else {
+            *j0 = j * nb;
+            *Nj = std::min(nb, N - *j0);
+        }
+    };
 
     // device copies: 16-byte row pitches, so TMA reads them in place
     const size_t a_bytes = 4ull * M * k4, b_bytes = 4ull * (size_t)std::max(K, 1) * n4,
@@ -264,12 +309,14 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     const size_t a_split = tf32 ? align(8ull * ((mb_max + 255) / 256 * 256) * k16) : 0;
     // placeholder pointers with the alignment the real ones will have
     const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
-    size_t ws_max = 0;  // over the (at most 4) block shapes: whole or ragged rows x columns
+    size_t ws_max = 0;  // over the block shapes (whole or ragged rows x columns, or full width)
     for (int i : {0, std::min(1, pm - 1), pm - 1})
-        for (int j : {0, pn - 1}) {
+        for (int j : {0, hb.col_blocks(i) - 1}) {
+            int j0 = 0, Nj = 0;
+            block_cols(i, j, &j0, &Nj);
             Plan pl;
-            make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), std::min(nb, N - j * nb), K, 1.0f, al, (int)k4,
-                      al, (int)n4, 0.0f, al, (int)n4, path, o.split_k, d->num_sms, &pl, tf32, tf32);
+            make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), Nj, K, 1.0f, al, (int)k4, al, (int)n4, 0.0f, al,
+                      (int)n4, path, o.split_k, d->num_sms, &pl, tf32, tf32);
             ws_max = std::max(ws_max, pl.ws_bytes);
         }
     const size_t ws_total = b_split + a_split + ws_max;
@@ -295,6 +342,9 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     // events: [0] start, [1] end of the copies in, [2] end of the copies
     // out, [3 + i] A_i in, [11 + j] B_j in, [19 + i*pn + j] C_ij computed
     cudaEvent_t* ev = hp->ev;
+    const char* trace_env = std::getenv("TG_HOST_TRACE");
+    HostTrace trace(trace_env != nullptr && trace_env[0] == '1');
+    trace.mark("start", stream);
     bool ok = cudaEventRecord(ev[0], stream) == cudaSuccess &&
               cudaStreamWaitEvent(hp->s_in, ev[0], 0) == cudaSuccess &&
               cudaStreamWaitEvent(hp->s_out, ev[0], 0) == cudaSuccess;
@@ -304,6 +354,7 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
              cudaMemcpy2DAsync(fA + (size_t)i0 * k4, 4ull * k4, A + (size_t)i0 * lda, 4ull * lda, 4ull * K, Mi,
                                cudaMemcpyHostToDevice, hp->s_in) == cudaSuccess &&
              cudaEventRecord(ev[3 + i], hp->s_in) == cudaSuccess;
+        trace.mark("in A" + std::to_string(i) + " rows " + std::to_string(Mi), hp->s_in);
     };
     auto copy_b = [&](int j) {
         const int j0 = j * nb, Nj = std::min(nb, N - j0);
@@ -311,18 +362,27 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
              cudaMemcpy2DAsync(fB + j0, 4ull * n4, B + j0, 4ull * ldb, 4ull * Nj, K, cudaMemcpyHostToDevice,
                                hp->s_in) == cudaSuccess &&
              cudaEventRecord(ev[11 + j], hp->s_in) == cudaSuccess;
+        trace.mark("in B" + std::to_string(j) + " cols " + std::to_string(Nj), hp->s_in);
     };
     if (K > 0) {  // in the order the products first need them
         copy_a(0);
         for (int j = 0; j < pn; ++j) copy_b(j);
         for (int i = 1; i < pm; ++i) copy_a(i);
     }
+    if (hb.defer_out)  // the copies out start once the copies in are done
+        ok = ok && cudaEventRecord(ev[1], hp->s_in) == cudaSuccess &&
+             cudaStreamWaitEvent(hp->s_out, ev[1], 0) == cudaSuccess;
     st = ok ? TG_OK : TG_ERR_CUDA;
     for (int i = 0; st == TG_OK && i < pm; ++i) {
-        for (int j = 0; st == TG_OK && j < pn; ++j) {
-            const int i0 = hb.row0(i), Mi = hb.rows(i, M), j0 = j * nb, Nj = std::min(nb, N - j0);
+        const int nc = hb.col_blocks(i);
+        for (int j = 0; st == TG_OK && j < nc; ++j) {
+            const int i0 = hb.row0(i), Mi = hb.rows(i, M);
+            int j0 = 0, Nj = 0;
+            block_cols(i, j, &j0, &Nj);
+            // B_j's copy for the first row block; all of B for a full-width one
+            const int b_event = nc == 1 ? 11 + pn - 1 : 11 + j;
             if (K > 0 && ((j == 0 && cudaStreamWaitEvent(stream, ev[3 + i], 0) != cudaSuccess) ||
-                          (i == 0 && cudaStreamWaitEvent(stream, ev[11 + j], 0) != cudaSuccess))) {
+                          ((i == 0 || nc == 1) && cudaStreamWaitEvent(stream, ev[b_event], 0) != cudaSuccess))) {
                 st = TG_ERR_CUDA;
                 break;
             }
@@ -338,13 +398,18 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
                 pl.ext_b = b_cat + (size_t)j0 * 2 * k16;
                 pl.b_ready = i > 0;
             }
+            const std::string blk = std::to_string(i) + "," + std::to_string(j) + " (" + std::to_string(Mi) +
+                                    " x " + std::to_string(Nj) + ")";
+            trace.mark("product " + blk + " begins", stream);
             st = launch_plan(pl, Ai, Bj, Cij, wplan, stream, nullptr, nullptr);
             if (st != TG_OK) break;
+            trace.mark("product " + blk + " ends", stream);
             cudaEvent_t done = ev[19 + i * pn + j];
             if (cudaEventRecord(done, stream) != cudaSuccess || cudaStreamWaitEvent(hp->s_out, done, 0) != cudaSuccess ||
                 cudaMemcpy2DAsync(C + (size_t)i0 * ldc + j0, 4ull * ldc, Cij, 4ull * n4, 4ull * Nj, Mi,
                                   cudaMemcpyDeviceToHost, hp->s_out) != cudaSuccess)
                 st = TG_ERR_CUDA;
+            trace.mark("out " + blk, hp->s_out);
         }
     }
     // the buffers are released on `stream` once both copy streams are done
@@ -356,18 +421,16 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
         if (q) cudaFreeAsync(q, stream);
     if (cudaStreamSynchronize(stream) != cudaSuccess) return TG_ERR_CUDA;
     if (st != TG_OK) return st;
+    trace.print();
     unsigned int word = 0;
     st = read_error_word(stream, true, &word);
     if (st != TG_OK) return st;
     return word != 0 ? TG_ERR_TIMEOUT : TG_OK;
 }
 
-tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* row_blocks, int* col_blocks,
-                               int* first_block_rows, int* block_rows, int* block_cols, double* model_ms) {
+tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, tg_host_blocks_info* out) {
     using namespace tg;
-    if (M < 0 || N < 0 || K < 0 || row_blocks == nullptr || col_blocks == nullptr || first_block_rows == nullptr ||
-        block_rows == nullptr || block_cols == nullptr)
-        return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || out == nullptr) return TG_ERR_INVALID_VALUE;
     if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3) return TG_ERR_INVALID_VALUE;
     if (num_sms <= 0) {
         DeviceState* d = nullptr;
@@ -376,12 +439,14 @@ tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, int* 
         num_sms = d->num_sms;
     }
     const HostBlocks hb = choose_host_blocks(M, N, K, path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3, num_sms);
-    *row_blocks = hb.pm;
-    *col_blocks = hb.pn;
-    *first_block_rows = hb.first;
-    *block_rows = hb.mb;
-    *block_cols = hb.nb;
-    if (model_ms != nullptr) *model_ms = hb.model_ms;
+    out->row_blocks = hb.pm;
+    out->col_blocks = hb.pn;
+    out->first_block_rows = hb.first;
+    out->block_rows = hb.mb;
+    out->block_cols = hb.nb;
+    out->split_row_blocks = hb.split;
+    out->defer_copies_out = hb.defer_out ? 1 : 0;
+    out->model_ms = hb.model_ms;
     return TG_OK;
 }
 

@@ -122,14 +122,22 @@ tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int l
 // ragged), column blocks nb columns (a multiple of 256, the last ragged).
 // The choice minimises a modelled pipeline time (copies in, products, copies
 // out).  Host arithmetic only.
+// Output blocks of the host-buffer pipeline: pm row blocks (the first of
+// `first` rows, the others of `mb`, the last one the remainder); row blocks
+// [0, split) are cut into pn column blocks of nb columns (the last ragged),
+// the later ones are computed full width (all of B is on the device by then).
+// With defer_out the copies of C out wait until every copy in is done (the
+// two directions then do not share the host link).
 struct HostBlocks {
-    int pm = 1, pn = 1, first = 0, mb = 0, nb = 0;
+    int pm = 1, pn = 1, first = 0, mb = 0, nb = 0, split = 1;
+    bool defer_out = false;
     double model_ms = 0.0;
     int row0(int i) const { return i == 0 ? 0 : first + (i - 1) * mb; }
     int rows(int i, int M) const {
         const int r = M - row0(i), cap = i == 0 ? first : mb;
         return r < cap ? r : cap;
     }
+    int col_blocks(int i) const { return i < split ? pn : 1; }
 };
 HostBlocks choose_host_blocks(int M, int N, int K, int path, int num_sms);
 

@@ -11,6 +11,7 @@
 // Block 크기", taken at its extreme: few warps, each with much work).
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -282,19 +283,120 @@ double product_seconds(const Plan& p, double rate) {
     return rounds * unit_flops / (rate / std::max(1, p.num_sms / p.pair)) + 25e-6;
 }
 
-// Host-buffer pipeline model.  Copies in run on one copy stream in the order
-// the products first need them (A_0, B_0, B_1, ..., A_1, ...), the products
-// run in row-block-major order (i, j) on the compute stream, and each C block
-// is copied out on a second copy stream once its product is done.  Rates are
-// the ones measured on GB300: pinned host memory over NVLink-C2C about 200
-// GB/s in and 190 GB/s out, the split pre-pass about 5.7 TB/s, and a full
-// round of work units 355 (3xTF32) or 62 (FFMA) useful TFLOP/s.
+// Host-buffer pipeline model: a small event simulation of one call.  Copies
+// in run on one copy stream in the order the products first need them (A_0,
+// B_0, B_1, ..., A_1, ...); the products run in row-block-major order on the
+// compute stream, each once its A row block and B column block (all of B for
+// a full-width one) are in; each C block is copied out on a second copy
+// stream once its product is done (with defer_out, not before the last copy
+// in).  Rates measured on GB300 over NVLink-C2C with pinned host memory:
+// 205 GB/s in alone, 190 GB/s out alone, about 170 GB/s each way while both
+// directions are busy, plus ~40 us per copy out; the split pre-pass about
+// 5.7 TB/s; a full round of work units 355 (3xTF32) or 62 (FFMA) useful
+// TFLOP/s.  Fitted to the measured 8192^3 layouts within ~2 %.
+namespace {
+
+struct HostCopy {
+    double bytes;
+    int a_block, b_block;  // which block it brings in (-1: none)
+};
+struct HostProduct {
+    int a_block, b_block;  // inputs it waits for
+    double seconds, out_bytes;
+};
+
+double simulate_host_pipeline(const std::vector<HostCopy>& ins, const std::vector<HostProduct>& prods, int pm,
+                              int pn, bool defer_out) {
+    const double r_in = 205e9, r_out = 190e9, r_both = 170e9;
+    std::vector<char> a_in(pm, 0), b_in(pn, 0);
+    size_t ik = 0, pk = 0, oh = 0;
+    double t = 0.0, in_rem = ins.empty() ? 0.0 : ins[0].bytes, gpu_end = -1.0, out_rem = -1.0;
+    std::vector<double> outq;
+    for (int iter = 0; iter < 100000; ++iter) {
+        if (gpu_end < 0.0 && pk < prods.size() && a_in[prods[pk].a_block] && b_in[prods[pk].b_block])
+            gpu_end = t + prods[pk].seconds;
+        if (out_rem < 0.0 && oh < outq.size() && (!defer_out || ik >= ins.size())) out_rem = outq[oh++];
+        const bool in_busy = ik < ins.size(), out_busy = out_rem >= 0.0;
+        if (!in_busy && !out_busy && gpu_end < 0.0) return pk == prods.size() ? t : 1e30;
+        const double ri = in_busy ? (out_busy ? r_both : r_in) : 0.0;
+        const double ro = out_busy ? (in_busy ? r_both : r_out) : 0.0;
+        double dt = 1e30;
+        if (in_busy) dt = std::min(dt, in_rem / ri);
+        if (out_busy) dt = std::min(dt, out_rem / ro);
+        if (gpu_end >= 0.0) dt = std::min(dt, gpu_end - t);
+        dt = std::max(dt, 0.0);
+        t += dt;
+        if (in_busy) {
+            in_rem -= ri * dt;
+            if (in_rem <= 1.0) {
+                if (ins[ik].a_block >= 0) a_in[ins[ik].a_block] = 1;
+                if (ins[ik].b_block >= 0) b_in[ins[ik].b_block] = 1;
+                if (++ik < ins.size()) in_rem = ins[ik].bytes;
+            }
+        }
+        if (out_busy) {
+            out_rem -= ro * dt;
+            if (out_rem <= 1.0) out_rem = -1.0;
+        }
+        if (gpu_end >= 0.0 && gpu_end <= t + 1e-12) {
+            outq.push_back(prods[pk++].out_bytes);
+            gpu_end = -1.0;
+        }
+    }
+    return 1e30;
+}
+
+}  // namespace
+
+// Modelled time of host calls of one shape, for any blocks.
+class HostModel {
+  public:
+    HostModel(int M, int N, int K, int path, int num_sms)
+        : M_(M), N_(N), K_(K), path_(path), sms_(num_sms), tf32_(path != TG_PATH_FFMA) {}
+
+    double ms(const HostBlocks& hb) {
+        const double bw_split = 5.7e12, out_fixed_bytes = 40e-6 * 190e9;
+        ins_.clear();
+        prods_.clear();
+        ins_.push_back({4.0 * hb.rows(0, M_) * K_, 0, -1});
+        for (int j = 0; j < hb.pn; ++j) ins_.push_back({4.0 * std::min(hb.nb, N_ - j * hb.nb) * K_, -1, j});
+        for (int i = 1; i < hb.pm; ++i) ins_.push_back({4.0 * hb.rows(i, M_) * K_, i, -1});
+        for (int i = 0; i < hb.pm; ++i) {
+            const int rows = hb.rows(i, M_), nc = hb.col_blocks(i);
+            for (int j = 0; j < nc; ++j) {
+                const int cols = nc == 1 ? N_ : std::min(hb.nb, N_ - j * hb.nb);
+                double sec = product(rows, cols);
+                if (tf32_) {
+                    if (j == 0) sec += 12.0 * rows * K_ / bw_split;
+                    if (i == 0) sec += 12.0 * cols * K_ / bw_split;
+                }
+                prods_.push_back({i, nc == 1 ? hb.pn - 1 : j, sec, 4.0 * rows * cols + out_fixed_bytes});
+            }
+        }
+        return simulate_host_pipeline(ins_, prods_, hb.pm, hb.pn, hb.defer_out) * 1e3;
+    }
+
+  private:
+    double product(int rows, int cols) {
+        auto it = product_s_.find({rows, cols});
+        if (it != product_s_.end()) return it->second;
+        const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
+        const int k4 = (int)round_up((size_t)std::max(K_, 1), 4), n4 = (int)round_up((size_t)std::max(N_, 1), 4);
+        Plan pl;
+        make_plan(TG_OP_N, TG_OP_N, rows, cols, K_, 1.0f, al, k4, al, n4, 0.0f, al, n4, path_, 0, sms_, &pl,
+                  tf32_, tf32_);
+        const double t = product_seconds(pl, tf32_ ? 355e12 : 62e12);
+        product_s_[{rows, cols}] = t;
+        return t;
+    }
+    int M_, N_, K_, path_, sms_;
+    bool tf32_;
+    std::map<std::pair<int, int>, double> product_s_;  // by (rows, columns)
+    std::vector<HostCopy> ins_;
+    std::vector<HostProduct> prods_;
+};
+
 HostBlocks model_host_blocks(int M, int N, int K, int path, int num_sms) {
-    const bool tf32 = path != TG_PATH_FFMA;
-    const double bw_in = 200e9, bw_out = 190e9, bw_split = 5.7e12;
-    const double rate = tf32 ? 355e12 : 62e12;
-    const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
-    const int k4 = (int)round_up((size_t)std::max(K, 1), 4), n4 = (int)round_up((size_t)std::max(N, 1), 4);
     HostBlocks best;
     best.mb = best.first = (int)round_up((size_t)std::max(M, 1), 128);
     best.nb = (int)round_up((size_t)std::max(N, 1), 256);
@@ -303,80 +405,78 @@ HostBlocks model_host_blocks(int M, int N, int K, int path, int num_sms) {
     // below 2^33 multiply-adds one block: the launches would cost more than
     // the copies they hide, and the result is then bit-identical to tg_sgemm's
     const int max_blocks = (double)M * N * K >= 8589934592.0 ? 8 : 1;
-    auto evaluate = [&](int pm, int first, int mb, int pn, int nb) {
-        auto row0 = [&](int i) { return i == 0 ? 0 : first + (i - 1) * mb; };
-        auto rows_of = [&](int i) { return std::min(i == 0 ? first : mb, M - row0(i)); };
-        // copies in, in the order the products first need them
-        std::vector<double> a_ready(pm), b_ready(pn);
-        double t_in = 0.0;
-        auto copy_a = [&](int i) {
-            t_in += 4.0 * rows_of(i) * K / bw_in;
-            a_ready[i] = t_in;
-        };
-        auto copy_b = [&](int j) {
-            t_in += 4.0 * std::min(nb, N - j * nb) * K / bw_in;
-            b_ready[j] = t_in;
-        };
-        copy_a(0);
-        for (int j = 0; j < pn; ++j) copy_b(j);
-        for (int i = 1; i < pm; ++i) copy_a(i);
-        // products and copies out; the blocks have at most 6 shapes (first,
-        // whole or ragged rows x whole or ragged columns)
-        double shape_s[3][2] = {{-1.0, -1.0}, {-1.0, -1.0}, {-1.0, -1.0}};
-        double t_gpu = 0.0, t_out = 0.0;
-        for (int i = 0; i < pm; ++i) {
-            for (int j = 0; j < pn; ++j) {
-                const int rows = rows_of(i), cols = std::min(nb, N - j * nb);
-                double t = std::max({t_gpu, a_ready[i], b_ready[j]});
-                if (tf32) {
-                    if (j == 0) t += 12.0 * rows * K / bw_split;
-                    if (i == 0) t += 12.0 * cols * K / bw_split;
-                }
-                double& ps = shape_s[i == 0 ? 0 : (i == pm - 1 ? 2 : 1)][j == pn - 1];
-                if (ps < 0.0) {
-                    Plan pl;
-                    make_plan(TG_OP_N, TG_OP_N, rows, cols, K, 1.0f, al, k4, al, n4, 0.0f, al, n4, path, 0,
-                              num_sms, &pl, tf32, tf32);
-                    ps = product_seconds(pl, rate);
-                }
-                t += ps;
-                t_gpu = t;
-                t_out = std::max(t_out, t) + 4.0 * rows * cols / bw_out;
-            }
-        }
-        const double ms = t_out * 1e3;
-        if (best.model_ms < 0.0 || ms < best.model_ms * 0.98) {  // prefer earlier (fewer) blocks on near ties
-            best.pm = pm;
-            best.pn = pn;
-            best.first = first;
-            best.mb = mb;
-            best.nb = nb;
-            best.model_ms = ms;
+    HostModel model(M, N, K, path, num_sms);
+    auto evaluate = [&](int pm, int first, int mb, int pn, int nb, int split) {
+        HostBlocks hb;
+        hb.pm = pm;
+        hb.pn = pn;
+        hb.first = first;
+        hb.mb = mb;
+        hb.nb = nb;
+        hb.split = split;
+        for (int defer = 0; defer < 2; ++defer) {
+            hb.defer_out = defer != 0;
+            hb.model_ms = model.ms(hb);
+            // candidates come simplest first; a later one must win by 0.5 %
+            if (best.model_ms < 0.0 || hb.model_ms < best.model_ms * 0.995) best = hb;
         }
     };
-    for (int pm = 1; pm <= max_blocks; ++pm) {
-        for (int pn = 1; pn <= max_blocks; ++pn) {
-            const int nb = (int)round_up((size_t)cdiv(N, pn), 256);
-            if (cdiv(N, nb) != pn || (pn > 1 && nb < 512)) continue;
-            // equal row blocks
+    // B column blocks are strided copies; on GB300 rows of a multiple of 4 KiB
+    // copied at the full rate (8 KiB: 185-208 GB/s) while 6 KiB rows ran at
+    // 140-200 and 2 KiB rows at 117, so wide B keeps to 1024-column blocks
+    const int nb_align = N >= 4096 ? 1024 : 256;
+    for (int pn = 1; pn <= max_blocks; ++pn) {
+        const int nb = (int)round_up((size_t)cdiv(N, pn), nb_align);
+        if (cdiv(N, nb) != pn || (pn > 1 && nb < 512)) continue;
+        // equal row blocks, every row block cut into the column blocks
+        for (int pm = 1; pm <= max_blocks; ++pm) {
             const int mb = (int)round_up((size_t)cdiv(M, pm), 128);
-            if (cdiv(M, mb) == pm && (pm == 1 || mb >= 512)) evaluate(pm, mb, mb, pn, nb);
-            // a short first row block (the first product starts sooner), the
-            // rest of the rows in pm - 1 equal blocks
-            for (int first = 256; pm > 1 && first <= 2048; first *= 2) {
-                if (first >= M) break;
-                const int rest = (int)round_up((size_t)cdiv(M - first, pm - 1), 128);
-                if (rest <= first || rest < 512 || cdiv(M - first, rest) != pm - 1) continue;
-                evaluate(pm, first, rest, pn, nb);
+            if (cdiv(M, mb) == pm && (pm == 1 || mb >= 512)) evaluate(pm, mb, mb, pn, nb, pm);
+        }
+        if (max_blocks == 1) continue;
+        // a first row block of `first` rows (the first product starts once it
+        // and B_0 are in), then blocks of mb rows and a shorter remainder;
+        // only the first row block cut into column blocks, or all of them
+        for (int first = 256; first < M && first <= 4096; first += 256) {
+            const int lo = std::max(512, (int)round_up((size_t)cdiv(M - first, max_blocks - 1), 256));
+            for (int mb = lo; mb <= lo + 4096 && mb < M; mb += 256) {
+                const int pm = 1 + cdiv(M - first, mb);
+                if (pm > max_blocks) continue;
+                evaluate(pm, first, mb, pn, nb, 1);
+                if (pn > 1) evaluate(pm, first, mb, pn, nb, pm);
             }
         }
     }
     return best;
 }
 
-// The model's answer is remembered per shape (a few hundred plans are
+// TG_HOST_BLOCKS="first,mb,nb,split[,defer_out]" fixes the blocks (for tests
+// of each layout); ignored unless it describes at most 8 x 8 valid blocks of C.
+bool host_blocks_override(int M, int N, HostBlocks* hb) {
+    const char* e = std::getenv("TG_HOST_BLOCKS");
+    int first = 0, mb = 0, nb = 0, split = 0, defer = 0;
+    if (e == nullptr || std::sscanf(e, "%d,%d,%d,%d,%d", &first, &mb, &nb, &split, &defer) < 4) return false;
+    if (M <= 0 || N <= 0 || first <= 0 || mb <= 0 || nb <= 0 || first % 128 || mb % 128 || nb % 256) return false;
+    const int pm = first >= M ? 1 : 1 + cdiv(M - first, mb), pn = cdiv(N, nb);
+    if (pm > 8 || pn > 8 || split < 1 || split > pm) return false;
+    hb->pm = pm;
+    hb->pn = pn;
+    hb->first = first;
+    hb->mb = mb;
+    hb->nb = nb;
+    hb->split = split;
+    hb->defer_out = defer != 0;
+    return true;
+}
+
+// The model's answer is remembered per shape (a few thousand layouts are
 // evaluated on first use; later calls with the same shape only look it up).
 HostBlocks choose_host_blocks(int M, int N, int K, int path, int num_sms) {
+    HostBlocks fixed;
+    if (host_blocks_override(M, N, &fixed)) {
+        fixed.model_ms = HostModel(M, N, K, path, num_sms).ms(fixed);
+        return fixed;
+    }
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, int>, HostBlocks> memo;
     const auto key = std::make_tuple(M, N, K, path, num_sms);

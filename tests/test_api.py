@@ -32,7 +32,7 @@ def test_library_exports_header_symbols():
 
 
 def test_version_and_status_strings():
-    assert tg.lib().tg_sgemm_version() == 101
+    assert tg.lib().tg_sgemm_version() == 102
     for code, name in tg.STATUS.items():
         assert tg.status_string(code).startswith(name)
 
@@ -293,12 +293,15 @@ def test_general_plan_packs_transposed_operands():
                                         (5000, 300, 0, "tf32x3")])
 def test_host_blocks_cover_c(M, N, K, path):
     """The host entry's output blocks: rows in multiples of 128, columns in
-    multiples of 256, exactly covering C (the last ones ragged), at most 8 x 8."""
+    multiples of 256, exactly covering C (the last ones ragged), at most 8 row
+    blocks, the first split_row_blocks of them cut into at most 8 column
+    blocks."""
     h = tg.host_blocks(M, N, K, path=path, num_sms=152)
     pm, pn, f, mb, nb = h["row_blocks"], h["col_blocks"], h["first_block_rows"], h["block_rows"], h["block_cols"]
-    assert 1 <= pm <= 8 and 1 <= pn <= 8
-    assert f % 128 == 0 and mb % 128 == 0 and nb % 256 == 0 and f <= mb
-    # row blocks: [0, f), then pm - 1 blocks of mb rows, the last ragged
+    split = h["split_row_blocks"]
+    assert 1 <= pm <= 8 and 1 <= pn <= 8 and 1 <= split <= pm
+    assert f % 128 == 0 and mb % 128 == 0 and nb % 256 == 0
+    # row blocks: [0, f), then blocks of mb rows, the last one the remainder
     assert (pm == 1 and f >= M) or (pm > 1 and f < M and -(-(M - f) // mb) == pm - 1)
     assert -(-N // nb) == pn
     assert h["model_ms"] >= 0
@@ -308,14 +311,42 @@ def test_host_blocks_cover_c(M, N, K, path):
         assert nb >= 512
 
 
+def test_host_blocks_override(monkeypatch):
+    """TG_HOST_BLOCKS fixes the layout when it describes valid blocks of C and
+    is ignored otherwise."""
+    model = tg.host_blocks(4100, 3000, 1500, path="tf32x3", num_sms=152)
+    monkeypatch.setenv("TG_HOST_BLOCKS", "1024,1024,1536,4")
+    h = tg.host_blocks(4100, 3000, 1500, path="tf32x3", num_sms=152)
+    assert (h["row_blocks"], h["col_blocks"], h["first_block_rows"], h["block_rows"], h["block_cols"],
+            h["split_row_blocks"], h["defer_copies_out"]) == (5, 2, 1024, 1024, 1536, 4, 0)
+    assert h["model_ms"] > 0
+    monkeypatch.setenv("TG_HOST_BLOCKS", "1024,1024,1536,4,1")
+    assert tg.host_blocks(4100, 3000, 1500, path="tf32x3", num_sms=152)["defer_copies_out"] == 1
+    for bad in ("1000,1024,1536,1", "1024,1024,1500,1", "1024,1024,1536,6", "128,128,256,1", "x"):
+        monkeypatch.setenv("TG_HOST_BLOCKS", bad)
+        assert tg.host_blocks(4100, 3000, 1500, path="tf32x3", num_sms=152) == model
+
+
+def test_host_blocks_full_width_later_rows():
+    """For 8192^3 the model cuts only the first row block into column blocks
+    (the first product starts early) and computes the later row blocks full
+    width, ending with a short row block (little work after the last copy in)."""
+    h = tg.host_blocks(8192, 8192, 8192, path="tf32x3", num_sms=152)
+    assert h["split_row_blocks"] == 1 and h["col_blocks"] > 1
+    last = 8192 - h["first_block_rows"] - (h["row_blocks"] - 2) * h["block_rows"]
+    assert 0 < last <= h["block_rows"]
+
+
 def test_host_blocks_pipeline_large_products():
     """A large product is cut so that the first block's operands are a small
     part of A and B, and the modelled time beats a single block."""
     h = tg.host_blocks(8192, 8192, 8192, path="tf32x3", num_sms=152)
     assert h["row_blocks"] * h["col_blocks"] >= 4
-    assert 4 * 8192 * (h["block_rows"] + h["block_cols"]) <= 0.5 * 4 * 8192 * 16384
-    assert tg.lib().tg_sgemm_host_blocks(-1, 4, 4, 0, 152, *[ctypes.byref(ctypes.c_int()) for _ in range(5)],
-                                         None) == 1
+    assert 4 * 8192 * (h["first_block_rows"] + h["block_cols"]) <= 0.5 * 4 * 8192 * 16384
+    info = tg.binding.HostBlocksInfo()
+    assert tg.lib().tg_sgemm_host_blocks(-1, 4, 4, 0, 152, ctypes.byref(info)) == 1
+    assert tg.lib().tg_sgemm_host_blocks(4, 4, 4, 0, 152, None) == 1
+    assert tg.lib().tg_sgemm_host_blocks(4, 4, 4, 7, 152, ctypes.byref(info)) == 1
     # below 2^33 multiply-adds: one block (bit-identical to the device entry)
     small = tg.host_blocks(777, 1029, 513, path="tf32x3", num_sms=152)
     assert (small["row_blocks"], small["col_blocks"]) == (1, 1)

@@ -207,15 +207,24 @@ def test_host_buffer_entry_row_blocks(tg, path):
     assert np.all(np.isnan(Cbig.numpy()[:, N:])), "host entry wrote past column N"
 
 
+@pytest.mark.parametrize("layout", [None, "1024,1024,1536,4", "512,1536,1024,2"])
 @pytest.mark.parametrize("path", ["tf32x3", "ffma"])
-def test_host_buffer_entry_2d_blocks(tg, path):
-    """The host entry point with C cut into row x column blocks (ragged last
-    ones): every block's product waits for its own A row block and B column
-    block, A and B are split once and reused, C blocks are copied out as they
-    finish.  Sampled rows at and around every row-block edge, all columns."""
+def test_host_buffer_entry_2d_blocks(tg, path, layout, monkeypatch):
+    """The host entry point with C cut into row blocks, the first ones also
+    into column blocks (ragged last ones), the later ones full width: every
+    product waits for its own A row block and B column block (all of B when
+    full width), A and B are split once and reused, C blocks are copied out
+    as they finish.  The model's layout, every row block cut, and two of four
+    cut.  Sampled rows at and around every row-block edge, all columns."""
+    if layout is not None:
+        monkeypatch.setenv("TG_HOST_BLOCKS", layout)
     M, N, K = 4100, 3000, 1500
     hb = tg.host_blocks(M, N, K, path=path)
-    assert hb["row_blocks"] > 1 and hb["col_blocks"] > 1
+    assert hb["row_blocks"] > 1
+    if layout is not None:
+        assert hb["col_blocks"] > 1
+        assert ",".join(str(hb[k]) for k in ("first_block_rows", "block_rows", "block_cols",
+                                               "split_row_blocks")) == layout
     A, B = make_inputs(M, N, K, "uniform", 322)
     Ap, Bp = A.pin_memory(), B.pin_memory()
     Cbig = torch.full((M, N + 3), float("nan")).pin_memory()
