@@ -493,7 +493,11 @@ constexpr long long kTileFloats = kTfAStage / 4;        // one 128-row tile: 409
 constexpr uint32_t kDescSwizzle128 = 2;
 static_assert(kTfRowBytes == 128, "one K block of hi and lo must fill one 128-byte swizzle row");
 constexpr int kTfBars = 2 * kTf32Stages + 5;
-constexpr size_t kTfSmemBytes = 1024 + (size_t)kTf32Stages * kTfStageBytes + kTfBars * 8 + 16;
+static_assert(kTfBars * 8 + 16 <= 128, "barriers and the tensor-memory slot fit in 128 bytes");
+// one 32 x 32 fp32 staging block per epilogue warp for the coalesced C store
+constexpr uint32_t kTfOutStageBytes = 8 * 32 * 32 * 4;
+constexpr size_t kTfSmemBytes = 1024 + (size_t)kTf32Stages * kTfStageBytes + 128 + kTfOutStageBytes;
+static_assert(kTfSmemBytes <= 232448, "fits the 227 KiB of shared memory a block may opt in to");
 
 template <int kPair>
 __global__ void __launch_bounds__(kTfThreads, 1)
@@ -507,6 +511,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     uint64_t* tempty = tfull + 2;  // [2] chunk drained by the epilogue
     uint64_t* drain = tempty + 2;  // every MMA of this CTA completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    float* out_stage = reinterpret_cast<float*>(smem + ST * kTfStageBytes + 128);  // [8 warps][32 x 32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WaitCtl wc{&g_error_word, args.timeout_ns};
@@ -647,7 +652,6 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         const int e = warp - 4;
         const int q = warp & 3;        // tensor-memory lanes 32q..32q+31 = tile rows
         const int h = e >> 2;          // tile columns 128h..128h+127
-        const bool vec = args.vec_out != 0;
         uint32_t chunk = 0;
         bool ok = true;
         Unit t;
@@ -678,23 +682,43 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                 if (lane == 0) mbar_arrive(&tempty[buf]);  // chunk buffer may be refilled
             }
             if (!ok) break;
-            // guarded store of this thread's row segment (row-contiguous 512 B)
-            const int grow = t.m0 + q * 32 + lane;
-            if (grow < args.M) {
-                float* row = t.out + (long long)grow * t.ldo;
-                const int col0 = t.n0 + h * 128;
-                if (args.scaled != 0 && t.direct) {
+            // Guarded store of the warp's 32 rows x 128 columns, coalesced: each
+            // 32 x 32 block goes through the warp's shared-memory buffer (lane
+            // = row on the way in, lane = column on the way out) and leaves one
+            // row per instruction, 128 contiguous bytes.  Storing each thread's
+            // row directly sent 32 separate 16-byte pieces per instruction, and
+            // the burst of requests at every unit's end held up the next unit's
+            // operand copies (measured: 2-6 % of the kernel, more for short K).
+            // The 4-value group g of row r sits at r*32 + 4*(g ^ (r & 7)): the
+            // 16-byte writes of 8 lanes (one row each) and the 4-byte reads of
+            // a warp (one column each) both touch 32 different banks.
+            float* stg = out_stage + e * 1024;
+            const bool scaled = args.scaled != 0 && t.direct;
+            const int row0 = t.m0 + q * 32;
+            float4* stg_row = reinterpret_cast<float4*>(stg + lane * 32);
+            const int rsw = lane & 7;
+            const int rows = min(32, args.M - row0);
 #pragma unroll
-                    for (int v = 0; v < 32; ++v)
-                        store_row4_scaled(row, col0 + 4 * v, args.N,
-                                          make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]),
-                                          vec, args.alpha, args.beta);
-                } else {
+            for (int cb = 0; cb < 4; ++cb) {
 #pragma unroll
-                    for (int v = 0; v < 32; ++v)
-                        store_row4(row, col0 + 4 * v, args.N,
-                                   make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]), vec);
+                for (int g = 0; g < 8; ++g)
+                    stg_row[g ^ rsw] = make_float4(acc[cb * 32 + 4 * g], acc[cb * 32 + 4 * g + 1],
+                                                   acc[cb * 32 + 4 * g + 2], acc[cb * 32 + 4 * g + 3]);
+                __syncwarp();
+                const int col = t.n0 + h * 128 + cb * 32 + lane;
+                if (col < args.N) {
+                    // (r, lane) sits at r*32 + (lane ^ 4*(r & 7))
+                    float* dst = t.out + (long long)row0 * t.ldo + col;
+#pragma unroll 1
+                    for (int r = 0; r < rows; ++r, dst += t.ldo) {
+                        const float v = stg[r * 32 + (lane ^ ((r & 7) << 2))];
+                        if (scaled)
+                            *dst = args.beta != 0.0f ? fmaf(args.alpha, v, args.beta * *dst) : args.alpha * v;
+                        else
+                            *dst = v;
+                    }
                 }
+                __syncwarp();
             }
         }
     }
