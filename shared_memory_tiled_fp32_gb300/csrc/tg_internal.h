@@ -117,11 +117,6 @@ struct Plan {
 tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int lda, const void* B,
                    int ldb, const void* C, int ldc, int path, int split_k, bool need_pointers = true);
 
-// Output blocks of the host-buffer entry point: C is cut into pm x pn blocks;
-// row block 0 has `first` rows, the others mb (multiples of 128, the last
-// ragged), column blocks nb columns (a multiple of 256, the last ragged).
-// The choice minimises a modelled pipeline time (copies in, products, copies
-// out).  Host arithmetic only.
 // Output blocks of the host-buffer pipeline: pm row blocks (the first of
 // `first` rows, the others of `mb`, the last one the remainder); row blocks
 // [0, split) are cut into pn column blocks of nb columns (the last ragged),
