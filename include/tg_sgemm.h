@@ -211,6 +211,16 @@ typedef struct {
  * path or out == NULL. */
 tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, tg_host_blocks_info* out);
 
+/* Device memory tg_sgemm_host allocates (stream-ordered, from the device's
+ * memory pool) for these sizes, with the blocks tg_sgemm_host_blocks reports:
+ * *total = the copies of A, B and C (16-byte row pitches), the split tiles
+ * and the largest workspace any one product needs (also in
+ * *product_workspace, which may be NULL).  Host arithmetic only; path and
+ * split_k as in tg_sgemm_opts, num_sms as in tg_sgemm_host_blocks.
+ * TG_ERR_INVALID_VALUE on negative sizes, an unknown path or total == NULL. */
+tg_status tg_sgemm_host_device_bytes(int M, int N, int K, int path, int split_k, int num_sms, size_t* total,
+                                     size_t* product_workspace);
+
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns TG_ERR_TIMEOUT if any kernel of this library on this device gave up
  * a bounded wait since the last check (the word is shared by all streams),

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     TgError,
     error_site,
     host_blocks,
+    host_device_bytes,
     lib,
     matmul,
     matmul_general,

@@ -35,6 +35,7 @@ EXPORTS = (
     "tg_sgemm_workspace_bytes",
     "tg_sgemm_host",
     "tg_sgemm_host_blocks",
+    "tg_sgemm_host_device_bytes",
     "tg_sgemm_noalloc",
     "tg_sgemm_sync_status",
     "tg_sgemm_error_site",
@@ -127,6 +128,9 @@ def lib():
         L.tg_sgemm_noalloc.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
         L.tg_sgemm_host_blocks.argtypes = [i, i, i, i, i, ctypes.POINTER(HostBlocksInfo)]
+        L.tg_sgemm_host_device_bytes.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t),
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+        L.tg_sgemm_host_device_bytes.restype = i
         L.tg_sgemm_host_blocks.restype = i
         L.tg_sgemm_plan.argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, ctypes.POINTER(PlanInfo)]
         L.tg_sgemm_plan.restype = i
@@ -360,6 +364,16 @@ def host_blocks(M, N, K, *, path="auto", num_sms=0) -> dict:
                                     ctypes.byref(info))
     _check(st, "tg_sgemm_host_blocks")
     return info.as_dict()
+
+
+def host_device_bytes(M, N, K, *, path="auto", split_k=0, num_sms=0) -> dict:
+    """Device memory one sgemm_host call allocates (host arithmetic): the total
+    and the largest single-product workspace within it."""
+    total, ws = ctypes.c_size_t(), ctypes.c_size_t()
+    st = lib().tg_sgemm_host_device_bytes(M, N, K, PATHS[path] if isinstance(path, str) else int(path), split_k,
+                                          num_sms, ctypes.byref(total), ctypes.byref(ws))
+    _check(st, "tg_sgemm_host_device_bytes")
+    return {"total": total.value, "product_workspace": ws.value}
 
 
 def plan(M, N, K, lda=None, ldb=None, ldc=None, *, A=0, B=0, C=0, path="auto", split_k=0,

@@ -259,6 +259,54 @@ struct HostTrace {
     }
 };
 
+// Device memory of one host-buffer call: the 16-byte-pitched copies of A, B
+// and C, the split tiles (all of B^T's, one A row block's) and the largest
+// workspace any of its products needs.
+struct HostBytes {
+    size_t a = 0, b = 0, c = 0, b_split = 0, a_split = 0, ws_max = 0;
+    size_t total() const { return a + b + c + b_split + a_split + ws_max; }
+};
+
+// The column offset and width of block j of row block i.
+void host_block_cols(const tg::HostBlocks& hb, int N, int i, int j, int* j0, int* Nj) {
+    if (hb.col_blocks(i) == 1) {
+        *j0 = 0;
+        *Nj = N;
+    } else {
+        *j0 = j * hb.nb;
+        *Nj = std::min(hb.nb, N - *j0);
+    }
+}
+
+HostBytes host_bytes(const tg::HostBlocks& hb, int M, int N, int K, int path, int split_k, int num_sms) {
+    using namespace tg;
+    const bool tf32 = path == TG_PATH_TF32X3;
+    const long long k4 = ((long long)std::max(K, 1) + 3) / 4 * 4, n4 = ((long long)N + 3) / 4 * 4;
+    const long long k16 = ((long long)std::max(K, 1) + 15) / 16 * 16;
+    auto align = [](size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; };
+    HostBytes r;
+    r.a = 4ull * M * k4;
+    r.b = 4ull * (size_t)std::max(K, 1) * n4;
+    r.c = 4ull * M * n4;
+    const int mb_max = std::max(hb.first, hb.mb);
+    r.b_split = tf32 ? align(8ull * ((N + 255) / 256 * 256) * k16) : 0;
+    r.a_split = tf32 ? align(8ull * ((mb_max + 255) / 256 * 256) * k16) : 0;
+    // placeholder pointers with the alignment the real ones will have
+    const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
+    // every product: a row block's shape (its rows, and column blocks or full
+    // width) can differ from its neighbours' anywhere in the list
+    for (int i = 0; i < hb.pm; ++i)
+        for (int j = 0; j < hb.col_blocks(i); ++j) {
+            int j0 = 0, Nj = 0;
+            host_block_cols(hb, N, i, j, &j0, &Nj);
+            Plan pl;
+            make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), Nj, K, 1.0f, al, (int)k4, al, (int)n4, 0.0f, al, (int)n4,
+                      path, split_k, num_sms, &pl, tf32, tf32);
+            r.ws_max = std::max(r.ws_max, pl.ws_bytes);
+        }
+    return r;
+}
+
 }  // namespace
 
 tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
@@ -287,39 +335,14 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     // full width once all of B is in.  A and B are split once, by the first
     // product that reads each block, into shared hi/lo regions.
     const HostBlocks hb = choose_host_blocks(M, N, K, path, d->num_sms);
-    const int pm = hb.pm, pn = hb.pn, nb = hb.nb, mb_max = std::max(hb.first, hb.mb);
-    // the (row offset, rows, column offset, columns) of block j of row block i
-    auto block_cols = [&](int i, int j, int* j0, int* Nj) {
-        if (hb.col_blocks(i) == 1) {
-            *j0 = 0;
-            *Nj = N;
-        } else {
-            *j0 = j * nb;
-            *Nj = std::min(nb, N - *j0);
-        }
-    };
-
+    const int pm = hb.pm, pn = hb.pn, nb = hb.nb;
+    auto block_cols = [&](int i, int j, int* j0, int* Nj) { host_block_cols(hb, N, i, j, j0, Nj); };
     // device copies: 16-byte row pitches, so TMA reads them in place
-    const size_t a_bytes = 4ull * M * k4, b_bytes = 4ull * (size_t)std::max(K, 1) * n4,
-                 c_bytes = 4ull * M * n4;
-    auto align = [](size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; };
+    const HostBytes hbytes = host_bytes(hb, M, N, K, path, o.split_k, d->num_sms);
+    const size_t a_bytes = hbytes.a, b_bytes = hbytes.b, c_bytes = hbytes.c, b_split = hbytes.b_split,
+                 a_split = hbytes.a_split;
     const long long k16 = ((long long)std::max(K, 1) + 15) / 16 * 16;
-    // split tiles (rows padded to 256): all of B^T's, and one A row block's
-    const size_t b_split = tf32 ? align(8ull * ((N + 255) / 256 * 256) * k16) : 0;
-    const size_t a_split = tf32 ? align(8ull * ((mb_max + 255) / 256 * 256) * k16) : 0;
-    // placeholder pointers with the alignment the real ones will have
-    const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
-    size_t ws_max = 0;  // over the block shapes (whole or ragged rows x columns, or full width)
-    for (int i : {0, std::min(1, pm - 1), pm - 1})
-        for (int j : {0, hb.col_blocks(i) - 1}) {
-            int j0 = 0, Nj = 0;
-            block_cols(i, j, &j0, &Nj);
-            Plan pl;
-            make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), Nj, K, 1.0f, al, (int)k4, al, (int)n4, 0.0f, al,
-                      (int)n4, path, o.split_k, d->num_sms, &pl, tf32, tf32);
-            ws_max = std::max(ws_max, pl.ws_bytes);
-        }
-    const size_t ws_total = b_split + a_split + ws_max;
+    const size_t ws_total = b_split + a_split + hbytes.ws_max;
 
     void *dA = nullptr, *dB = nullptr, *dC = nullptr, *W = nullptr;
     if (cudaMallocFromPoolAsync(&dA, a_bytes, d->pool, stream) != cudaSuccess ||
@@ -426,6 +449,27 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     st = read_error_word(stream, true, &word);
     if (st != TG_OK) return st;
     return word != 0 ? TG_ERR_TIMEOUT : TG_OK;
+}
+
+tg_status tg_sgemm_host_device_bytes(int M, int N, int K, int path, int split_k, int num_sms, size_t* total,
+                                     size_t* product_workspace) {
+    using namespace tg;
+    if (M < 0 || N < 0 || K < 0 || split_k < 0 || total == nullptr) return TG_ERR_INVALID_VALUE;
+    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3) return TG_ERR_INVALID_VALUE;
+    if (num_sms <= 0) {
+        DeviceState* d = nullptr;
+        const tg_status st = current_device(&d);
+        if (st != TG_OK) return st;
+        num_sms = d->num_sms;
+    }
+    *total = 0;
+    if (product_workspace != nullptr) *product_workspace = 0;
+    if (M == 0 || N == 0) return TG_OK;
+    const int p = path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3;
+    const HostBytes b = host_bytes(choose_host_blocks(M, N, K, p, num_sms), M, N, K, p, split_k, num_sms);
+    *total = b.total();
+    if (product_workspace != nullptr) *product_workspace = b.ws_max;
+    return TG_OK;
 }
 
 tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, tg_host_blocks_info* out) {

@@ -327,6 +327,28 @@ def test_host_blocks_override(monkeypatch):
         assert tg.host_blocks(4100, 3000, 1500, path="tf32x3", num_sms=152) == model
 
 
+def test_host_device_bytes_cover_every_product(monkeypatch):
+    """The host call's workspace is sized over every product.  In this layout
+    the middle row blocks are full width (1024 x 3000, a stream-K tail of 48
+    pair units over 76 lanes with two partial slots per lane) while the first
+    two and the last are not: their shapes alone would under-size it."""
+    monkeypatch.setenv("TG_HOST_BLOCKS", "1024,1024,1536,2,1")
+    got = tg.host_device_bytes(4100, 3000, 1500, path="tf32x3", num_sms=152)
+    mid = tg.plan(1024, 3000, 1500, num_sms=152, path="tf32x3")
+    assert mid["tail_lanes"] > 0 and mid["tail_kx"] == 0
+    tail_slots = 2 * mid["tail_lanes"] * mid["pair"] * 128 * 256 * 4
+    assert got["product_workspace"] >= tail_slots
+    for shape in ((1024, 1536), (1024, 1464), (4, 3000)):
+        q = tg.plan(*shape, 1500, num_sms=152, path="tf32x3")
+        assert tail_slots > (2 * q["tail_lanes"] * q["pair"] * 128 * 256 * 4 if q["tail_kx"] == 0 else 0)
+    # copies of A, B, C with 16-byte row pitches come on top
+    assert got["total"] > got["product_workspace"] + 4 * (4100 * 1500 + 1500 * 3000 + 4100 * 3000)
+    assert tg.host_device_bytes(0, 5, 5, num_sms=152) == {"total": 0, "product_workspace": 0}
+    total = ctypes.c_size_t()
+    assert tg.lib().tg_sgemm_host_device_bytes(-1, 4, 4, 0, 0, 152, ctypes.byref(total), None) == 1
+    assert tg.lib().tg_sgemm_host_device_bytes(4, 4, 4, 0, 0, 152, None, None) == 1
+
+
 def test_host_blocks_full_width_later_rows():
     """For 8192^3 the model cuts only the first row block into column blocks
     (the first product starts early) and computes the later row blocks full

@@ -8,6 +8,8 @@ otherwise normwise relative error <= 1e-5 and element-wise error
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -207,15 +209,16 @@ def test_host_buffer_entry_row_blocks(tg, path):
     assert np.all(np.isnan(Cbig.numpy()[:, N:])), "host entry wrote past column N"
 
 
-@pytest.mark.parametrize("layout", [None, "1024,1024,1536,4", "512,1536,1024,2"])
+@pytest.mark.parametrize("layout", [None, "1024,1024,1536,4", "512,1536,1024,2,1"])
 @pytest.mark.parametrize("path", ["tf32x3", "ffma"])
 def test_host_buffer_entry_2d_blocks(tg, path, layout, monkeypatch):
     """The host entry point with C cut into row blocks, the first ones also
     into column blocks (ragged last ones), the later ones full width: every
     product waits for its own A row block and B column block (all of B when
     full width), A and B are split once and reused, C blocks are copied out
-    as they finish.  The model's layout, every row block cut, and two of four
-    cut.  Sampled rows at and around every row-block edge, all columns."""
+    as they finish (or after the last copy in).  The model's layout, every
+    row block cut, and two of four cut with the copies out held back.
+    Sampled rows at and around every row-block edge, all columns."""
     if layout is not None:
         monkeypatch.setenv("TG_HOST_BLOCKS", layout)
     M, N, K = 4100, 3000, 1500
@@ -223,8 +226,9 @@ def test_host_buffer_entry_2d_blocks(tg, path, layout, monkeypatch):
     assert hb["row_blocks"] > 1
     if layout is not None:
         assert hb["col_blocks"] > 1
-        assert ",".join(str(hb[k]) for k in ("first_block_rows", "block_rows", "block_cols",
-                                               "split_row_blocks")) == layout
+        fields = ("first_block_rows", "block_rows", "block_cols", "split_row_blocks", "defer_copies_out")
+        want = [int(x) for x in layout.split(",")]
+        assert [hb[k] for k in fields[:len(want)]] == want
     A, B = make_inputs(M, N, K, "uniform", 322)
     Ap, Bp = A.pin_memory(), B.pin_memory()
     Cbig = torch.full((M, N + 3), float("nan")).pin_memory()
@@ -239,6 +243,36 @@ def test_host_buffer_entry_2d_blocks(tg, path, layout, monkeypatch):
     assert np.all(np.isnan(Cbig.numpy()[:, N:])), "host entry wrote past column N"
     dev = run(tg, A, B, path=path)  # same products as the device entry, block by block
     assert_close(C.numpy(), dev, K, f"host vs device {path}")
+
+
+def test_host_trace_timeline(tg):
+    """TG_HOST_TRACE=1 prints the host call's timeline: every copy in, every
+    product's begin and end and every copy out, with times that start at 0
+    and products that end after they begin."""
+    import re
+    import subprocess
+    import sys
+
+    code = ("import numpy as np, torch, shared_memory_tiled_fp32_gb300 as tg;"
+            "A = torch.ones(4100, 1500).pin_memory(); B = torch.ones(1500, 3000).pin_memory();"
+            "C = torch.empty(4100, 3000).pin_memory(); tg.sgemm_host(A, B, C);"
+            "assert float(C[0, 0]) == 1500.0 and float(C[-1, -1]) == 1500.0")
+    env = dict(os.environ, TG_HOST_TRACE="1", TG_HOST_BLOCKS="1024,1024,1536,2,1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("tg_host_trace")]
+    times = {m.group(2): float(m.group(1)) for m in
+             (re.match(r"tg_host_trace\s+([0-9.]+) ms (.*)$", ln) for ln in lines) if m}
+    # 5 row blocks: the first two cut into 2 column blocks, the other three full width
+    assert sum(k.startswith("in A") for k in times) == 5 and sum(k.startswith("in B") for k in times) == 2
+    products = [k[len("product "):-len(" begins")] for k in times if k.endswith(" begins")]
+    assert len(products) == 2 * 2 + 3
+    for p in products:
+        assert times[f"product {p} ends"] >= times[f"product {p} begins"] >= 0.0
+        assert times[f"out {p}"] >= times[f"product {p} ends"]
+    # copies out held back until the last copy in
+    assert min(times[f"out {p}"] for p in products) >= max(v for k, v in times.items() if k.startswith("in "))
 
 
 def test_side_stream(tg):
