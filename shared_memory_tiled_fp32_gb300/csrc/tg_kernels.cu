@@ -492,26 +492,44 @@ constexpr uint32_t kSwRowGroupBytes = 8 * kTfRowBytes;  // 8 rows of the 128-byt
 constexpr long long kTileFloats = kTfAStage / 4;        // one 128-row tile: 4096 floats
 constexpr uint32_t kDescSwizzle128 = 2;
 static_assert(kTfRowBytes == 128, "one K block of hi and lo must fill one 128-byte swizzle row");
-constexpr int kTfBars = 2 * kTf32Stages + 5;
-static_assert(kTfBars * 8 + 16 <= 128, "barriers and the tensor-memory slot fit in 128 bytes");
 // one 32 x 32 fp32 staging block per epilogue warp for the coalesced C store
 constexpr uint32_t kTfOutStageBytes = 8 * 32 * 32 * 4;
-constexpr size_t kTfSmemBytes = 1024 + (size_t)kTf32Stages * kTfStageBytes + 128 + kTfOutStageBytes;
-static_assert(kTfSmemBytes <= 232448, "fits the 227 KiB of shared memory a block may opt in to");
+constexpr uint32_t kTfBarBytes = 256;  // mbarriers and the tensor-memory slot
 
-template <int kPair>
+// Stage ring of the two forms of the kernel.  Per-CTA tensor-core issue
+// (kPairMma false): a stage holds the A tile and the whole B tile, 48 KiB, 4
+// stages.  Pair MMA (cta_group::2, the pair's first CTA issuing M = 256
+// products for both): a CTA holds its A tile and its half of B, 32 KiB, so 6
+// stages fit.
+template <bool kPairMma>
+struct TfRing {
+    static constexpr int kStages = kPairMma ? 6 : kTf32Stages;
+    static constexpr uint32_t kStageBytes = kPairMma ? 2 * kTfAStage : kTfStageBytes;
+    static constexpr int kBars = 2 * kStages + 5;
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kTfBarBytes + kTfOutStageBytes;
+    static_assert(kBars * 8 + 16 <= (int)kTfBarBytes, "barriers and the tensor-memory slot fit");
+    static_assert(kSmemBytes <= 232448, "fits the 227 KiB of shared memory a block may opt in to");
+};
+constexpr size_t kTfSmemBytes = TfRing<false>::kSmemBytes;
+constexpr size_t kTfSmemBytesPairMma = TfRing<true>::kSmemBytes;
+
+template <int kPair, bool kPairMma>
 __global__ void __launch_bounds__(kTfThreads, 1)
-    tf32x3_gemm_kernel(GemmArgs args) {
-    constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK, ST = kTf32Stages;
+    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       GemmArgs args) {
+    static_assert(!kPairMma || kPair == 2, "the pair MMA needs a CTA pair");
+    constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK;
+    constexpr int ST = TfRing<kPairMma>::kStages;
+    constexpr uint32_t kStageBytes = TfRing<kPairMma>::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem_1024(smem_raw);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * kTfStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * kStageBytes);
     uint64_t* empty = full + ST;
     uint64_t* tfull = empty + ST;  // [2] chunk accumulated
     uint64_t* tempty = tfull + 2;  // [2] chunk drained by the epilogue
     uint64_t* drain = tempty + 2;  // every MMA of this CTA completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-    float* out_stage = reinterpret_cast<float*>(smem + ST * kTfStageBytes + 128);  // [8 warps][32 x 32]
+    float* out_stage = reinterpret_cast<float*>(smem + ST * kStageBytes + kTfBarBytes);  // [8 warps][32 x 32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WaitCtl wc{&g_error_word, args.timeout_ns};
@@ -521,22 +539,31 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     const long long first_unit = blockIdx.x / kPair, unit_stride = gridDim.x / kPair;
     constexpr uint16_t kPairMask = (uint16_t)((1u << kPair) - 1u);
     constexpr uint32_t kBHalf = kTfBStage / kPair;  // bytes of the B tile one CTA loads
+    // pair MMA: the first CTA's barriers gather both CTAs' copies (full) and
+    // both CTAs' chunk drains (tempty)
+    const bool issuer = !kPairMma || rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kPair);  // one MMA commit from each CTA of the pair
+            // one MMA commit from each CTA of a multicast pair; one for both with the pair MMA
+            mbar_init(&empty[s], kPairMma ? 1 : kPair);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 8);
+            mbar_init(&tempty[b], kPairMma ? 16 : 8);
         }
         mbar_init(drain, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        if (kPairMma) {
+            tmem_alloc_pair(tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -562,7 +589,23 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = smem + stage * kTfStageBytes;
+                    uint8_t* st = smem + stage * kStageBytes;
+                    if (kPairMma) {
+                        // this CTA's A tile and B half into its own ring; both
+                        // CTAs' copies complete on the first CTA's "full"
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                        const uint32_t bar0 = cluster_addr(&full[stage], 0);
+                        tma_load_2d_pair(st, &tmA, bar0, 0, ((t.m0 >> 7) * args.kbs + kb) * 128);
+                        tma_load_2d_pair(st + kTfAStage, &tmB, bar0, 0,
+                                         (((t.n0 >> 7) + rank) * args.kbs + kb) * 128);
+                        issued |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == ST) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     // this CTA receives the whole A and B tiles (48 KiB), half
                     // of B from its own copy and half from the peer's
                     mbar_arrive_expect_tx(&full[stage], kTfStageBytes);
@@ -586,10 +629,19 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                     }
                 }
             }
-            for (int s = 0; s < ST; ++s)
-                if ((issued >> s) & 1u) mbar_drain(&full[s], (last_par >> s) & 1u, args.timeout_ns);
-        } else if (warp == 1 && lane == 0) {  // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_tf32(BM, BN);
+            // every copy must land before the CTA may exit.  Pair MMA: the
+            // first CTA's "full" barriers count both CTAs' bytes; the second
+            // CTA waits instead until the products have consumed its last
+            // stages ("empty" completes only after the copies landed).
+            for (int s = 0; s < ST; ++s) {
+                if (!((issued >> s) & 1u)) continue;
+                if (issuer)
+                    mbar_drain(&full[s], (last_par >> s) & 1u, args.timeout_ns);
+                else
+                    mbar_drain(&empty[s], (last_par >> s) & 1u, args.timeout_ns);
+            }
+        } else if (warp == 1 && lane == 0 && issuer) {  // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_tf32(kPairMma ? 2 * BM : BM, BN);
             static_assert(BK == 16 && kTfRowBytes == 128, "the issue loop below is written for two 8-wide slices");
             const uint64_t desc_stage0 = smem_desc_kmajor(smem_addr(smem), kSwRowGroupBytes, kDescSwizzle128);
             int stage = 0;
@@ -615,8 +667,23 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         // descriptors of this stage's tiles; their address field
                         // counts 16-byte units, so the lo half of each 128-byte row
                         // is +4 and the second 8-wide K slice +2
-                        const uint64_t da = desc_stage0 + (uint64_t)stage * (kTfStageBytes >> 4);
+                        const uint64_t da = desc_stage0 + (uint64_t)stage * (kStageBytes >> 4);
                         const uint64_t db = da + (kTfAStage >> 4);
+                        if (kPairMma) {  // M = 256 over the pair: each CTA's A rows and B half
+                            const uint32_t acc = kb > c0 ? 1u : 0u;
+                            mma_tf32_ss_pair(d_tmem, da, db + 4, idesc, acc);
+                            mma_tf32_ss_pair(d_tmem, da, db, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, da + 4, db, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, da + 2, db + 6, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, da + 2, db + 2, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, da + 6, db + 2, idesc, 1u);
+                            mma_commit_pair(&empty[stage], kPairMask);
+                            if (++stage == ST) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                            continue;
+                        }
                         // A_hi is read from shared memory once per slice and kept in
                         // the tensor core's A collector for its second product.  The
                         // chunk's first K block starts the accumulator.  No branch
@@ -640,11 +707,19 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                             phase ^= 1u;
                         }
                     }
-                    if (ok) mma_commit(&tfull[buf]);
+                    if (ok) {
+                        if (kPairMma)
+                            mma_commit_pair(&tfull[buf], kPairMask);
+                        else
+                            mma_commit(&tfull[buf]);
+                    }
                 }
             }
             // no tensor-memory access may be in flight when the CTA frees it
-            mma_commit(drain);
+            if (kPairMma)
+                mma_commit_pair(drain, kPairMask);
+            else
+                mma_commit(drain);
             mbar_drain(drain, 0, args.timeout_ns);
         }
     } else {  // ---------------------------------------------------- epilogue
@@ -679,7 +754,12 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);  // chunk buffer may be refilled
+                if (lane == 0) {  // chunk buffer may be refilled
+                    if (kPairMma)
+                        mbar_arrive_cluster(cluster_addr(&tempty[buf], 0));
+                    else
+                        mbar_arrive(&tempty[buf]);
+                }
             }
             if (!ok) break;
             // Guarded store of the warp's 32 rows x 128 columns, coalesced: each
@@ -724,10 +804,16 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     }
 
     __syncthreads();
+    // pair MMA: the first CTA's products write both CTAs' tensor memory, and
+    // its MMA thread has seen them all complete before it gets here
+    if (kPairMma) cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (kPairMma)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
     // neither CTA of a pair may exit while the other can still multicast into
     // its shared memory or arrive on its barriers
@@ -1260,6 +1346,16 @@ int g_prepass_blocks_per_sm[2] = {4, 4};
 // CTA pairs of the 3xTF32 kernel resident at once (0 = unknown).
 int g_tf32_pair_clusters = 0;
 
+// CTA pairs issue one M = 256 tensor-core product over both CTAs
+// (cta_group::2), each CTA holding its A tile and its half of B, so the ring
+// has 6 stages instead of 4 (measured: 3xTF32 steps 2.8-3.5 % faster at
+// 4096^3, 8192^3 and 2048 x 2048 x 16384).  TG_TF32X3_PAIRMMA=0 keeps one
+// M = 128 product per CTA with B multicast to both.
+bool pair_mma_enabled() {
+    const char* e = std::getenv("TG_TF32X3_PAIRMMA");
+    return !(e != nullptr && e[0] == '0');
+}
+
 tg_status prepare_device_kernels() {
     int nb = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<false>, 256, 0) == cudaSuccess && nb > 0)
@@ -1275,11 +1371,16 @@ tg_status prepare_device_kernels() {
     if (cudaFuncSetAttribute(ffma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFfmaSmemBytes) != cudaSuccess)
         return TG_ERR_CUDA;
-    for (auto kern : {tf32x3_gemm_kernel<1>, tf32x3_gemm_kernel<2>}) {
-        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TG_ERR_CUDA;
+    struct {
+        void (*kern)(CUtensorMap, CUtensorMap, GemmArgs);
+        size_t smem;
+    } tf_kernels[] = {{tf32x3_gemm_kernel<1, false>, kTfSmemBytes},
+                      {tf32x3_gemm_kernel<2, false>, kTfSmemBytes},
+                      {tf32x3_gemm_kernel<2, true>, kTfSmemBytesPairMma}};
+    for (const auto& k : tf_kernels) {
+        if (cudaFuncGetAttributes(&fa, k.kern) != cudaSuccess) return TG_ERR_CUDA;
         if (fa.numRegs != kTfLaunchRegs) return TG_ERR_CUDA;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTfSmemBytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(k.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem) != cudaSuccess)
             return TG_ERR_CUDA;
     }
     // how many CTA pairs the GPU holds at once (one CTA per SM)
@@ -1295,7 +1396,7 @@ tg_status prepare_device_kernels() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tf32x3_gemm_kernel<2>, &cfg) == cudaSuccess && clusters > 0)
+    if (cudaOccupancyMaxActiveClusters(&clusters, tf32x3_gemm_kernel<2, false>, &cfg) == cudaSuccess && clusters > 0)
         g_tf32_pair_clusters = clusters;
     else
         cudaGetLastError();
@@ -1403,15 +1504,28 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         ga.b_tiles = b_tiles;
         ga.kbs = p.k16 / 16;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
+        // the pair-MMA form reads the tiles through 2-D tensor maps: rows of
+        // 32 floats (one tile row, hi and lo), boxes of one 128-row tile
+        CUtensorMap mA{}, mB{};
+        const bool pair_mma = p.pair == 2 && pair_mma_enabled();
+        if (pair_mma &&
+            (!make_map(&mA, a_tiles, 32, (uint64_t)p.a_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+             !make_map(&mB, b_tiles, 32, (uint64_t)p.b_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return TG_ERR_CUDA;
         if (p.pair == 2) {
             int clusters = p.grid / 2;
             if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
-            if (launch_dependent(tf32x3_gemm_kernel<2>, dim3(2 * clusters), dim3(kTfThreads), kTfSmemBytes, stream, 2,
-                                 ga) != TG_OK)
+            if (pair_mma) {
+                if (launch_dependent(tf32x3_gemm_kernel<2, true>, dim3(2 * clusters), dim3(kTfThreads),
+                                     kTfSmemBytesPairMma, stream, 2, mA, mB, ga) != TG_OK)
+                    return TG_ERR_CUDA;
+            } else if (launch_dependent(tf32x3_gemm_kernel<2, false>, dim3(2 * clusters), dim3(kTfThreads),
+                                        kTfSmemBytes, stream, 2, mA, mB, ga) != TG_OK) {
                 return TG_ERR_CUDA;
+            }
         } else {
-            if (launch_dependent(tf32x3_gemm_kernel<1>, dim3(p.grid), dim3(kTfThreads), kTfSmemBytes, stream, 1,
-                                 ga) != TG_OK)
+            if (launch_dependent(tf32x3_gemm_kernel<1, false>, dim3(p.grid), dim3(kTfThreads), kTfSmemBytes, stream,
+                                 1, mA, mB, ga) != TG_OK)
                 return TG_ERR_CUDA;
         }
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;

@@ -292,18 +292,26 @@ def test_plan_on_device(tg):
     assert p["path"] == "tf32x3"
 
 
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_tf32x3_cluster_pairs_on_and_off(tg, pair, monkeypatch):
-    """The 3xTF32 kernel with and without CTA pairs sharing B by TMA multicast,
-    including odd tile-row counts (the last pair's second CTA is all ghost)."""
+@pytest.mark.parametrize("pair,pair_mma", [("0", "1"), ("1", "0"), ("1", "1")])
+def test_tf32x3_cluster_pairs_on_and_off(tg, pair, pair_mma, monkeypatch):
+    """The three forms of the 3xTF32 kernel: one CTA per tile; CTA pairs with
+    one M = 128 product per CTA and B multicast to both; CTA pairs with one
+    M = 256 product over both (cta_group::2, each CTA holding its half of B)
+    -- including odd tile-row counts (the last pair's second CTA is all
+    ghost), split K and a stream-K tail."""
     monkeypatch.setenv("TG_TF32X3_PAIR", pair)
-    for i, (M, N, K) in enumerate([(129, 300, 700), (383, 513, 300), (640, 256, 2048), (1, 7, 9)]):
+    monkeypatch.setenv("TG_TF32X3_PAIRMMA", pair_mma)
+    for i, (M, N, K) in enumerate([(129, 300, 700), (383, 513, 300), (640, 256, 2048), (1, 7, 9),
+                                   (1000, 3000, 1100)]):
         A, B = make_inputs(M, N, K, "uniform", 900 + i)
         ref = oracle.sgemm(A.numpy(), B.numpy())
         p = tg.plan(M, N, K, path="tf32x3")
         assert p["tiles_m"] == -(-M // 128)
         for split in (0, 1, 2):
-            assert_close(run(tg, A, B, path="tf32x3", split_k=split), ref, K, f"pair={pair} {M}x{N}x{K} s{split}")
+            assert_close(run(tg, A, B, path="tf32x3", split_k=split), ref, K,
+                         f"pair={pair} mma={pair_mma} {M}x{N}x{K} s{split}")
+    A, B = make_inputs(1000, 3000, 1100, "int", 911)
+    assert_bitexact(run(tg, A, B, path="tf32x3"), oracle.sgemm(A.numpy(), B.numpy()), "pair forms, integers")
 
 
 TAIL_CASES = [(1000, 3000, 1100, "uniform", "tf32x3"), (1000, 3000, 1100, "int", "tf32x3"),
