@@ -1507,7 +1507,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         // the pair-MMA form reads the tiles through 2-D tensor maps: rows of
         // 32 floats (one tile row, hi and lo), boxes of one 128-row tile
         CUtensorMap mA{}, mB{};
-        const bool pair_mma = p.pair == 2 && pair_mma_enabled();
+        // (tile-row coordinates are 32-bit: larger arrays keep the per-CTA form)
+        const bool pair_mma = p.pair == 2 && pair_mma_enabled() && (long long)p.a_rows * ga.kbs < (1ll << 31) &&
+                              (long long)p.b_rows * ga.kbs < (1ll << 31);
         if (pair_mma &&
             (!make_map(&mA, a_tiles, 32, (uint64_t)p.a_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
              !make_map(&mB, b_tiles, 32, (uint64_t)p.b_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
