@@ -11,10 +11,11 @@ namespace tg {
 
 // CTA tile shapes of the two math paths.
 //
-// TF32x3: a 128 x 256 output tile per CTA (tcgen05 M=128, N=256 accumulator,
-// 256 of the 512 tensor-memory columns, so two chunks are in flight), K staged
-// 16 values at a time (hi and lo: one 128-byte swizzle row per tile row),
-// 4 stages of 48 KiB.
+// TF32x3: a 128 x 256 output tile per CTA (a 256 x 256 tile per CTA pair;
+// N=256 accumulator rows of 256 of the 512 tensor-memory columns, so two
+// chunks are in flight), K staged 16 values at a time (hi and lo: one
+// 128-byte swizzle row per tile row); kTf32Stages stages of 48 KiB in the
+// per-CTA form (the pair-MMA form holds 6 of 32 KiB, see tg_kernels.cu).
 constexpr int kTf32BM = 128, kTf32BN = 256, kTf32BK = 16, kTf32Stages = 4;
 // FFMA: a 128 x 256 output tile, 256 math threads each holding an 8 x 16
 // register block, K staged 32 floats at a time, 4 stages of 48 KiB.

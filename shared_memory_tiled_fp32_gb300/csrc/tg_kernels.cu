@@ -446,19 +446,28 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 // Operands come from the split pre-pass as 16 KiB tiles: 128 rows of A (or
 // of B transposed) x one 16-wide K block, each row 16 hi values then the same
 // 16 lo values (128 bytes), already in the 128-byte-swizzled order of the
-// tensor core's K-major layout.  A stage is then one contiguous bulk copy per
-// 128-row tile (A, and B's two halves: one per CTA of a pair, multicast to
-// both) rather than a TMA box of 128 or 256 separate rows.  Measured on
-// GB300 with cycle counters: four boxes of 64-byte rows per stage left the
-// MMA thread waiting for data 19 % of the time, two boxes of 128-byte rows
-// 12 %.  Within a stage the hi slice ks (8 values) starts ks * 32 bytes into
-// each row and the lo slice 64 bytes after it.
+// tensor core's K-major layout.  A stage is then one copy per 128-row tile
+// rather than a TMA box of 128 or 256 separate rows.  Measured on GB300 with
+// cycle counters: four boxes of 64-byte rows per stage left the MMA thread
+// waiting for data 19 % of the time, two boxes of 128-byte rows 12 %.
+// Within a stage the hi slice ks (8 values) starts ks * 32 bytes into each
+// row and the lo slice 64 bytes after it.
+//
+// Two forms.  Pair MMA (the default for CTA pairs): the pair's first CTA
+// issues M = 256 products (tcgen05.mma.cta_group::2) whose A rows and B rows
+// (N) are split between the two CTAs' shared memory, each CTA holding its A
+// tile and its half of B (32 KiB a stage, 6 stages), loaded by 2-D
+// tensor-map copies that complete on the first CTA's barrier; each CTA's
+// tensor memory holds its 128 rows of the accumulator.  Per-CTA MMA (single
+// CTAs, or pairs with the pair MMA off): each CTA issues M = 128 products
+// on its A tile and the whole B tile (48 KiB a stage, 4 stages), its own B
+// half fetched by one bulk copy multicast into both CTAs of the pair.
 //
 // Per 8-wide K slice the MMA thread issues
 //     D += A_hi B_lo;  D += A_hi B_hi;  D += A_lo B_hi
-// (A_lo B_lo, of relative size 2^-22, is dropped).  The first two share A_hi,
-// which the tensor core keeps in its A collector buffer, so each slice reads
-// A_hi from shared memory once.
+// (A_lo B_lo, of relative size 2^-22, is dropped).  In the per-CTA form the
+// first two share A_hi, which the tensor core keeps in its A collector
+// buffer, so each slice reads A_hi from shared memory once.
 //
 // Accumulation precision.  The tensor core's fp32 accumulation loses about
 // one unit in the last place towards zero per MMA instead of rounding to
@@ -471,8 +480,8 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 // 7e-9 * 256 ~ 2e-6 relative, independent of K.
 //
 // Warp roles (384 threads, 3 warpgroups): warp 0 = copy producer, warp 1 =
-// tensor-memory owner and MMA issuer (one thread), warps 2-3 idle; warps 4-11
-// = epilogue.  Epilogue warp e reads tensor-memory lanes 32*(e%4).. (a warp
+// tensor-memory owner and MMA issuer (one thread; with the pair MMA only in
+// the pair's first CTA), warps 2-3 idle; warps 4-11 = epilogue.  Epilogue warp e reads tensor-memory lanes 32*(e%4).. (a warp
 // may only touch the lane quarter of its warp index modulo 4) and columns
 // 128*(e/4)..+127, so each thread owns 128 accumulators of one output row.
 // Two chunk buffers of 256 columns (all 512 tensor-memory columns) let the
