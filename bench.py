@@ -174,11 +174,21 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def kernel_source_fingerprint() -> str:
+    """sha256 (first 16 hex digits) of tg_kernels.cu without its comments and
+    blank lines: the counters in a profile summary stay valid while the code
+    they were taken on is unchanged."""
+    src = open(os.path.join(ROOT, "shared_memory_tiled_fp32_gb300", "csrc", "tg_kernels.cu")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines()]
+    code = "\n".join(ln for ln in lines if ln.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def traffic_from_profiles(kernel_tag: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
-    src = os.path.join(ROOT, "shared_memory_tiled_fp32_gb300", "csrc", "tg_kernels.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    the current kernel code (else None)."""
+    sha = kernel_source_fingerprint()
     prof = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
     if not os.path.exists(prof):
         return None
