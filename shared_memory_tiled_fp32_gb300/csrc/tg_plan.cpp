@@ -292,7 +292,7 @@ double product_seconds(const Plan& p, double rate) {
 // in).  Rates measured on GB300 over NVLink-C2C with pinned host memory:
 // 205 GB/s in alone, 190 GB/s out alone, about 170 GB/s each way while both
 // directions are busy, plus ~40 us per copy out; the split pre-pass about
-// 5.7 TB/s; a full round of work units 355 (3xTF32) or 62 (FFMA) useful
+// 5.7 TB/s; a full round of work units 375 (3xTF32) or 62 (FFMA) useful
 // TFLOP/s.  Fitted to the measured 8192^3 layouts within ~2 %.
 namespace {
 
@@ -385,7 +385,7 @@ class HostModel {
         Plan pl;
         make_plan(TG_OP_N, TG_OP_N, rows, cols, K_, 1.0f, al, k4, al, n4, 0.0f, al, n4, path_, 0, sms_, &pl,
                   tf32_, tf32_);
-        const double t = product_seconds(pl, tf32_ ? 355e12 : 62e12);
+        const double t = product_seconds(pl, tf32_ ? 375e12 : 62e12);
         product_s_[{rows, cols}] = t;
         return t;
     }
