@@ -4,7 +4,7 @@ One step = one product through the C ABI (split pre-pass + GEMM kernel [+
 split-K reduce]) with A, B and C resident in HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--path auto|tf32x3|ffma] [--split-k S]
+                  [--workload NAME] [--path auto|tf32x3|ffma|tf32bf16] [--split-k S]
 
 --impl reference times the CPU oracle (the plain fp64 triple loop) on a
 bounded row sample of the same workload.  Under torchrun every rank runs the
@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "tf32x3", "ffma", "tiled"])
+    ap.add_argument("--path", default="auto", choices=["auto", "tf32x3", "ffma", "tiled", "tf32bf16"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--op-a", default="N", choices=["N", "T"], help="A stored transposed (K x M)")
     ap.add_argument("--op-b", default="N", choices=["N", "T"], help="B stored transposed (N x K)")
@@ -61,6 +61,8 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline (profiling runs)")
     ap.add_argument("--no-probes", action="store_true", help="skip the instruction-mix peak probes")
+    ap.add_argument("--no-alt", action="store_true",
+                    help="skip the opt-in tf32 + bf16 cross-product path's line on the headline workload")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the 4096^3 measurement reported beside the 8192^3 headline")
     ap.add_argument("--transpose", action="store_true",
@@ -388,7 +390,7 @@ def run_all_configs(args, local):
         A, B = (t.to(dev) for t in make_inputs(w.M, w.N, w.K, w.dist, w.seed))
         C = torch.empty(w.M, w.N, device=dev)
         auto = tg.plan(w.M, w.N, w.K, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())["path"]
-        for path in ("tf32x3", "ffma") + (("tiled",) if auto == "tiled" else ()):
+        for path in ("tf32x3", "tf32bf16", "ffma") + (("tiled",) if auto == "tiled" else ()):
             plan = tg.plan(w.M, w.N, w.K, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr(), path=path)
             ws = torch.empty(max(1, plan["workspace_bytes"] // 4 + 64), device=dev)
             steps = max(3, min(args.steps, int(2e12 / w.flop) + 3))
@@ -544,6 +546,16 @@ def main():
         peak_note = (f"tf32 dense = {'sustained' if sustained else 'burst'} bf16 of {peak_src} "
                      f"({bf16} TFLOP/s) x 1.1/2.25; three tf32 products per useful FMA -> / 3")
         kernel_tag = "tf32x3_gemm"
+    elif plan["path"] == "tf32bf16":
+        # per useful multiply-add: one tf32 product (hi x hi) and two bf16
+        # products (hi x lo, lo x hi)
+        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        tf32 = bf16 * TF32_OVER_BF16
+        peak = 1.0 / (1.0 / tf32 + 2.0 / bf16)
+        bound = "tensor"
+        peak_note = (f"{'sustained' if sustained else 'burst'} bf16 of {peak_src} ({bf16} TFLOP/s), tf32 = bf16 x "
+                     f"1.1/2.25; one tf32 and two bf16 products per useful FMA -> 1 / (1/tf32 + 2/bf16)")
+        kernel_tag = "tf32bf16_gemm"
     else:
         peak = FFMA_FLOP_PER_CLK * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         bound = "alu"
@@ -594,6 +606,45 @@ def main():
                      "l2": "inputs larger than L2 (A+B = 128 MiB)"}
         del A2, B2, C2, ws2
 
+    # the opt-in tf32 + bf16 cross-product path on the same inputs: throughput,
+    # fraction of its own derived peak, and its error on the oracle's rows
+    alt = None
+    if not args.no_alt and args.path == "auto" and w.name == DEFAULT_WORKLOAD and not general and world == 1:
+        pa = tg.plan(w.M, w.N, w.K, A=Ad.data_ptr(), B=Bd.data_ptr(), C=Cd.data_ptr(), path="tf32bf16")
+        wsa = torch.empty(max(1, pa["workspace_bytes"] // 4 + 64), device=dev)
+        stepsa = max(args.steps, 10)
+        eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(stepsa)]
+        for e0, e1 in eva:
+            e0.record(stream)
+            e1.record(stream)
+        for _ in range(args.warmup):
+            tg.matmul(Ad, Bd, out=Cd, path="tf32bf16", workspace=wsa, stream=stream)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        s0.record(stream)
+        for i in range(stepsa):
+            tg.matmul(Ad, Bd, out=Cd, path="tf32bf16", workspace=wsa, main_begin=eva[i][0], main_end=eva[i][1],
+                      stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        if tg.sync_status() != 0:
+            raise RuntimeError("a kernel reported a timeout on the tf32 + bf16 path")
+        msa = s0.elapsed_time(s1) / stepsa
+        ka = float(np.mean([a.elapsed_time(b) for a, b in eva]))
+        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        peak_a = 1.0 / (1.0 / (bf16 * TF32_OVER_BF16) + 2.0 / bf16)
+        alt = {"path": "tf32bf16", "value": w.flop / (msa * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": msa,
+               "kernel_ms": ka, "kernel_tflops": w.flop / (ka * 1e-3) / 1e12,
+               "roofline_frac": w.flop / (ka * 1e-3) / 1e12 / peak_a, "peak": peak_a, "steps": stepsa,
+               "peak_source": "1 / (1/tf32 + 2/bf16), tf32 = bf16 x 1.1/2.25, bf16 as the main line"}
+        if cpu is not None:
+            got = Cd[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
+            r64 = ref.astype(np.float64)
+            alt["max_rel_error"] = {"normwise_rel": float(np.linalg.norm(got - r64) / np.linalg.norm(r64)),
+                                    "max_abs_over_max_ref": float(np.abs(got - r64).max() / np.abs(r64).max()),
+                                    "rows_checked": len(rows)}
+        del wsa
+
     # ceilings of the two instruction mixes on this GPU (context for the roofline)
     probes = None
     if not args.no_probes:
@@ -638,6 +689,7 @@ def main():
         "clocks": clocks,
         "probes": probes,
         "secondary": secondary,
+        "alt_path": alt,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

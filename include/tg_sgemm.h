@@ -72,9 +72,25 @@ typedef enum tg_op { TG_OP_N = 0, TG_OP_T = 1 } tg_op;
  *    launch (no pre-pass, no split), 64 x 64 tiles, fp32 fused multiply-adds;
  *    operands read in place with any alignment.  A block of 256 threads
  *    handles one tile, so large products run it far below the other paths.
+ *  - TG_PATH_TF32_BF16: the TG_PATH_TF32X3 kernels and split (hi = tf32(x),
+ *    lo = x - hi), with the two cross products taken in bf16: the product is
+ *    hi*hi (kind::tf32) + bf16(hi)*bf16(lo) + bf16(lo)*bf16(hi) (kind::f16,
+ *    bf16 operands, fp32 accumulator).  A cross product is at most 2^-11 of
+ *    the main one, so rounding its operands to bf16's 8 significant bits adds
+ *    at most about 2^-18 of |a*b| per product (3xTF32: about 2^-22); bf16 has
+ *    fp32's exponent range, so no operand scaling is needed.  Two of the
+ *    three products run at bf16 rate: four tensor instructions per 16-wide K
+ *    block instead of six.  Integer inputs with |x| < 2^8 stay exact (lo is
+ *    zero).  Only on request; TG_PATH_AUTO never picks it.
  *  - TG_PATH_AUTO: TG_PATH_TILED for small products (where one launch beats
  *    the three of the 3xTF32 path; see tg_sgemm_plan), else TG_PATH_TF32X3. */
-typedef enum tg_path { TG_PATH_AUTO = 0, TG_PATH_FFMA = 1, TG_PATH_TF32X3 = 2, TG_PATH_TILED = 3 } tg_path;
+typedef enum tg_path {
+    TG_PATH_AUTO = 0,
+    TG_PATH_FFMA = 1,
+    TG_PATH_TF32X3 = 2,
+    TG_PATH_TILED = 3,
+    TG_PATH_TF32_BF16 = 4
+} tg_path;
 
 /* Options for tg_sgemm_ex.  Zero-initialise and set what you need.
  *  path            tg_path value.
@@ -99,7 +115,7 @@ typedef struct tg_sgemm_opts {
 
 /* What one call would launch (filled by tg_sgemm_plan). */
 typedef struct tg_plan_info {
-    int path;          /* TG_PATH_FFMA, TG_PATH_TF32X3 or TG_PATH_TILED */
+    int path;          /* TG_PATH_FFMA, TG_PATH_TF32X3, TG_PATH_TILED or TG_PATH_TF32_BF16 */
     int split_k;       /* K slices */
     int block_m, block_n, block_k, stages; /* CTA tile and pipeline depth */
     int tiles_m, tiles_n;

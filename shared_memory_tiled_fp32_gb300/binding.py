@@ -22,7 +22,7 @@ STATUS = {
     5: "TG_ERR_TIMEOUT",
     6: "TG_ERR_WORKSPACE_TOO_SMALL",
 }
-PATHS = {"auto": 0, "ffma": 1, "tf32x3": 2, "tiled": 3}
+PATHS = {"auto": 0, "ffma": 1, "tf32x3": 2, "tiled": 3, "tf32bf16": 4}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Every symbol the headers in include/ declare.

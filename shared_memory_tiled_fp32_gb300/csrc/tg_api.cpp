@@ -111,7 +111,7 @@ void fill_info(const Plan& p, tg_plan_info* out) {
     out->tiles_n = p.tiles_n;
     out->units = p.units;
     out->grid = p.grid;
-    out->prepass = (p.path == TG_PATH_TF32X3 && !p.zero_fill && p.M > 0 && p.N > 0) || p.pack_a || p.pack_b;
+    out->prepass = (tensor_path(p.path) && !p.zero_fill && p.M > 0 && p.N > 0) || p.pack_a || p.pack_b;
     out->launches = p.launches;
     out->workspace_bytes = p.ws_bytes;
     out->pair = p.pair;
@@ -154,7 +154,7 @@ const char* tg_status_string(tg_status s) {
     return "unknown tg_status";
 }
 
-int tg_sgemm_version(void) { return 102; }
+int tg_sgemm_version(void) { return 103; }
 
 tg_status tg_sgemm_plan_general(int op_a, int op_b, int M, int N, int K, const void* A, int lda,
                                 const void* B, int ldb, const void* C, int ldc, int path,
@@ -280,7 +280,7 @@ void host_block_cols(const tg::HostBlocks& hb, int N, int i, int j, int* j0, int
 
 HostBytes host_bytes(const tg::HostBlocks& hb, int M, int N, int K, int path, int split_k, int num_sms) {
     using namespace tg;
-    const bool tf32 = path == TG_PATH_TF32X3;
+    const bool tf32 = tensor_path(path);
     const long long k4 = ((long long)std::max(K, 1) + 3) / 4 * 4, n4 = ((long long)N + 3) / 4 * 4;
     const long long k16 = ((long long)std::max(K, 1) + 15) / 16 * 16;
     auto align = [](size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; };
@@ -325,8 +325,8 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
     if (st != TG_OK) return st;
     std::lock_guard<std::mutex> lock(hp->mu);  // one host-buffer call per device at a time
 
-    const int path = o.path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3;
-    const bool tf32 = path == TG_PATH_TF32X3;
+    const int path = o.path == TG_PATH_FFMA || o.path == TG_PATH_TF32_BF16 ? o.path : TG_PATH_TF32X3;
+    const bool tf32 = tensor_path(path);
     const long long k4 = ((long long)std::max(K, 1) + 3) / 4 * 4, n4 = ((long long)N + 3) / 4 * 4;
     // Output blocks: C is cut into row blocks, the first ones also into
     // column blocks, so the first product needs only A_0 and B_0 on the
@@ -455,7 +455,8 @@ tg_status tg_sgemm_host_device_bytes(int M, int N, int K, int path, int split_k,
                                      size_t* product_workspace) {
     using namespace tg;
     if (M < 0 || N < 0 || K < 0 || split_k < 0 || total == nullptr) return TG_ERR_INVALID_VALUE;
-    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3) return TG_ERR_INVALID_VALUE;
+    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3 && path != TG_PATH_TF32_BF16)
+        return TG_ERR_INVALID_VALUE;
     if (num_sms <= 0) {
         DeviceState* d = nullptr;
         const tg_status st = current_device(&d);
@@ -465,7 +466,7 @@ tg_status tg_sgemm_host_device_bytes(int M, int N, int K, int path, int split_k,
     *total = 0;
     if (product_workspace != nullptr) *product_workspace = 0;
     if (M == 0 || N == 0) return TG_OK;
-    const int p = path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3;
+    const int p = path == TG_PATH_FFMA || path == TG_PATH_TF32_BF16 ? path : TG_PATH_TF32X3;
     const HostBytes b = host_bytes(choose_host_blocks(M, N, K, p, num_sms), M, N, K, p, split_k, num_sms);
     *total = b.total();
     if (product_workspace != nullptr) *product_workspace = b.ws_max;
@@ -475,14 +476,16 @@ tg_status tg_sgemm_host_device_bytes(int M, int N, int K, int path, int split_k,
 tg_status tg_sgemm_host_blocks(int M, int N, int K, int path, int num_sms, tg_host_blocks_info* out) {
     using namespace tg;
     if (M < 0 || N < 0 || K < 0 || out == nullptr) return TG_ERR_INVALID_VALUE;
-    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3) return TG_ERR_INVALID_VALUE;
+    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3 && path != TG_PATH_TF32_BF16)
+        return TG_ERR_INVALID_VALUE;
     if (num_sms <= 0) {
         DeviceState* d = nullptr;
         const tg_status st = current_device(&d);
         if (st != TG_OK) return st;
         num_sms = d->num_sms;
     }
-    const HostBlocks hb = choose_host_blocks(M, N, K, path == TG_PATH_FFMA ? TG_PATH_FFMA : TG_PATH_TF32X3, num_sms);
+    const HostBlocks hb = choose_host_blocks(
+        M, N, K, path == TG_PATH_FFMA || path == TG_PATH_TF32_BF16 ? path : TG_PATH_TF32X3, num_sms);
     out->row_blocks = hb.pm;
     out->col_blocks = hb.pn;
     out->first_block_rows = hb.first;

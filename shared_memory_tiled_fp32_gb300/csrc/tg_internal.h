@@ -9,6 +9,10 @@
 
 namespace tg {
 
+// The tensor-core paths (3xTF32 and its bf16-cross-product variant) share
+// the plan, the pre-pass tiles and the GEMM kernel.
+inline bool tensor_path(int path) { return path == TG_PATH_TF32X3 || path == TG_PATH_TF32_BF16; }
+
 // CTA tile shapes of the two math paths.
 //
 // TF32x3: a 128 x 256 output tile per CTA (a 256 x 256 tile per CTA pair;

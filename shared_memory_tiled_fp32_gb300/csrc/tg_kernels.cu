@@ -15,6 +15,7 @@
 //    from global memory (warp-uniform role split by warp index, as in the
 //    pages' divergence-free branching by warp number).
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -522,7 +523,10 @@ struct TfRing {
 constexpr size_t kTfSmemBytes = TfRing<false>::kSmemBytes;
 constexpr size_t kTfSmemBytesPairMma = TfRing<true>::kSmemBytes;
 
-template <int kPair, bool kPairMma>
+// kMixed: the operand tiles hold tf32 hi and bf16 hi / lo (the pre-pass's
+// kSplitBf16 layout) and each 16-wide K block takes two tf32 hi x hi products
+// and two bf16 cross products (hi x lo, lo x hi) instead of six tf32 ones.
+template <int kPair, bool kPairMma, bool kMixed = false>
 __global__ void __launch_bounds__(kTfThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        GemmArgs args) {
@@ -651,6 +655,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             }
         } else if (warp == 1 && lane == 0 && issuer) {  // ---------------- MMA issuer
             constexpr uint32_t idesc = idesc_tf32(kPairMma ? 2 * BM : BM, BN);
+            constexpr uint32_t idesc_x = idesc_bf16(kPairMma ? 2 * BM : BM, BN);
             static_assert(BK == 16 && kTfRowBytes == 128, "the issue loop below is written for two 8-wide slices");
             const uint64_t desc_stage0 = smem_desc_kmajor(smem_addr(smem), kSwRowGroupBytes, kDescSwizzle128);
             int stage = 0;
@@ -678,6 +683,31 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         // is +4 and the second 8-wide K slice +2
                         const uint64_t da = desc_stage0 + (uint64_t)stage * (kStageBytes >> 4);
                         const uint64_t db = da + (kTfAStage >> 4);
+                        if (kMixed) {
+                            // bf16 hi at +4 (K 0-15 in one 32-byte slice), bf16 lo at +6
+                            const uint32_t acc = kb > c0 ? 1u : 0u;
+                            if (kPairMma) {
+                                mma_f16_ss_pair(d_tmem, da + 4, db + 6, idesc_x, acc);
+                                mma_f16_ss_pair(d_tmem, da + 6, db + 4, idesc_x, 1u);
+                                mma_tf32_ss_pair(d_tmem, da, db, idesc, 1u);
+                                mma_tf32_ss_pair(d_tmem, da + 2, db + 2, idesc, 1u);
+                                mma_commit_pair(&empty[stage], kPairMask);
+                            } else {
+                                mma_f16_ss(d_tmem, da + 4, db + 6, idesc_x, acc);
+                                mma_f16_ss(d_tmem, da + 6, db + 4, idesc_x, 1u);
+                                mma_tf32_ss(d_tmem, da, db, idesc, 1u);
+                                mma_tf32_ss(d_tmem, da + 2, db + 2, idesc, 1u);
+                                if (kPair > 1)
+                                    mma_commit_multicast(&empty[stage], kPairMask);
+                                else
+                                    mma_commit(&empty[stage]);
+                            }
+                            if (++stage == ST) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                            continue;
+                        }
                         if (kPairMma) {  // M = 256 over the pair: each CTA's A rows and B half
                             const uint32_t acc = kb > c0 ? 1u : 0u;
                             mma_tf32_ss_pair(d_tmem, da, db + 4, idesc, acc);
@@ -879,34 +909,72 @@ __device__ __forceinline__ float4 load_row4(const float* src, long long ld, int 
     return v;
 }
 
-// Offset of destination element (r, c): hi of the interleaved layout (SPLIT)
-// or the plain padded row (PACK).
-// Offset of destination element (r, c): hi in its swizzled tile (SPLIT; the
-// lo value sits at offset ^ 16, its 16-byte group j + 4 swizzled the same
-// way) or the plain padded row (PACK).
-template <bool SPLIT>
+// Pre-pass modes: kPack copies (FFMA: op(A) -> [M][k4], op(B) -> [K][n4]);
+// kSplitTf32 writes hi = tf32(x) and lo = tf32(x - hi) (3xTF32); kSplitBf16
+// writes hi = tf32(x) and the bf16 roundings of hi and of x - hi (the
+// bf16-cross-product path).  Both split modes fill 128-byte tile rows of
+// eight 16-byte groups, group g of row r stored at position g ^ (r % 8):
+// kSplitTf32: groups 0-3 hi of K values 4g..4g+3, groups 4-7 their lo;
+// kSplitBf16: groups 0-3 hi (tf32), group 4 / 5 bf16(hi) of K values 0-7 /
+// 8-15, group 6 / 7 bf16(lo) of the same.
+constexpr int kPack = 0, kSplitTf32 = 1, kSplitBf16 = 2;
+
+// Offset of destination element (r, c): hi in its swizzled tile (split
+// modes) or the plain padded row (kPack).
+template <int MODE>
 __device__ __forceinline__ long long dst_offset(int pitch, int r, int c) {
-    if (SPLIT)
+    if (MODE != kPack)
         return ((long long)(r >> 7) * (pitch >> 4) + (c >> 4)) * 4096 + (r & 127) * 32 +
                ((((c & 15) >> 2) ^ (r & 7)) << 2) + (c & 3);
     return (long long)r * pitch + c;
 }
 
-// Store destination columns c..c+3 of a row (c a multiple of 4: one 16-byte
+// kSplitBf16: float offset of the bf16 value(s) of K index c (row r) in
+// logical group `first` (4: bf16 hi, 6: bf16 lo) of the row whose hi group
+// sits at offset o.
+__device__ __forceinline__ long long bf16_offset(long long o, int r, int c, int first) {
+    const int j = (c & 15) >> 2;
+    return (o & ~31ll) + (((first + (j >> 1)) ^ (r & 7)) << 2) + ((j & 1) << 1);
+}
+
+// hi of the split: x rounded to tf32 (nearest, ties away), or truncated where
+// that rounding would carry one of the largest finite values to infinity.
+__device__ __forceinline__ float split_hi(float x) {
+    const float h = to_tf32(x);
+    return (isinf(h) && !isinf(x)) ? __uint_as_float(__float_as_uint(x) & 0xffffe000u) : h;
+}
+
+// x rounded to bf16 (nearest even), truncated where that would overflow.
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return __bfloat16_as_ushort((__hisinf(b) && !isinf(x)) ? __float2bfloat16_rz(x) : b);
+}
+
+__device__ __forceinline__ uint2 to_bf16x4(float a, float b, float c, float d) {
+    return make_uint2(bf16_bits(a) | (bf16_bits(b) << 16), bf16_bits(c) | (bf16_bits(d) << 16));
+}
+
+// Store destination columns c..c+3 of row r (c a multiple of 4: one 16-byte
 // group) at offset o.
-template <bool SPLIT>
-__device__ __forceinline__ void store_split4(float* d0, long long o, float4 x) {
-    if (SPLIT) {
-        const float4 hi = make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
-        *reinterpret_cast<float4*>(d0 + o) = hi;
+template <int MODE>
+__device__ __forceinline__ void store_split4(float* d0, long long o, float4 x, int r, int c) {
+    if (MODE == kPack) {
+        *reinterpret_cast<float4*>(d0 + o) = x;
+        return;
+    }
+    const float4 hi = make_float4(split_hi(x.x), split_hi(x.y), split_hi(x.z), split_hi(x.w));
+    *reinterpret_cast<float4*>(d0 + o) = hi;
+    if (MODE == kSplitTf32) {
         *reinterpret_cast<float4*>(d0 + (o ^ 16)) =
             make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
     } else {
-        *reinterpret_cast<float4*>(d0 + o) = x;
+        *reinterpret_cast<uint2*>(d0 + bf16_offset(o, r, c, 4)) = to_bf16x4(hi.x, hi.y, hi.z, hi.w);
+        *reinterpret_cast<uint2*>(d0 + bf16_offset(o, r, c, 6)) =
+            to_bf16x4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
     }
 }
 
-template <bool SPLIT>
+template <int MODE>
 __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
     constexpr int kInFlight = 8;  // 16-byte loads issued before the first store
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -914,6 +982,7 @@ __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < p.items; i += kInFlight * stride) {
         float4 v[kInFlight];
         long long o[kInFlight];
+        int rr[kInFlight], cc[kInFlight];
 #pragma unroll
         for (int u = 0; u < kInFlight; ++u) {
             const long long it = i + u * stride;
@@ -922,12 +991,14 @@ __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
                 const int r = (int)(it / groups), c = (int)(it % groups) * 4;
                 v[u] = r < p.rows_valid ? load_row4(p.src, p.ld, r, c, p.cols, p.vec != 0)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                o[u] = dst_offset<SPLIT>(p.pitch, r, c);
+                o[u] = dst_offset<MODE>(p.pitch, r, c);
+                rr[u] = r;
+                cc[u] = c;
             }
         }
 #pragma unroll
         for (int u = 0; u < kInFlight; ++u)
-            if (o[u] >= 0) store_split4<SPLIT>(p.d0, o[u], v[u]);
+            if (o[u] >= 0) store_split4<MODE>(p.d0, o[u], v[u], rr[u], cc[u]);
     }
 }
 
@@ -945,7 +1016,7 @@ __device__ __forceinline__ void transpose_load(const OperandPass& p, long long t
 // The tiles are software-pipelined: the loads of a block's next tile are
 // issued before the stores of the current one, so reads stay in flight while
 // the block writes.
-template <bool SPLIT>
+template <int MODE>
 __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*tile)[65]) {
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4 threads
     long long t = blockIdx.x;
@@ -964,13 +1035,20 @@ __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*til
             const int r = r0 + ty + 4 * j, c = c0 + tx;
             if (r < p.rows && c < p.pitch) {
                 const float x = tile[tx][ty + 4 * j];
-                const long long o = dst_offset<SPLIT>(p.pitch, r, c);
-                if (SPLIT) {
-                    const float hi = to_tf32(x);
-                    p.d0[o] = hi;
-                    p.d0[o ^ 16] = to_tf32(x - hi);
-                } else {
+                const long long o = dst_offset<MODE>(p.pitch, r, c);
+                if (MODE == kPack) {
                     p.d0[o] = x;
+                } else {
+                    const float hi = split_hi(x);
+                    p.d0[o] = hi;
+                    if (MODE == kSplitTf32) {
+                        p.d0[o ^ 16] = to_tf32(x - hi);
+                    } else {  // one bf16 of each, element c % 4 of its 8-byte run
+                        __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, r, c, 4));
+                        __nv_bfloat16* lb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, r, c, 6));
+                        hb[c & 3] = __ushort_as_bfloat16((unsigned short)bf16_bits(hi));
+                        lb[c & 3] = __ushort_as_bfloat16((unsigned short)bf16_bits(x - hi));
+                    }
                 }
             }
         }
@@ -978,22 +1056,22 @@ __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*til
     }
 }
 
-template <bool SPLIT>
+template <int MODE>
 __global__ void __launch_bounds__(256) prepass_kernel(PrepassArgs a) {
     __shared__ float tile[64][65];
     grid_dep_launch();  // the GEMM may start its set-up as this pass drains
     // A, then B (constant indices: the arguments stay in parameter space)
     if (a.op[0].d0 != nullptr) {
         if (a.op[0].trans)
-            transpose_pass<SPLIT>(a.op[0], tile);
+            transpose_pass<MODE>(a.op[0], tile);
         else
-            rowwise_pass<SPLIT>(a.op[0]);
+            rowwise_pass<MODE>(a.op[0]);
     }
     if (a.op[1].d0 != nullptr) {
         if (a.op[1].trans)
-            transpose_pass<SPLIT>(a.op[1], tile);
+            transpose_pass<MODE>(a.op[1], tile);
         else
-            rowwise_pass<SPLIT>(a.op[1]);
+            rowwise_pass<MODE>(a.op[1]);
     }
 }
 
@@ -1351,7 +1429,7 @@ tg_status launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 
 // Resident 256-thread blocks per SM of the two pre-pass kernels (the grid is
 // sized to exactly fill the GPU once).
-int g_prepass_blocks_per_sm[2] = {4, 4};
+int g_prepass_blocks_per_sm[3] = {4, 4, 4};
 // CTA pairs of the 3xTF32 kernel resident at once (0 = unknown).
 int g_tf32_pair_clusters = 0;
 
@@ -1367,10 +1445,14 @@ bool pair_mma_enabled() {
 
 tg_status prepare_device_kernels() {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<false>, 256, 0) == cudaSuccess && nb > 0)
-        g_prepass_blocks_per_sm[0] = nb;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<true>, 256, 0) == cudaSuccess && nb > 0)
-        g_prepass_blocks_per_sm[1] = nb;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<kPack>, 256, 0) == cudaSuccess && nb > 0)
+        g_prepass_blocks_per_sm[kPack] = nb;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<kSplitTf32>, 256, 0) == cudaSuccess &&
+        nb > 0)
+        g_prepass_blocks_per_sm[kSplitTf32] = nb;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<kSplitBf16>, 256, 0) == cudaSuccess &&
+        nb > 0)
+        g_prepass_blocks_per_sm[kSplitBf16] = nb;
     // The warpgroup register splits of both GEMM kernels only balance when the
     // kernels are launched with exactly the register counts they were designed
     // for; refuse to run a build that differs.
@@ -1385,7 +1467,10 @@ tg_status prepare_device_kernels() {
         size_t smem;
     } tf_kernels[] = {{tf32x3_gemm_kernel<1, false>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, false>, kTfSmemBytes},
-                      {tf32x3_gemm_kernel<2, true>, kTfSmemBytesPairMma}};
+                      {tf32x3_gemm_kernel<2, true>, kTfSmemBytesPairMma},
+                      {tf32x3_gemm_kernel<1, false, true>, kTfSmemBytes},
+                      {tf32x3_gemm_kernel<2, false, true>, kTfSmemBytes},
+                      {tf32x3_gemm_kernel<2, true, true>, kTfSmemBytesPairMma}};
     for (const auto& k : tf_kernels) {
         if (cudaFuncGetAttributes(&fa, k.kern) != cudaSuccess) return TG_ERR_CUDA;
         if (fa.numRegs != kTfLaunchRegs) return TG_ERR_CUDA;
@@ -1497,16 +1582,21 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     };
     PrepassArgs pa{};
     // one full wave of resident blocks keeps HBM busy without a tail
-    const int prepass_grid = g_prepass_blocks_per_sm[p.path == TG_PATH_TF32X3 ? 1 : 0] * p.num_sms;
+    const bool mixed = p.path == TG_PATH_TF32_BF16;
+    const int mode = mixed ? kSplitBf16 : (p.path == TG_PATH_TF32X3 ? kSplitTf32 : kPack);
+    const int prepass_grid = g_prepass_blocks_per_sm[mode] * p.num_sms;
 
-    if (p.path == TG_PATH_TF32X3) {
+    if (tensor_path(p.path)) {
         float* a_tiles = p.ext_a ? p.ext_a : reinterpret_cast<float*>(w + p.off_a0);
         float* b_tiles = p.ext_b ? p.ext_b : reinterpret_cast<float*>(w + p.off_b0);
         // split tiles: A [a_rows/128][k16/16] from op(A); B [b_rows/128][k16/16] from op(B)^T
         pa.op[0] = pass(A, p.lda, p.M, p.K, p.k16, p.op_a == TG_OP_T, p.a_ready ? nullptr : a_tiles, p.a_rows);
         pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, p.b_ready ? nullptr : b_tiles, p.b_rows);
         if (!(p.a_ready && p.b_ready)) {
-            prepass_kernel<true><<<prepass_grid, 256, 0, stream>>>(pa);
+            if (mixed)
+                prepass_kernel<kSplitBf16><<<prepass_grid, 256, 0, stream>>>(pa);
+            else
+                prepass_kernel<kSplitTf32><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
         }
         ga.a_tiles = a_tiles;
@@ -1523,22 +1613,17 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
             (!make_map(&mA, a_tiles, 32, (uint64_t)p.a_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
              !make_map(&mB, b_tiles, 32, (uint64_t)p.b_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
             return TG_ERR_CUDA;
-        if (p.pair == 2) {
-            int clusters = p.grid / 2;
-            if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
-            if (pair_mma) {
-                if (launch_dependent(tf32x3_gemm_kernel<2, true>, dim3(2 * clusters), dim3(kTfThreads),
-                                     kTfSmemBytesPairMma, stream, 2, mA, mB, ga) != TG_OK)
-                    return TG_ERR_CUDA;
-            } else if (launch_dependent(tf32x3_gemm_kernel<2, false>, dim3(2 * clusters), dim3(kTfThreads),
-                                        kTfSmemBytes, stream, 2, mA, mB, ga) != TG_OK) {
-                return TG_ERR_CUDA;
-            }
-        } else {
-            if (launch_dependent(tf32x3_gemm_kernel<1, false>, dim3(p.grid), dim3(kTfThreads), kTfSmemBytes, stream,
-                                 1, mA, mB, ga) != TG_OK)
-                return TG_ERR_CUDA;
-        }
+        int clusters = p.grid / 2;
+        if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
+        void (*kern)(CUtensorMap, CUtensorMap, GemmArgs);
+        if (p.pair == 2)
+            kern = pair_mma ? (mixed ? tf32x3_gemm_kernel<2, true, true> : tf32x3_gemm_kernel<2, true>)
+                            : (mixed ? tf32x3_gemm_kernel<2, false, true> : tf32x3_gemm_kernel<2, false>);
+        else
+            kern = mixed ? tf32x3_gemm_kernel<1, false, true> : tf32x3_gemm_kernel<1, false>;
+        if (launch_dependent(kern, dim3(p.pair == 2 ? 2 * clusters : p.grid), dim3(kTfThreads),
+                             pair_mma ? kTfSmemBytesPairMma : kTfSmemBytes, stream, p.pair, mA, mB, ga) != TG_OK)
+            return TG_ERR_CUDA;
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
     } else {
         const float* a_src = A;
@@ -1550,7 +1635,7 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
             float* bp = p.pack_b ? reinterpret_cast<float*>(w + p.off_b0) : nullptr;
             pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, ap, p.M);
             pa.op[1] = pass(B, p.ldb, p.K, p.N, p.n4, p.op_b == TG_OP_T, bp, p.K);
-            prepass_kernel<false><<<prepass_grid, 256, 0, stream>>>(pa);
+            prepass_kernel<kPack><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
             if (p.pack_a) {
                 a_src = ap;

@@ -73,7 +73,8 @@ tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int l
     const int b_rows = op_b == TG_OP_N ? K : N, b_cols = op_b == TG_OP_N ? N : K;
     if (lda < std::max(1, a_cols) || ldb < std::max(1, b_cols) || ldc < std::max(1, N))
         return TG_ERR_INVALID_VALUE;
-    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3 && path != TG_PATH_TILED)
+    if (path != TG_PATH_AUTO && path != TG_PATH_FFMA && path != TG_PATH_TF32X3 && path != TG_PATH_TILED &&
+        path != TG_PATH_TF32_BF16)
         return TG_ERR_INVALID_VALUE;
     if (split_k < 0) return TG_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return TG_OK;  // nothing is read or written
@@ -109,14 +110,14 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     p->alpha = alpha;
     p->beta = beta;
     p->num_sms = num_sms;
-    if (path == TG_PATH_FFMA || path == TG_PATH_TILED)
+    if (path == TG_PATH_FFMA || path == TG_PATH_TILED || path == TG_PATH_TF32_BF16)
         p->path = path;
     else if (path == TG_PATH_AUTO && split_k <= 1 && tiled_is_faster(M, N, K, num_sms))
         p->path = TG_PATH_TILED;
     else
         p->path = TG_PATH_TF32X3;
     p->vec_c = C != nullptr && (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
-    if (p->path == TG_PATH_TF32X3) {
+    if (tensor_path(p->path)) {
         p->bm = kTf32BM; p->bn = kTf32BN; p->bk = kTf32BK; p->stages = kTf32Stages;
     } else if (p->path == TG_PATH_FFMA) {
         p->bm = kFfmaBM; p->bn = kFfmaBN; p->bk = kFfmaBK; p->stages = kFfmaStages;
@@ -164,7 +165,7 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     // halves the B traffic from L2.  TG_TF32X3_PAIR=0 turns this off.
     const char* pair_env = std::getenv("TG_TF32X3_PAIR");
     const bool pair_off = pair_env != nullptr && std::strcmp(pair_env, "0") == 0;
-    p->pair = (p->path == TG_PATH_TF32X3 && p->tiles_m >= 2 && num_sms >= 2 && !pair_off) ? 2 : 1;
+    p->pair = (tensor_path(p->path) && p->tiles_m >= 2 && num_sms >= 2 && !pair_off) ? 2 : 1;
     p->units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n * S;
     const long long cap = num_sms / p->pair;  // units in flight at once (lanes)
     p->grid = p->pair * (int)std::min<long long>(p->units, cap);
@@ -233,7 +234,7 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         off = round_up(off + bytes, kWsAlign);
         return at;
     };
-    if (p->path == TG_PATH_TF32X3) {
+    if (tensor_path(p->path)) {
         // split tiles of 128 rows x (16 hi + 16 lo): A's rows padded to whole
         // units (pair x 128), B^T's to whole 256-row B tiles
         p->a_rows = (int)round_up((size_t)M, 128 * (size_t)p->pair);
@@ -262,7 +263,7 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->off_tail = take(4ull * slots * p->pair * p->bm * p->bn);
     }
     p->ws_bytes = off;
-    const bool prepass = p->path == TG_PATH_TF32X3 || p->pack_a || p->pack_b;
+    const bool prepass = tensor_path(p->path) || p->pack_a || p->pack_b;
     p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_lanes > 0 ? 1 : 0);
 }
 
@@ -385,7 +386,7 @@ class HostModel {
         Plan pl;
         make_plan(TG_OP_N, TG_OP_N, rows, cols, K_, 1.0f, al, k4, al, n4, 0.0f, al, n4, path_, 0, sms_, &pl,
                   tf32_, tf32_);
-        const double t = product_seconds(pl, tf32_ ? 375e12 : 62e12);
+        const double t = product_seconds(pl, path_ == TG_PATH_TF32_BF16 ? 525e12 : (tf32_ ? 375e12 : 62e12));
         product_s_[{rows, cols}] = t;
         return t;
     }

@@ -48,7 +48,7 @@ static int cpu_checks(void) {
     CHECK(info.path == TG_PATH_TF32X3 && info.tiles_m == 64 && info.tiles_n == 32 && info.grid == 152,
           "plan fields");
     CHECK(strncmp(tg_status_string(TG_ERR_TIMEOUT), "TG_ERR_TIMEOUT", 14) == 0, "status string");
-    CHECK(tg_sgemm_version() == 102, "version");
+    CHECK(tg_sgemm_version() == 103, "version");
     return 0;
 }
 

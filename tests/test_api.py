@@ -32,7 +32,7 @@ def test_library_exports_header_symbols():
 
 
 def test_version_and_status_strings():
-    assert tg.lib().tg_sgemm_version() == 102
+    assert tg.lib().tg_sgemm_version() == 103
     for code, name in tg.STATUS.items():
         assert tg.status_string(code).startswith(name)
 
@@ -133,6 +133,12 @@ def test_plan_tiles_split_and_workspace():
     assert tg.plan(512, 512, 512, num_sms=sms)["path"] == "tf32x3"    # 2^27 multiply-adds
     assert tg.plan(64, 64, 8192, num_sms=sms)["path"] == "tf32x3"     # long K: split instead
     assert tg.plan(777, 1029, 513, num_sms=sms, path="tiled")["tiles_m"] == 13
+    # the tf32 + bf16 cross-product path only on request, with the 3xTF32
+    # tiles, workspace and launches (its split tiles have the same size)
+    for shape in [(8192, 8192, 8192), (777, 1029, 513), (4000, 3900, 8000), (64, 64, 8192)]:
+        x, m = tg.plan(*shape, num_sms=sms, path="tf32x3"), tg.plan(*shape, num_sms=sms, path="tf32bf16")
+        assert m["path"] == "tf32bf16" and tg.plan(*shape, num_sms=sms)["path"] != "tf32bf16"
+        assert {k: v for k, v in m.items() if k != "path"} == {k: v for k, v in x.items() if k != "path"}
 
 
 def _split_point_pieces(U, nkb, L, kx, slots):

@@ -56,6 +56,10 @@ CASES = [
     ("longk_2048x2048x16384_normal", "tf32x3", 4), ("longk_2048x2048x16384_normal", "ffma", 0),
     ("sq256_uniform", "tiled", 0), ("sq256_int", "tiled", 0), ("ragged_777x1029x513", "tiled", 0),
     ("sq4096_int", "tiled", 0), ("sq4096_uniform", "auto", 0), ("sq256_uniform", "auto", 0),
+    ("sq256_uniform", "tf32bf16", 0), ("sq256_int", "tf32bf16", 0), ("sq256_int", "tf32bf16", 1),
+    ("ragged_777x1029x513", "tf32bf16", 0), ("ragged_777x1029x513", "tf32bf16", 3),
+    ("sq4096_uniform", "tf32bf16", 0), ("sq4096_int", "tf32bf16", 0), ("sq8192_normal", "tf32bf16", 0),
+    ("longk_2048x2048x16384_normal", "tf32bf16", 0), ("longk_2048x2048x16384_normal", "tf32bf16", 4),
 ]
 
 
@@ -71,7 +75,7 @@ def test_workload(tg, name, path, split):
         assert_close(got, ref, w.K, f"{name} {path} split {split}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled", "tf32bf16"])
 def test_ragged_random_shapes(tg, path):
     """Shapes around tile edges and random shapes in [1, 300]^3."""
     rng = np.random.default_rng(7)
@@ -84,7 +88,7 @@ def test_ragged_random_shapes(tg, path):
         assert_close(run(tg, A, B, path=path), ref, K, f"{path} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled", "tf32bf16"])
 def test_integer_random_shapes_bitexact(tg, path):
     rng = np.random.default_rng(8)
     for i in range(6):
@@ -95,7 +99,7 @@ def test_integer_random_shapes_bitexact(tg, path):
             assert_bitexact(run(tg, A, B, path=path, split_k=split), ref, f"{path} {M}x{N}x{K} s{split}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled", "tf32bf16"])
 @pytest.mark.parametrize("split", [0, 1, 2])
 def test_strided_unaligned_views_and_canaries(tg, path, split):
     """Odd leading dimensions, unaligned base pointers (sub-views at odd
@@ -129,7 +133,7 @@ def test_strided_unaligned_views_and_canaries(tg, path, split):
 
 def test_k_zero_and_empty(tg):
     dev = torch.device("cuda")
-    for path in ("tf32x3", "ffma", "tiled"):
+    for path in ("tf32x3", "ffma", "tiled", "tf32bf16"):
         C = torch.empty(5, 7, device=dev)
         fill_sentinel(C)
         tg.matmul(torch.empty(5, 0, device=dev), torch.empty(0, 7, device=dev), out=C, path=path)
@@ -147,11 +151,34 @@ def test_nan_row_propagates(tg):
     A[3, 17] = float("nan")
     ref = oracle.sgemm(A.numpy(), B.numpy())
     assert np.all(np.isnan(ref[3]))
-    for path in ("tf32x3", "ffma", "tiled"):
+    for path in ("tf32x3", "ffma", "tiled", "tf32bf16"):
         C = run(tg, A, B, path=path)
         assert np.all(np.isnan(C[3])), path
         keep = np.arange(M) != 3
         assert_close(C[keep], ref[keep], K, f"nan row {path}")
+
+
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled", "tf32bf16"])
+def test_operands_near_float_max(tg, path):
+    """Finite operands within 2^-11 of the largest float, times small ones:
+    every product and sum is finite, so C must be too.  Rounding such a value
+    to tf32 (or bf16) to nearest would carry it to infinity; the split
+    truncates it instead."""
+    M, N, K = 130, 260, 40
+    rng = np.random.default_rng(77)
+    fmax = np.finfo(np.float32).max
+    A = (rng.uniform(0.9996, 1.0, (M, K)) * fmax * rng.choice([-1.0, 1.0], (M, K))).astype(np.float32)
+    A[:, ::3] = rng.uniform(-1, 1, (M, (K + 2) // 3)).astype(np.float32)  # mixed with ordinary values
+    B = (rng.uniform(-1, 1, (K, N)) * 2.0 ** -100).astype(np.float32)
+    # large values in A (split row by row) and, transposed, in B (split by the
+    # transposing pass)
+    for X, Y in [(A, B), (np.ascontiguousarray(B.T), np.ascontiguousarray(A.T))]:
+        X, Y = torch.from_numpy(X), torch.from_numpy(Y)
+        ref = oracle.sgemm(X.numpy(), Y.numpy())
+        assert np.all(np.isfinite(ref))
+        C = run(tg, X, Y, path=path)
+        assert np.all(np.isfinite(C)), path
+        assert_close(C, ref, K, f"near FLT_MAX {path} {tuple(X.shape)}")
 
 
 def test_deterministic(tg):
@@ -292,8 +319,9 @@ def test_plan_on_device(tg):
     assert p["path"] == "tf32x3"
 
 
+@pytest.mark.parametrize("path", ["tf32x3", "tf32bf16"])
 @pytest.mark.parametrize("pair,pair_mma", [("0", "1"), ("1", "0"), ("1", "1")])
-def test_tf32x3_cluster_pairs_on_and_off(tg, pair, pair_mma, monkeypatch):
+def test_tf32x3_cluster_pairs_on_and_off(tg, pair, pair_mma, path, monkeypatch):
     """The three forms of the 3xTF32 kernel: one CTA per tile; CTA pairs with
     one M = 128 product per CTA and B multicast to both; CTA pairs with one
     M = 256 product over both (cta_group::2, each CTA holding its half of B)
@@ -305,18 +333,19 @@ def test_tf32x3_cluster_pairs_on_and_off(tg, pair, pair_mma, monkeypatch):
                                    (1000, 3000, 1100)]):
         A, B = make_inputs(M, N, K, "uniform", 900 + i)
         ref = oracle.sgemm(A.numpy(), B.numpy())
-        p = tg.plan(M, N, K, path="tf32x3")
-        assert p["tiles_m"] == -(-M // 128)
+        p = tg.plan(M, N, K, path=path)
+        assert p["tiles_m"] == -(-M // 128) and p["path"] == path
         for split in (0, 1, 2):
-            assert_close(run(tg, A, B, path="tf32x3", split_k=split), ref, K,
-                         f"pair={pair} mma={pair_mma} {M}x{N}x{K} s{split}")
+            assert_close(run(tg, A, B, path=path, split_k=split), ref, K,
+                         f"{path} pair={pair} mma={pair_mma} {M}x{N}x{K} s{split}")
     A, B = make_inputs(1000, 3000, 1100, "int", 911)
-    assert_bitexact(run(tg, A, B, path="tf32x3"), oracle.sgemm(A.numpy(), B.numpy()), "pair forms, integers")
+    assert_bitexact(run(tg, A, B, path=path), oracle.sgemm(A.numpy(), B.numpy()), f"{path} pair forms, integers")
 
 
 TAIL_CASES = [(1000, 3000, 1100, "uniform", "tf32x3"), (1000, 3000, 1100, "int", "tf32x3"),
               (4000, 3900, 8000, "uniform", "tf32x3"), (400, 8000, 20000, "normal", "tf32x3"),
-              (400, 8000, 20000, "int", "tf32x3"), (1000, 3000, 1100, "uniform", "ffma"),
+              (400, 8000, 20000, "int", "tf32x3"), (1000, 3000, 1100, "uniform", "tf32bf16"),
+              (400, 8000, 20000, "int", "tf32bf16"), (1000, 3000, 1100, "uniform", "ffma"),
               (1000, 3000, 1100, "int", "ffma"), (400, 8000, 20000, "normal", "ffma")]
 
 
@@ -360,7 +389,7 @@ def test_balanced_tail_scaled(tg, path, M, N, K):
     assert_close(Cd.cpu().numpy(), ref, K, f"balanced tail scaled {path} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tf32bf16"])
 @pytest.mark.parametrize("M,N,K", [(3, 5, 1 << 22), (2, 1 << 24, 3), (1 << 22, 7, 9)])
 def test_extreme_aspect_ratios(tg, path, M, N, K):
     """Products of hundreds of MB with one dimension in the millions and the

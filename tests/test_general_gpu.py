@@ -41,7 +41,7 @@ def gpu_general(tg, op_a, op_b, alpha, As, Bs, beta, C0, **kw):
     return C.cpu().numpy()
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled", "tf32bf16"])
 @pytest.mark.parametrize("op_a,op_b", OPS)
 def test_general_ops_alpha_beta(tg, path, op_a, op_b):
     M, N, K = 300, 257, 513
@@ -56,7 +56,7 @@ def test_general_ops_alpha_beta(tg, path, op_a, op_b):
             assert_close(got, ref, K, f"{path} op=({op_a},{op_b}) a={alpha} b={beta} s={split}")
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tiled", "tf32bf16"])
 @pytest.mark.parametrize("op_a,op_b", OPS)
 def test_general_integer_bitexact(tg, path, op_a, op_b):
     M, N, K = 130, 270, 300
@@ -73,7 +73,7 @@ def test_general_integer_bitexact(tg, path, op_a, op_b):
 def test_general_k0_and_beta0_ignores_c(tg):
     M, N = 9, 11
     C0 = np.random.default_rng(7).uniform(-1, 1, (M, N)).astype(np.float32)
-    for path in ("tf32x3", "ffma", "tiled"):
+    for path in ("tf32x3", "ffma", "tiled", "tf32bf16"):
         got = gpu_general(tg, 1, 1, 3.0, np.zeros((0, M), np.float32), np.zeros((N, 0), np.float32), 0.5, C0,
                           path=path)
         assert_bitexact(got, 0.5 * C0, f"K=0 {path}")
