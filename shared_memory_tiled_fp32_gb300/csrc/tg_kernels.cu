@@ -929,12 +929,13 @@ __device__ __forceinline__ long long dst_offset(int pitch, int r, int c) {
     return (long long)r * pitch + c;
 }
 
-// kSplitBf16: float offset of the bf16 value(s) of K index c (row r) in
-// logical group `first` (4: bf16 hi, 6: bf16 lo) of the row whose hi group
-// sits at offset o.
-__device__ __forceinline__ long long bf16_offset(long long o, int r, int c, int first) {
-    const int j = (c & 15) >> 2;
-    return (o & ~31ll) + (((first + (j >> 1)) ^ (r & 7)) << 2) + ((j & 1) << 1);
+// kSplitBf16: float offset of the 4 bf16 values (8 bytes) that belong to the
+// hi group at offset o, in logical group `first` (4: bf16 hi, 6: bf16 lo).
+// o encodes the row (bits 5-11, swizzle key bits 5-7) and the stored group
+// position (bits 2-4), so the logical group j follows from o alone.
+__device__ __forceinline__ long long bf16_offset(long long o, int first) {
+    const int key = (int)(o >> 5) & 7, j = ((int)(o >> 2) & 7) ^ key;
+    return (o & ~31ll) + (((first + (j >> 1)) ^ key) << 2) + ((j & 1) << 1);
 }
 
 // hi of the split: x rounded to tf32 (nearest, ties away), or truncated where
@@ -957,7 +958,7 @@ __device__ __forceinline__ uint2 to_bf16x4(float a, float b, float c, float d) {
 // Store destination columns c..c+3 of row r (c a multiple of 4: one 16-byte
 // group) at offset o.
 template <int MODE>
-__device__ __forceinline__ void store_split4(float* d0, long long o, float4 x, int r, int c) {
+__device__ __forceinline__ void store_split4(float* d0, long long o, float4 x) {
     if (MODE == kPack) {
         *reinterpret_cast<float4*>(d0 + o) = x;
         return;
@@ -968,8 +969,8 @@ __device__ __forceinline__ void store_split4(float* d0, long long o, float4 x, i
         *reinterpret_cast<float4*>(d0 + (o ^ 16)) =
             make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
     } else {
-        *reinterpret_cast<uint2*>(d0 + bf16_offset(o, r, c, 4)) = to_bf16x4(hi.x, hi.y, hi.z, hi.w);
-        *reinterpret_cast<uint2*>(d0 + bf16_offset(o, r, c, 6)) =
+        *reinterpret_cast<uint2*>(d0 + bf16_offset(o, 4)) = to_bf16x4(hi.x, hi.y, hi.z, hi.w);
+        *reinterpret_cast<uint2*>(d0 + bf16_offset(o, 6)) =
             to_bf16x4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
     }
 }
@@ -982,7 +983,6 @@ __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < p.items; i += kInFlight * stride) {
         float4 v[kInFlight];
         long long o[kInFlight];
-        int rr[kInFlight], cc[kInFlight];
 #pragma unroll
         for (int u = 0; u < kInFlight; ++u) {
             const long long it = i + u * stride;
@@ -992,13 +992,11 @@ __device__ __forceinline__ void rowwise_pass(const OperandPass& p) {
                 v[u] = r < p.rows_valid ? load_row4(p.src, p.ld, r, c, p.cols, p.vec != 0)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                 o[u] = dst_offset<MODE>(p.pitch, r, c);
-                rr[u] = r;
-                cc[u] = c;
             }
         }
 #pragma unroll
         for (int u = 0; u < kInFlight; ++u)
-            if (o[u] >= 0) store_split4<MODE>(p.d0, o[u], v[u], rr[u], cc[u]);
+            if (o[u] >= 0) store_split4<MODE>(p.d0, o[u], v[u]);
     }
 }
 
@@ -1044,8 +1042,8 @@ __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*til
                     if (MODE == kSplitTf32) {
                         p.d0[o ^ 16] = to_tf32(x - hi);
                     } else {  // one bf16 of each, element c % 4 of its 8-byte run
-                        __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, r, c, 4));
-                        __nv_bfloat16* lb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, r, c, 6));
+                        __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, 4));
+                        __nv_bfloat16* lb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, 6));
                         hb[c & 3] = __ushort_as_bfloat16((unsigned short)bf16_bits(hi));
                         lb[c & 3] = __ushort_as_bfloat16((unsigned short)bf16_bits(x - hi));
                     }

@@ -65,7 +65,7 @@ static int gpu_checks(void) {
     for (int i = 0; i < M; ++i)
         for (int k = 0; k < K; ++k) At[(size_t)k * M + i] = A[(size_t)i * K + k];
     CHECK(tg_oracle_sgemm(M, N, K, A, K, B, N, R, N) == 0, "oracle");
-    for (int path = TG_PATH_FFMA; path <= TG_PATH_TF32X3; ++path) {
+    for (int path = TG_PATH_FFMA; path <= TG_PATH_TF32_BF16; ++path) {
         tg_sgemm_opts o;
         memset(&o, 0, sizeof o);
         o.path = path;
