@@ -1027,28 +1027,15 @@ __device__ __forceinline__ void transpose_pass(const OperandPass& p, float (*til
         for (int j = 0; j < 16; ++j) tile[ty + 4 * j][tx] = v[j];
         __syncthreads();
         if (t + gridDim.x < p.items) transpose_load(p, t + gridDim.x, tx, ty, v);
-        // destination row r, column c: coalesced along c
+        // one 16-byte group (destination columns c..c+3) of row r per store;
+        // 16 threads cover a row's 64 columns
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int r = r0 + ty + 4 * j, c = c0 + tx;
-            if (r < p.rows && c < p.pitch) {
-                const float x = tile[tx][ty + 4 * j];
-                const long long o = dst_offset<MODE>(p.pitch, r, c);
-                if (MODE == kPack) {
-                    p.d0[o] = x;
-                } else {
-                    const float hi = split_hi(x);
-                    p.d0[o] = hi;
-                    if (MODE == kSplitTf32) {
-                        p.d0[o ^ 16] = to_tf32(x - hi);
-                    } else {  // one bf16 of each, element c % 4 of its 8-byte run
-                        __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, 4));
-                        __nv_bfloat16* lb = reinterpret_cast<__nv_bfloat16*>(p.d0 + bf16_offset(o, 6));
-                        hb[c & 3] = __ushort_as_bfloat16((unsigned short)bf16_bits(hi));
-                        lb[c & 3] = __ushort_as_bfloat16((unsigned short)bf16_bits(x - hi));
-                    }
-                }
-            }
+        for (int q = 0; q < 4; ++q) {
+            const int g = threadIdx.x + 256 * q, rl = g >> 4, cl = (g & 15) * 4;
+            const int r = r0 + rl, c = c0 + cl;
+            if (r < p.rows && c < p.pitch)  // pitch is a multiple of 4: the whole group is in range
+                store_split4<MODE>(p.d0, dst_offset<MODE>(p.pitch, r, c),
+                                   make_float4(tile[cl][rl], tile[cl + 1][rl], tile[cl + 2][rl], tile[cl + 3][rl]));
         }
         __syncthreads();
     }
