@@ -107,18 +107,75 @@ def test_unswizzled_a_would_conflict():
 # -------------------------------------------------------- pre-pass transpose
 
 
-def test_prepass_transpose_tile_conflict_free():
+def test_prepass_transpose_tile_banks():
     """The pre-pass stages a 64 x 64 tile as tile[ty + 4j][tx] (row writes,
-    tx = 0..63, a warp holds 32 consecutive tx) and reads it as
-    tile[tx][ty + 4j] with a 65-float pitch: both are conflict-free."""
+    tx = 0..63, a warp holds 32 consecutive tx; conflict-free with the
+    65-float pitch) and reads it back one 16-byte destination group per
+    thread: thread g = threadIdx + 256q reads tile[cl + e][rl], e = 0..3, with
+    rl = g / 16 and cl = 4 (g % 16).  Those reads are two-way: lanes whose
+    groups are 8 apart (cl 32 apart) land on the same bank."""
     pitch = 65
     for ty in range(4):
         for half in (0, 32):
             for j in range(16):
                 writes = [4 * ((ty + 4 * j) * pitch + tx) for tx in range(half, half + 32)]
-                reads = [4 * (tx * pitch + ty + 4 * j) for tx in range(half, half + 32)]
                 assert wavefronts_32(writes) == 1
-                assert wavefronts_32(reads) == 1
+    for warp in range(8):
+        for q in range(4):
+            for e in range(4):
+                reads = []
+                for lane in range(32):
+                    g = 32 * warp + lane + 256 * q
+                    rl, cl = g >> 4, (g & 15) * 4
+                    reads.append(4 * ((cl + e) * pitch + rl))
+                assert wavefronts_32(reads) == 2
+
+
+def split_tile_offset(pitch, r, c):
+    """dst_offset of the split pre-pass modes (csrc/tg_kernels.cu), in floats:
+    16 KiB tiles [r / 128][c / 16], row r % 128 of 32 floats, 16-byte group
+    (c % 16) / 4 at position group ^ (r % 8)."""
+    return ((r >> 7) * (pitch >> 4) + (c >> 4)) * 4096 + (r & 127) * 32 + ((((c & 15) >> 2) ^ (r & 7)) << 2) + (c & 3)
+
+
+def bf16_run_offset(o, first):
+    """bf16_offset of the tf32 + bf16 mode: the 8-byte run of the group at o
+    inside logical group first (4: bf16 hi, 6: bf16 lo), in floats."""
+    key = (o >> 5) & 7
+    j = ((o >> 2) & 7) ^ key
+    return (o & ~31) + (((first + (j >> 1)) ^ key) << 2) + ((j & 1) << 1)
+
+
+@pytest.mark.parametrize("rows,pitch", [(300, 64), (128, 16), (1, 32)])
+def test_split_tile_layouts_cover_each_slot_once(rows, pitch):
+    """Both split layouts write every byte of the padded tiles exactly once:
+    3xTF32 (hi at o, lo at o ^ 16) and tf32 + bf16 (tf32 hi at o, bf16 hi and
+    lo in groups 4-7), and in the mixed layout the bf16 values of K 0-7 / 8-15
+    of a row fill logical groups 4 / 5 (hi) and 6 / 7 (lo) in K order, so
+    that one 32-byte MMA slice starts at group 4 or 6."""
+    padded = -(-rows // 128) * 128
+    total = padded // 128 * (pitch // 16) * 4096 * 4  # bytes
+    tf32 = [0] * total
+    mixed = [0] * total
+    for r in range(padded):
+        for c in range(pitch):
+            o = split_tile_offset(pitch, r, c)
+            for b in range(4):
+                tf32[4 * o + b] += 1
+                tf32[4 * (o ^ 16) + b] += 1
+                mixed[4 * o + b] += 1
+            for first in (4, 6):
+                ob = 2 * bf16_run_offset(o, first) + (c & 3)  # in 2-byte units
+                mixed[2 * ob] += 1
+                mixed[2 * ob + 1] += 1
+                # logical position inside the row: group first + (c % 16) / 8, slot (c % 8)
+                row_base = o & ~31
+                phys_group = ((ob // 2) - row_base) // 4
+                logical = phys_group ^ (r & 7)
+                assert logical == first + ((c & 15) >> 3)
+                assert (ob - 2 * (row_base + 4 * phys_group)) == (c & 7)
+    assert all(v == 1 for v in tf32)
+    assert all(v == 1 for v in mixed)
 
 
 # ------------------------------------------------------- transpose workload
