@@ -62,7 +62,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline (profiling runs)")
     ap.add_argument("--no-probes", action="store_true", help="skip the instruction-mix peak probes")
     ap.add_argument("--no-alt", action="store_true",
-                    help="skip the opt-in tf32 + bf16 cross-product path's line on the headline workload")
+                    help="skip the lines of the other math paths (tf32 + bf16, FFMA) on the headline workload")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the 4096^3 measurement reported beside the 8192^3 headline")
     ap.add_argument("--transpose", action="store_true",
@@ -606,11 +606,11 @@ def main():
                      "l2": "inputs larger than L2 (A+B = 128 MiB)"}
         del A2, B2, C2, ws2
 
-    # the opt-in tf32 + bf16 cross-product path on the same inputs: throughput,
-    # fraction of its own derived peak, and its error on the oracle's rows
-    alt = None
-    if not args.no_alt and args.path == "auto" and w.name == DEFAULT_WORKLOAD and not general and world == 1:
-        pa = tg.plan(w.M, w.N, w.K, A=Ad.data_ptr(), B=Bd.data_ptr(), C=Cd.data_ptr(), path="tf32bf16")
+    # the other math paths on the same inputs, one line each: the opt-in tf32 +
+    # bf16 cross-product path and the FFMA path, with throughput, the fraction
+    # of their own peak and their error on the oracle's rows
+    def other_path(path, peak_p, peak_source):
+        pa = tg.plan(w.M, w.N, w.K, A=Ad.data_ptr(), B=Bd.data_ptr(), C=Cd.data_ptr(), path=path)
         wsa = torch.empty(max(1, pa["workspace_bytes"] // 4 + 64), device=dev)
         stepsa = max(args.steps, 10)
         eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(stepsa)]
@@ -618,32 +618,38 @@ def main():
             e0.record(stream)
             e1.record(stream)
         for _ in range(args.warmup):
-            tg.matmul(Ad, Bd, out=Cd, path="tf32bf16", workspace=wsa, stream=stream)
+            tg.matmul(Ad, Bd, out=Cd, path=path, workspace=wsa, stream=stream)
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         s0.record(stream)
         for i in range(stepsa):
-            tg.matmul(Ad, Bd, out=Cd, path="tf32bf16", workspace=wsa, main_begin=eva[i][0], main_end=eva[i][1],
+            tg.matmul(Ad, Bd, out=Cd, path=path, workspace=wsa, main_begin=eva[i][0], main_end=eva[i][1],
                       stream=stream)
         s1.record(stream)
         torch.cuda.synchronize(dev)
         if tg.sync_status() != 0:
-            raise RuntimeError("a kernel reported a timeout on the tf32 + bf16 path")
+            raise RuntimeError(f"a kernel reported a timeout on the {path} path")
         msa = s0.elapsed_time(s1) / stepsa
         ka = float(np.mean([a.elapsed_time(b) for a, b in eva]))
-        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-        peak_a = 1.0 / (1.0 / (bf16 * TF32_OVER_BF16) + 2.0 / bf16)
-        alt = {"path": "tf32bf16", "value": w.flop / (msa * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": msa,
+        out = {"path": path, "value": w.flop / (msa * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": msa,
                "kernel_ms": ka, "kernel_tflops": w.flop / (ka * 1e-3) / 1e12,
-               "roofline_frac": w.flop / (ka * 1e-3) / 1e12 / peak_a, "peak": peak_a, "steps": stepsa,
-               "peak_source": "1 / (1/tf32 + 2/bf16), tf32 = bf16 x 1.1/2.25, bf16 as the main line"}
+               "roofline_frac": w.flop / (ka * 1e-3) / 1e12 / peak_p, "peak": peak_p, "steps": stepsa,
+               "peak_source": peak_source}
         if cpu is not None:
             got = Cd[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
             r64 = ref.astype(np.float64)
-            alt["max_rel_error"] = {"normwise_rel": float(np.linalg.norm(got - r64) / np.linalg.norm(r64)),
+            out["max_rel_error"] = {"normwise_rel": float(np.linalg.norm(got - r64) / np.linalg.norm(r64)),
                                     "max_abs_over_max_ref": float(np.abs(got - r64).max() / np.abs(r64).max()),
                                     "rows_checked": len(rows)}
-        del wsa
+        return out
+
+    alt = ffma_line = None
+    if not args.no_alt and args.path == "auto" and w.name == DEFAULT_WORKLOAD and not general and world == 1:
+        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        alt = other_path("tf32bf16", 1.0 / (1.0 / (bf16 * TF32_OVER_BF16) + 2.0 / bf16),
+                         "1 / (1/tf32 + 2/bf16), tf32 = bf16 x 1.1/2.25, bf16 as the main line")
+        ffma_line = other_path("ffma", FFMA_FLOP_PER_CLK * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12,
+                               "152 SMs x 128 FMA lanes x 2 FLOP x max SM clock (CUDA-core fp32 peak)")
 
     # ceilings of the two instruction mixes on this GPU (context for the roofline)
     probes = None
@@ -690,6 +696,7 @@ def main():
         "probes": probes,
         "secondary": secondary,
         "alt_path": alt,
+        "ffma_path": ffma_line,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
