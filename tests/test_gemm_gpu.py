@@ -183,7 +183,7 @@ def test_operands_near_float_max(tg, path):
 
 def test_deterministic(tg):
     A, B, _, _ = workload_case("ragged_777x1029x513")
-    for path in ("tf32x3", "ffma", "tiled"):
+    for path in ("tf32x3", "ffma", "tiled", "tf32bf16"):
         c1 = run(tg, A, B, path=path)
         c2 = run(tg, A, B, path=path)
         assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32)), path
@@ -215,7 +215,7 @@ def test_host_buffer_entry(tg):
     assert np.array_equal(C.numpy().view(np.uint32), dev.view(np.uint32))
 
 
-@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tf32bf16"])
 def test_host_buffer_entry_row_blocks(tg, path):
     """A product large enough for the host entry point to pipeline row blocks
     (copies of one block overlapping the product of another), with a ragged
@@ -237,7 +237,7 @@ def test_host_buffer_entry_row_blocks(tg, path):
 
 
 @pytest.mark.parametrize("layout", [None, "1024,1024,1536,4", "512,1536,1024,2,1"])
-@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+@pytest.mark.parametrize("path", ["tf32x3", "ffma", "tf32bf16"])
 def test_host_buffer_entry_2d_blocks(tg, path, layout, monkeypatch):
     """The host entry point with C cut into row blocks, the first ones also
     into column blocks (ragged last ones), the later ones full width: every
