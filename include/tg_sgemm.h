@@ -77,11 +77,13 @@ typedef enum tg_op { TG_OP_N = 0, TG_OP_T = 1 } tg_op;
  *    hi*hi (kind::tf32) + bf16(hi)*bf16(lo) + bf16(lo)*bf16(hi) (kind::f16,
  *    bf16 operands, fp32 accumulator).  A cross product is at most 2^-11 of
  *    the main one, so rounding its operands to bf16's 8 significant bits adds
- *    at most about 2^-18 of |a*b| per product (3xTF32: about 2^-22); bf16 has
- *    fp32's exponent range, so no operand scaling is needed.  Two of the
- *    three products run at bf16 rate: four tensor instructions per 16-wide K
- *    block instead of six.  Integer inputs with |x| < 2^8 stay exact (lo is
- *    zero).  Only on request; TG_PATH_AUTO never picks it.
+ *    at most about 2^-18 of |a*b| each, about 2^-17 per product with the
+ *    dropped lo*lo (3xTF32: about 2^-21); bf16 has fp32's exponent range, so
+ *    no operand scaling is needed.  Two of the three products run at bf16
+ *    rate: four tensor instructions per 16-wide K block instead of six.
+ *    Integers with |x| <= 2^11 (and partial sums below 2^24) stay exact: lo
+ *    is zero, so the cross products vanish.  Only on request; TG_PATH_AUTO
+ *    never picks it.
  *  - TG_PATH_AUTO: TG_PATH_TILED for small products (where one launch beats
  *    the three of the 3xTF32 path; see tg_sgemm_plan), else TG_PATH_TF32X3. */
 typedef enum tg_path {
