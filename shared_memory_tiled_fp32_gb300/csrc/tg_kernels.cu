@@ -482,9 +482,10 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 //
 // Warp roles (384 threads, 3 warpgroups): warp 0 = copy producer, warp 1 =
 // tensor-memory owner and MMA issuer (one thread; with the pair MMA only in
-// the pair's first CTA), warps 2-3 idle; warps 4-11 = epilogue.  Epilogue warp e reads tensor-memory lanes 32*(e%4).. (a warp
-// may only touch the lane quarter of its warp index modulo 4) and columns
-// 128*(e/4)..+127, so each thread owns 128 accumulators of one output row.
+// the pair's first CTA), warps 2-3 idle; warps 4-11 = epilogue.  Epilogue
+// warp e reads tensor-memory lanes 32*(e%4).. (a warp may only touch the lane
+// quarter of its warp index modulo 4) and columns 128*(e/4)..+127, so each
+// thread owns 128 accumulators of one output row.
 // Two chunk buffers of 256 columns (all 512 tensor-memory columns) let the
 // epilogue drain one chunk while the MMAs fill the next.
 
