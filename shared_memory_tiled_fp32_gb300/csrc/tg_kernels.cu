@@ -829,13 +829,25 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                 if (col < args.N) {
                     // (r, lane) sits at r*32 + (lane ^ 4*(r & 7))
                     float* dst = t.out + (long long)row0 * t.ldo + col;
+                    if (scaled && args.beta != 0.0f) {
+                        // C's old values first, all 32 loads in flight at once:
+                        // one load per store, each waited for in turn, held
+                        // the epilogue up long enough to stall the next unit's
+                        // MMAs (8192^3 kernel 317 against 384 TFLOP/s)
+                        float old[32];
+                        const float* src = dst;
+#pragma unroll
+                        for (int r = 0; r < 32; ++r, src += t.ldo) old[r] = r < rows ? *src : 0.0f;
+#pragma unroll
+                        for (int r = 0; r < 32; ++r, dst += t.ldo)
+                            if (r < rows)
+                                *dst = fmaf(args.alpha, stg[r * 32 + (lane ^ ((r & 7) << 2))], args.beta * old[r]);
+                    } else {
 #pragma unroll 1
-                    for (int r = 0; r < rows; ++r, dst += t.ldo) {
-                        const float v = stg[r * 32 + (lane ^ ((r & 7) << 2))];
-                        if (scaled)
-                            *dst = args.beta != 0.0f ? fmaf(args.alpha, v, args.beta * *dst) : args.alpha * v;
-                        else
-                            *dst = v;
+                        for (int r = 0; r < rows; ++r, dst += t.ldo) {
+                            const float v = stg[r * 32 + (lane ^ ((r & 7) << 2))];
+                            *dst = scaled ? args.alpha * v : v;
+                        }
                     }
                 }
                 __syncwarp();
