@@ -224,26 +224,27 @@ __device__ __forceinline__ void store_row4(float* row, int col, int N, float4 v,
     }
 }
 
+// The 4 values of C at row[col..col+3] (guarded like store_row4; zero past N).
+__device__ __forceinline__ float4 load_row4_c(const float* row, int col, int N, bool vec) {
+    if (vec && col + 3 < N) return *reinterpret_cast<const float4*>(row + col);
+    return make_float4(col < N ? row[col] : 0.0f, col + 1 < N ? row[col + 1] : 0.0f,
+                       col + 2 < N ? row[col + 2] : 0.0f, col + 3 < N ? row[col + 3] : 0.0f);
+}
+
+// alpha * v + beta * c (c ignored when beta == 0, so C may hold anything).
+__device__ __forceinline__ float4 scale4(float4 v, float4 c, float alpha, float beta) {
+    if (beta != 0.0f)
+        return make_float4(fmaf(alpha, v.x, beta * c.x), fmaf(alpha, v.y, beta * c.y), fmaf(alpha, v.z, beta * c.z),
+                           fmaf(alpha, v.w, beta * c.w));
+    return make_float4(alpha * v.x, alpha * v.y, alpha * v.z, alpha * v.w);
+}
+
 // The final value alpha * v + beta * C of 4 consecutive outputs (C read only
 // when beta != 0), then the guarded store.
 __device__ __forceinline__ void store_row4_scaled(float* row, int col, int N, float4 v, bool vec,
                                                   float alpha, float beta) {
-    if (beta != 0.0f) {
-        float4 c;
-        if (vec && col + 3 < N) {
-            c = *reinterpret_cast<const float4*>(row + col);
-        } else {
-            c.x = col < N ? row[col] : 0.0f;
-            c.y = col + 1 < N ? row[col + 1] : 0.0f;
-            c.z = col + 2 < N ? row[col + 2] : 0.0f;
-            c.w = col + 3 < N ? row[col + 3] : 0.0f;
-        }
-        v = make_float4(fmaf(alpha, v.x, beta * c.x), fmaf(alpha, v.y, beta * c.y), fmaf(alpha, v.z, beta * c.z),
-                        fmaf(alpha, v.w, beta * c.w));
-    } else {
-        v = make_float4(alpha * v.x, alpha * v.y, alpha * v.z, alpha * v.w);
-    }
-    store_row4(row, col, N, v, vec);
+    const float4 c = beta != 0.0f ? load_row4_c(row, col, N, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+    store_row4(row, col, N, scale4(v, c, alpha, beta), vec);
 }
 
 __device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {
@@ -427,15 +428,22 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
             const int r = t.m0 + wm * 32 + lm + 4 * i;
             if (r < args.M) {
                 float* row = t.out + (long long)r * t.ldo;
+                // with beta != 0 the row's four old C groups are loaded before
+                // any store, so their loads overlap instead of each store
+                // waiting for its own load
+                const bool read_c = scale && args.beta != 0.0f;
+                float4 old[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = t.n0 + wn * 128 + 32 * j + 4 * ln;
+                    old[j] = read_c ? load_row4_c(row, c, args.N, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int c = t.n0 + wn * 128 + 32 * j + 4 * ln;
                     const float2 lo = f32x2_unpack(acc[i][2 * j]), hi = f32x2_unpack(acc[i][2 * j + 1]);
                     const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
-                    if (scale)
-                        store_row4_scaled(row, c, args.N, v, vec, args.alpha, args.beta);
-                    else
-                        store_row4(row, c, args.N, v, vec);
+                    store_row4(row, c, args.N, scale ? scale4(v, old[j], args.alpha, args.beta) : v, vec);
                 }
             }
         }
