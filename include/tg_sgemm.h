@@ -126,7 +126,7 @@ typedef struct tg_plan_info {
     int prepass;       /* 1 = an operand re-layout kernel runs first */
     int launches;      /* kernels one call launches */
     size_t workspace_bytes;
-    int pair;          /* 3xTF32: CTAs per cluster sharing one B tile by TMA multicast (1 or 2);
+    int pair;          /* 3xTF32: CTAs per cluster sharing one B tile through a pair MMA (1 or 2);
                           a unit is then `pair` vertically adjacent tiles */
     long long tail_units; /* units after the last whole round of lanes, balanced (0 = none) */
     int tail_lanes;       /* lanes (CTAs, or CTA pairs) sharing those units' K blocks equally */
@@ -274,10 +274,13 @@ tg_status tg_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream)
  * other allocating call.
  *
  * Arguments, layout, ownership and results are those of tg_sgemm.  Limit: the
- * hi/lo copies need 8*(M+N)*roundup(K,4) bytes (plus split-K partials, which
- * are dropped when they would not fit); a product whose scratch exceeds
+ * hi/lo copies need 8*(M'+N')*K' bytes, with M' = M rounded up to a multiple
+ * of 256 (128 when M <= 128), N' = N rounded up to a multiple of 256 and K' =
+ * K rounded up to a multiple of 16 (the split tiles are whole 128-row tiles,
+ * paired along M).  Split-K and balanced-tail partials come on top and are
+ * dropped when they would not fit.  A product whose split tiles exceed
  * TG_SGEMM_NOALLOC_SCRATCH_BYTES returns TG_ERR_WORKSPACE_TOO_SMALL and
- * launches nothing (M = N = K = 2048 fits exactly).
+ * launches nothing (M = N = K = 2048 fits exactly; N = 2049 does not).
  *
  * The first call on each device does a one-time set-up there (capability
  * check, kernel attributes, and the scratch's device address via

@@ -78,7 +78,7 @@ struct Plan {
     int split = 1;
     int bm = 0, bn = 0, bk = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0;
-    int pair = 1;        // 3xTF32: CTAs per cluster sharing one B tile (TMA multicast)
+    int pair = 1;        // 3xTF32: CTAs per cluster on vertically adjacent tiles (pair MMA)
     long long units = 0; // work units (a unit is `pair` vertically adjacent tiles x one K slice)
     // stream-K tail: the tile units past full_units (tail_units of them) are
     // shared out over tail_lanes lanes, each running an equal share of their

@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 #include <cstdlib>
@@ -469,8 +470,9 @@ __global__ void __launch_bounds__(kFfmaThreads, 1)
 // tensor-map copies that complete on the first CTA's barrier; each CTA's
 // tensor memory holds its 128 rows of the accumulator.  Per-CTA MMA (single
 // CTAs, or pairs with the pair MMA off): each CTA issues M = 128 products
-// on its A tile and the whole B tile (48 KiB a stage, 4 stages), its own B
-// half fetched by one bulk copy multicast into both CTAs of the pair.
+// on its A tile and the whole B tile (48 KiB a stage, 4 stages), fetching
+// both halves of B itself with plain bulk copies; the two CTAs of a pair
+// then share nothing but their cluster rank.
 //
 // Per 8-wide K slice the MMA thread issues
 //     D += A_hi B_lo;  D += A_hi B_hi;  D += A_lo B_hi
@@ -555,12 +557,11 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WaitCtl wc{&g_error_word, args.timeout_ns};
-    // cluster of kPair CTAs: CTA `rank` computes tile row 2*row + rank and
-    // loads rank's half of the shared B tile for both CTAs (TMA multicast)
+    // cluster of kPair CTAs: CTA `rank` computes tile row 2*row + rank (with
+    // the pair MMA it also loads rank's half of the pair's B tile)
     const int rank = kPair > 1 ? (int)cluster_ctarank() : 0;
     const long long first_unit = blockIdx.x / kPair, unit_stride = gridDim.x / kPair;
     constexpr uint16_t kPairMask = (uint16_t)((1u << kPair) - 1u);
-    constexpr uint32_t kBHalf = kTfBStage / kPair;  // bytes of the B tile one CTA loads
     // pair MMA: the first CTA's barriers gather both CTAs' copies (full) and
     // both CTAs' chunk drains (tempty)
     const bool issuer = !kPairMma || rank == 0;
@@ -568,8 +569,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
-            // one MMA commit from each CTA of a multicast pair; one for both with the pair MMA
-            mbar_init(&empty[s], kPairMma ? 1 : kPair);
+            // one MMA commit: this CTA's own, or the pair MMA's (which arrives in both CTAs)
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (kPair > 1) cluster_sync_all();  // the peer's barriers exist before any multicast
+    if (kPairMma) cluster_sync_all();  // the peer's barriers exist before any remote arrive
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // the set-up above overlaps the end of the pre-pass; its output is read below
@@ -605,8 +606,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             Unit t;
             for (long long j = 0; ok && work_item<true, false>(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    // with a pair, "empty" completes only when both CTAs are done
-                    // with the stage, since this CTA's B half lands in both
+                    // pair MMA: "empty" completes when the pair's products
+                    // that read this stage in both CTAs are done
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteTfProducer)) {
                         ok = false;
                         break;
@@ -628,21 +629,14 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         }
                         continue;
                     }
-                    // this CTA receives the whole A and B tiles (48 KiB), half
-                    // of B from its own copy and half from the peer's
+                    // this CTA's A tile and the whole B tile (48 KiB), each
+                    // 128-row tile one bulk copy into this CTA's own ring
                     mbar_arrive_expect_tx(&full[stage], kTfStageBytes);
                     const float* a_src = args.a_tiles + ((long long)(t.m0 >> 7) * args.kbs + kb) * kTileFloats;
                     const float* b_src = args.b_tiles + ((long long)(t.n0 >> 7) * args.kbs + kb) * kTileFloats;
                     bulk_load(st, a_src, kTfAStage, &full[stage]);
-                    if (kPair > 1) {
-                        bulk_load_multicast(st + kTfAStage + rank * kBHalf,
-                                            b_src + (long long)rank * args.kbs * kTileFloats, kBHalf, &full[stage],
-                                            kPairMask);
-                    } else {
-                        bulk_load(st + kTfAStage, b_src, kTfAStage, &full[stage]);
-                        bulk_load(st + 2 * kTfAStage, b_src + (long long)args.kbs * kTileFloats, kTfAStage,
-                                  &full[stage]);
-                    }
+                    bulk_load(st + kTfAStage, b_src, kTfAStage, &full[stage]);
+                    bulk_load(st + 2 * kTfAStage, b_src + (long long)args.kbs * kTileFloats, kTfAStage, &full[stage]);
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == ST) {
@@ -706,10 +700,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                                 mma_f16_ss(d_tmem, da + 6, db + 4, idesc_x, 1u);
                                 mma_tf32_ss(d_tmem, da, db, idesc, 1u);
                                 mma_tf32_ss(d_tmem, da + 2, db + 2, idesc, 1u);
-                                if (kPair > 1)
-                                    mma_commit_multicast(&empty[stage], kPairMask);
-                                else
-                                    mma_commit(&empty[stage]);
+                                mma_commit(&empty[stage]);
                             }
                             if (++stage == ST) {
                                 stage = 0;
@@ -745,11 +736,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         mma_tf32_ss_fill_a(d_tmem, da + 2, db + 6, idesc, 1u);
                         mma_tf32_ss_lastuse_a(d_tmem, da + 2, db + 2, idesc, 1u);
                         mma_tf32_ss(d_tmem, da + 6, db + 2, idesc, 1u);
-                        // frees the stage (in both CTAs of a pair) once these MMAs are done
-                        if (kPair > 1)
-                            mma_commit_multicast(&empty[stage], kPairMask);
-                        else
-                            mma_commit(&empty[stage]);
+                        // frees the stage once these MMAs are done
+                        mma_commit(&empty[stage]);
                         if (++stage == ST) {
                             stage = 0;
                             phase ^= 1u;
@@ -875,9 +863,9 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         else
             tmem_dealloc(tmem_base, kTmemCols);
     }
-    // neither CTA of a pair may exit while the other can still multicast into
-    // its shared memory or arrive on its barriers
-    if (kPair > 1) cluster_sync_all();
+    // pair MMA: neither CTA may exit while the other can still arrive on its
+    // barriers or have products read its shared memory
+    if (kPairMma) cluster_sync_all();
 }
 
 // ------------------------------------------------------------ pre-pass
@@ -1400,6 +1388,31 @@ bool pdl_enabled() {
     return on;
 }
 
+// NVTX ranges around the launches of one call (pre-pass, GEMM, reduce), so a
+// profiler can select a phase (e.g. ncu --nvtx --nvtx-include "tg_gemm/").
+// Off unless TG_NVTX=1: the ranges cost a little host time per call.  NVTX
+// is header-only and does nothing unless a profiler has attached its
+// injection library.
+bool nvtx_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("TG_NVTX");
+        return e != nullptr && std::strcmp(e, "1") == 0;
+    }();
+    return on;
+}
+
+struct NvtxRange {
+    bool on;
+    explicit NvtxRange(const char* name) : on(nvtx_enabled()) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~NvtxRange() {
+        if (on) nvtxRangePop();
+    }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 template <typename... KArgs, typename... Args>
 tg_status launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                            unsigned cluster, Args&&... args) {
@@ -1443,7 +1456,7 @@ int g_tf32_pair_clusters = 0;
 // (cta_group::2), each CTA holding its A tile and its half of B, so the ring
 // has 6 stages instead of 4 (measured: 3xTF32 steps 2.8-3.5 % faster at
 // 4096^3, 8192^3 and 2048 x 2048 x 16384).  TG_TF32X3_PAIRMMA=0 keeps one
-// M = 128 product per CTA with B multicast to both.
+// M = 128 product per CTA, each CTA loading the whole B tile itself.
 bool pair_mma_enabled() {
     const char* e = std::getenv("TG_TF32X3_PAIRMMA");
     return !(e != nullptr && e[0] == '0');
@@ -1487,7 +1500,7 @@ tg_status prepare_device_kernels() {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(kTfThreads);
-    cfg.dynamicSmemBytes = kTfSmemBytes;
+    cfg.dynamicSmemBytes = kTfSmemBytesPairMma;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -1496,7 +1509,7 @@ tg_status prepare_device_kernels() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tf32x3_gemm_kernel<2, false>, &cfg) == cudaSuccess && clusters > 0)
+    if (cudaOccupancyMaxActiveClusters(&clusters, tf32x3_gemm_kernel<2, true>, &cfg) == cudaSuccess && clusters > 0)
         g_tf32_pair_clusters = clusters;
     else
         cudaGetLastError();
@@ -1529,6 +1542,7 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         ta.scaled = (p.alpha != 1.0f || p.beta != 0.0f) ? 1 : 0;
         ta.vec_c = p.vec_c ? 1 : 0;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
+        NvtxRange r("tg_gemm");
         if (launch_dependent(tiled_gemm_kernel, dim3((unsigned)((long long)p.tiles_m * p.tiles_n)),
                              dim3(kTiledThreads), 0, stream, 1, ta) != TG_OK)
             return TG_ERR_CUDA;
@@ -1599,6 +1613,7 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         pa.op[0] = pass(A, p.lda, p.M, p.K, p.k16, p.op_a == TG_OP_T, p.a_ready ? nullptr : a_tiles, p.a_rows);
         pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, p.b_ready ? nullptr : b_tiles, p.b_rows);
         if (!(p.a_ready && p.b_ready)) {
+            NvtxRange r("tg_prepass");
             if (mixed)
                 prepass_kernel<kSplitBf16><<<prepass_grid, 256, 0, stream>>>(pa);
             else
@@ -1621,6 +1636,7 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
             return TG_ERR_CUDA;
         int clusters = p.grid / 2;
         if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
+        NvtxRange r("tg_gemm");
         void (*kern)(CUtensorMap, CUtensorMap, GemmArgs);
         if (p.pair == 2)
             kern = pair_mma ? (mixed ? tf32x3_gemm_kernel<2, true, true> : tf32x3_gemm_kernel<2, true>)
@@ -1641,6 +1657,7 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
             float* bp = p.pack_b ? reinterpret_cast<float*>(w + p.off_b0) : nullptr;
             pa.op[0] = pass(A, p.lda, p.M, p.K, p.k4, p.op_a == TG_OP_T, ap, p.M);
             pa.op[1] = pass(B, p.ldb, p.K, p.N, p.n4, p.op_b == TG_OP_T, bp, p.K);
+            NvtxRange r("tg_prepass");
             prepass_kernel<kPack><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
             if (p.pack_a) {
@@ -1657,12 +1674,14 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
             !make_map(&mB, b_src, p.N, p.K, 4ull * b_row, kFfmaBN, kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE))
             return TG_ERR_CUDA;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
+        NvtxRange r("tg_gemm");
         if (launch_dependent(ffma_gemm_kernel, dim3(p.grid), dim3(kFfmaThreads), kFfmaSmemBytes, stream, 1, mA, mB,
                              ga) != TG_OK)
             return TG_ERR_CUDA;
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
     }
 
+    NvtxRange r("tg_reduce");
     if (p.tail_lanes > 0) {
         const long long work = p.tail_units * p.pair * p.bm * (p.bn / 4);
         if (launch_dependent(tail_reduce_kernel, dim3(elementwise_grid(work, 256)), dim3(256), 0, stream, 1, ga, C,

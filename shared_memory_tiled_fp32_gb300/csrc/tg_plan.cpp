@@ -160,9 +160,10 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         S = (int)std::max<long long>(1, s);
     }
     p->split = S;
-    // 3xTF32: two CTAs of a cluster take vertically adjacent tiles and share
-    // the B tile, each loading half of it for both (TMA multicast), which
-    // halves the B traffic from L2.  TG_TF32X3_PAIR=0 turns this off.
+    // 3xTF32: two CTAs of a cluster take vertically adjacent tiles; the
+    // pair's first CTA issues one M = 256 product over both (cta_group::2),
+    // each CTA holding its A tile and half of the shared B tile, which halves
+    // the B traffic from L2.  TG_TF32X3_PAIR=0 turns this off.
     const char* pair_env = std::getenv("TG_TF32X3_PAIR");
     const bool pair_off = pair_env != nullptr && std::strcmp(pair_env, "0") == 0;
     p->pair = (tensor_path(p->path) && p->tiles_m >= 2 && num_sms >= 2 && !pair_off) ? 2 : 1;

@@ -144,18 +144,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
         : "memory");
 }
 
-// The same, delivered to the same shared-memory offset of every CTA in
-// `cta_mask` (cluster ranks), each signalling its own mbarrier at `bar`'s
-// offset.
-__device__ __forceinline__ void bulk_load_multicast(void* smem_dst, const void* src, uint32_t bytes,
-                                                    uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "h"(cta_mask)
-        : "memory");
-}
-
 // ------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -318,17 +306,10 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
-// As mma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// As mma_commit_multicast for MMAs issued with cta_group::2.
+// As mma_commit for MMAs issued with cta_group::2 (by the pair's first CTA):
+// arrives once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
+// (cluster ranks) when the products have completed.  An arrive on a barrier,
+// not a data copy.
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

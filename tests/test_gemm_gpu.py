@@ -323,7 +323,7 @@ def test_plan_on_device(tg):
 @pytest.mark.parametrize("pair,pair_mma", [("0", "1"), ("1", "0"), ("1", "1")])
 def test_tf32x3_cluster_pairs_on_and_off(tg, pair, pair_mma, path, monkeypatch):
     """The three forms of the 3xTF32 kernel: one CTA per tile; CTA pairs with
-    one M = 128 product per CTA and B multicast to both; CTA pairs with one
+    one M = 128 product per CTA, each CTA loading the whole B tile; CTA pairs with one
     M = 256 product over both (cta_group::2, each CTA holding its half of B)
     -- including odd tile-row counts (the last pair's second CTA is all
     ghost), split K and a stream-K tail."""

@@ -70,6 +70,27 @@ def test_general_integer_bitexact(tg, path, op_a, op_b):
                         f"{path} op=({op_a},{op_b}) s={split}")
 
 
+@pytest.mark.parametrize("path", ["tf32x3", "ffma"])
+def test_general_ragged_alpha_beta(tg, path):
+    """The ragged workload shape (777 x 1029 x 513: no dimension a tile
+    multiple, ldc = 1029 so C rows are not 16-byte aligned) with alpha = 0.5
+    and beta = 1: exercises the scaled epilogue's partial row blocks (fewer
+    than 32 rows, columns past N) on both GEMM kernels, with and without a
+    split of K and with the planner's own choice."""
+    M, N, K = 777, 1029, 513
+    A, B = make_inputs(M, N, K, "uniform", 3)
+    A, B = A.numpy(), B.numpy()
+    C0 = np.random.default_rng(11).uniform(-1, 1, (M, N)).astype(np.float32)
+    ref = oracle.sgemm_general(0, 0, 0.5, A, B, 1.0, C0.copy())
+    for split in (0, 1, 2):
+        got = gpu_general(tg, 0, 0, 0.5, A, B, 1.0, C0, path=path, split_k=split)
+        assert_close(got, ref, K, f"{path} ragged alpha=0.5 beta=1 s={split}")
+    Ai, Bi = (x.numpy() for x in make_inputs(M, N, K, "int", 12))
+    Ci = np.random.default_rng(13).integers(-9, 10, (M, N)).astype(np.float32)
+    assert_bitexact(gpu_general(tg, 0, 0, 0.5, Ai, Bi, 1.0, Ci, path=path),
+                    oracle.sgemm_general(0, 0, 0.5, Ai, Bi, 1.0, Ci.copy()), f"{path} ragged integers")
+
+
 def test_general_k0_and_beta0_ignores_c(tg):
     M, N = 9, 11
     C0 = np.random.default_rng(7).uniform(-1, 1, (M, N)).astype(np.float32)

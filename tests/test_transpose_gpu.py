@@ -34,6 +34,18 @@ def test_transpose_shapes(tg, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+def test_transpose_full_size(tg, variant):
+    """8192 x 8192 (256 MiB, larger than L2) and 16384 x 1024: every block of
+    the one-wave grid runs many iterations of its grid-stride loop, as in the
+    benchmarked 16384^2 case; the whole output is compared bit for bit."""
+    for i, (r, c) in enumerate([(8192, 8192), (16384, 1024)]):
+        X = np.random.default_rng(40 + i).standard_normal((r, c)).astype(np.float32)
+        got = tg.transpose(torch.from_numpy(X).cuda(), variant=variant)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy().view(np.uint32), oracle.transpose(X).view(np.uint32)), (variant, r, c)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 def test_transpose_strided_with_canaries(tg, variant):
     rows, cols, ld_in, ld_out, guard = 70, 45, 53, 77, 512
     X = np.random.default_rng(4).uniform(-1, 1, (rows, ld_in)).astype(np.float32)
