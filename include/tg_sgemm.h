@@ -133,6 +133,8 @@ typedef struct tg_plan_info {
     int tail_kx;          /* 0: the lanes run the units' K blocks laid end to end (stream-K) or
                              equal K slices; > 0: unit q's first tail_kx K blocks run on lane q,
                              all in step, the rest of every unit over the other lanes */
+    int fused_split;      /* 3xTF32: bit 0 = A, bit 1 = B is staged raw from the caller's buffer and
+                             split into hi/lo inside the GEMM kernel (no pre-pass copy of it) */
 } tg_plan_info;
 
 /* C = A x B with automatic path and split choice (see the file comment for
@@ -277,10 +279,13 @@ tg_status tg_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream)
  * hi/lo copies need 8*(M'+N')*K' bytes, with M' = M rounded up to a multiple
  * of 256 (128 when M <= 128), N' = N rounded up to a multiple of 256 and K' =
  * K rounded up to a multiple of 16 (the split tiles are whole 128-row tiles,
- * paired along M).  Split-K and balanced-tail partials come on top and are
- * dropped when they would not fit.  A product whose split tiles exceed
+ * paired along M); M' is 0 when the GEMM kernel splits A itself (M > 128, A's
+ * base and lda*4 multiples of 16 bytes; see tg_plan_info.fused_split).
+ * Split-K and balanced-tail partials come on top and are dropped when they
+ * would not fit.  A product whose split tiles exceed
  * TG_SGEMM_NOALLOC_SCRATCH_BYTES returns TG_ERR_WORKSPACE_TOO_SMALL and
- * launches nothing (M = N = K = 2048 fits exactly; N = 2049 does not).
+ * launches nothing (M = 2048, N = 4096, K = 2048 with A split in the kernel
+ * fits exactly; N = 4097 does not).
  *
  * The first call on each device does a one-time set-up there (capability
  * check, kernel attributes, and the scratch's device address via

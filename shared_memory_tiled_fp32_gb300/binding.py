@@ -96,6 +96,7 @@ class PlanInfo(ctypes.Structure):
         ("tail_units", ctypes.c_longlong),
         ("tail_lanes", ctypes.c_int),
         ("tail_kx", ctypes.c_int),
+        ("fused_split", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -111,13 +111,15 @@ void fill_info(const Plan& p, tg_plan_info* out) {
     out->tiles_n = p.tiles_n;
     out->units = p.units;
     out->grid = p.grid;
-    out->prepass = (tensor_path(p.path) && !p.zero_fill && p.M > 0 && p.N > 0) || p.pack_a || p.pack_b;
+    out->prepass = (tensor_path(p.path) && !p.zero_fill && p.M > 0 && p.N > 0 && !(p.raw_a && p.raw_b)) ||
+                   p.pack_a || p.pack_b;
     out->launches = p.launches;
     out->workspace_bytes = p.ws_bytes;
     out->pair = p.pair;
     out->tail_units = p.tail_units;
     out->tail_lanes = p.tail_lanes;
     out->tail_kx = p.tail_kx;
+    out->fused_split = (p.raw_a ? 1 : 0) | (p.raw_b ? 2 : 0);
 }
 
 }  // namespace
@@ -267,6 +269,32 @@ struct HostBytes {
     size_t total() const { return a + b + c + b_split + a_split + ws_max; }
 };
 
+// Plan of product (i, j) of a host-buffer call.  The products share B's split
+// tiles, written by the first row block's products, so their layout follows
+// that row block: if its products split A in the kernel (which needs the
+// fused kernel's tile layout for B), so may the others; a later row block
+// that cannot (128 rows or fewer: no CTA pair) splits its own copy of B in
+// its workspace instead of reading the shared one.  If the first row block
+// cannot, no product does.
+tg::Plan host_product_plan(const tg::HostBlocks& hb, int M, int N, int K, int i, int Nj, const void* Ai,
+                           int lda, const void* Bj, int ldb, const void* Cij, int ldc, int path, int split_k,
+                           int num_sms, bool* shared_b) {
+    using namespace tg;
+    const bool tf32 = tensor_path(path);
+    Plan first;
+    make_plan(TG_OP_N, TG_OP_N, hb.rows(0, M), Nj, K, 1.0f, Ai, lda, Bj, ldb, 0.0f, Cij, ldc, path, split_k,
+              num_sms, &first, tf32, tf32);
+    const bool fused_pipe = first.raw_a;
+    Plan pl;
+    make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), Nj, K, 1.0f, Ai, lda, Bj, ldb, 0.0f, Cij, ldc, path, split_k,
+              num_sms, &pl, tf32, tf32, fused_pipe);
+    *shared_b = tf32 && pl.raw_a == fused_pipe;
+    if (tf32 && !*shared_b)  // its own split of B, in its workspace
+        make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), Nj, K, 1.0f, Ai, lda, Bj, ldb, 0.0f, Cij, ldc, path,
+                  split_k, num_sms, &pl, false, tf32, fused_pipe);
+    return pl;
+}
+
 // The column offset and width of block j of row block i.
 void host_block_cols(const tg::HostBlocks& hb, int N, int i, int j, int* j0, int* Nj) {
     if (hb.col_blocks(i) == 1) {
@@ -290,7 +318,7 @@ HostBytes host_bytes(const tg::HostBlocks& hb, int M, int N, int K, int path, in
     r.c = 4ull * M * n4;
     const int mb_max = std::max(hb.first, hb.mb);
     r.b_split = tf32 ? align(8ull * ((N + 255) / 256 * 256) * k16) : 0;
-    r.a_split = tf32 ? align(8ull * ((mb_max + 255) / 256 * 256) * k16) : 0;
+    bool a_split = false;  // some row block's A is split by the pre-pass (not by the kernel)
     // placeholder pointers with the alignment the real ones will have
     const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
     // every product: a row block's shape (its rows, and column blocks or full
@@ -299,11 +327,13 @@ HostBytes host_bytes(const tg::HostBlocks& hb, int M, int N, int K, int path, in
         for (int j = 0; j < hb.col_blocks(i); ++j) {
             int j0 = 0, Nj = 0;
             host_block_cols(hb, N, i, j, &j0, &Nj);
-            Plan pl;
-            make_plan(TG_OP_N, TG_OP_N, hb.rows(i, M), Nj, K, 1.0f, al, (int)k4, al, (int)n4, 0.0f, al, (int)n4,
-                      path, split_k, num_sms, &pl, tf32, tf32);
+            bool shared_b = false;
+            const Plan pl = host_product_plan(hb, M, N, K, i, Nj, al, (int)k4, al, (int)n4, al, (int)n4, path,
+                                              split_k, num_sms, &shared_b);
             r.ws_max = std::max(r.ws_max, pl.ws_bytes);
+            a_split = a_split || (tf32 && !pl.raw_a);
         }
+    r.a_split = a_split ? align(8ull * ((mb_max + 255) / 256 * 256) * k16) : 0;
     return r;
 }
 
@@ -412,14 +442,20 @@ tg_status tg_sgemm_host(int M, int N, int K, const float* A, int lda, const floa
             const float* Ai = fA + (size_t)i0 * k4;
             const float* Bj = fB + j0;
             float* Cij = fC + (size_t)i0 * n4 + j0;
-            Plan pl;
-            make_plan(TG_OP_N, TG_OP_N, Mi, Nj, K, 1.0f, Ai, (int)k4, Bj, (int)n4, 0.0f, Cij, (int)n4, path,
-                      o.split_k, d->num_sms, &pl, tf32, tf32);
-            if (tf32) {  // A_i split by its first product (j == 0), B_j by its first (i == 0)
-                pl.ext_a = a_cat;
-                pl.a_ready = j > 0;
-                pl.ext_b = b_cat + (size_t)j0 * 2 * k16;
-                pl.b_ready = i > 0;
+            bool shared_b = false;
+            Plan pl = host_product_plan(hb, M, N, K, i, Nj, Ai, (int)k4, Bj, (int)n4, Cij, (int)n4, path,
+                                        o.split_k, d->num_sms, &shared_b);
+            (void)Mi;
+            if (tf32) {  // A_i split by its first product (j == 0), B_j by its first (i == 0);
+                         // an A_i the kernel splits itself is read in place
+                if (!pl.raw_a) {
+                    pl.ext_a = a_cat;
+                    pl.a_ready = j > 0;
+                }
+                if (shared_b) {
+                    pl.ext_b = b_cat + (size_t)j0 * 2 * k16;
+                    pl.b_ready = i > 0;
+                }
             }
             const std::string blk = std::to_string(i) + "," + std::to_string(j) + " (" + std::to_string(Mi) +
                                     " x " + std::to_string(Nj) + ")";

@@ -69,6 +69,12 @@ constexpr int kTailMinK = 512;
 // overall and a 512 MiB one 10 %).
 constexpr long long kTailL2Bytes = 112ll << 20;
 
+// Whether the 3xTF32 kernel splits raw K-major operands itself (TMA copies of
+// the caller's fp32 tile; the raw value is the tensor core's hi operand, since
+// kind::tf32 reads only the top 19 bits, and lo is written beside it in shared
+// memory).  TG_FUSED_SPLIT=0 keeps the pre-pass for every operand.
+bool fused_split_enabled();
+
 struct Plan {
     int M = 0, N = 0, K = 0;
     long long lda = 0, ldb = 0, ldc = 0;
@@ -78,7 +84,12 @@ struct Plan {
     int split = 1;
     int bm = 0, bn = 0, bk = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0;
-    int pair = 1;        // 3xTF32: CTAs per cluster on vertically adjacent tiles (pair MMA)
+    int pair = 1;        // 3xTF32: CTAs per cluster on vertically adjacent tiles
+    bool pair_mma = false;  // 3xTF32 pairs: one M = 256 product over both CTAs (cta_group::2)
+    // 3xTF32 with the pair MMA: an operand stored K-major (A untransposed, B
+    // transposed) with a 16-byte-aligned base and pitch is staged raw by TMA
+    // and split into hi/lo inside the GEMM kernel (no pre-pass copy of it)
+    bool raw_a = false, raw_b = false;
     long long units = 0; // work units (a unit is `pair` vertically adjacent tiles x one K slice)
     // stream-K tail: the tile units past full_units (tail_units of them) are
     // shared out over tail_lanes lanes, each running an equal share of their
@@ -110,7 +121,8 @@ struct Plan {
     // 3xTF32 only: A's split tiles (a_rows x 2*k16 floats; B^T's, b_rows x
     // 2*k16) live outside the workspace at ext_a (ext_b), planned with external_a
     // (external_b); a_ready (b_ready) = it already holds that operand's split,
-    // so the pre-pass skips it (and is not launched if both are)
+    // so the pre-pass skips it (and is not launched if both are).  An operand
+    // the kernel splits itself (raw_a, raw_b) has no split tiles.
     float* ext_a = nullptr;
     float* ext_b = nullptr;
     bool a_ready = false;
@@ -142,9 +154,11 @@ struct HostBlocks {
 HostBlocks choose_host_blocks(int M, int N, int K, int path, int num_sms);
 
 // Fill `p` for the given call; num_sms > 0.  Assumes validate() passed.
+// allow_fuse = false keeps every operand on the pre-pass (raw_a = raw_b =
+// false), for callers that share split tiles between products.
 void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
                const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
-               int num_sms, Plan* p, bool external_b = false, bool external_a = false);
+               int num_sms, Plan* p, bool external_b = false, bool external_a = false, bool allow_fuse = true);
 
 // Enqueue every kernel of plan `p` on `stream` (defined in tg_kernels.cu).
 tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, void* ws,

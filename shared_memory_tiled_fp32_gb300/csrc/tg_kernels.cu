@@ -42,6 +42,7 @@ enum : uint32_t {
     kSiteTfMmaSmem = 0x202,
     kSiteTfMmaTmem = 0x203,
     kSiteTfEpilogue = 0x204,
+    kSiteTfSplit = 0x205,
     kSiteSelftest = 0x301,
 };
 
@@ -526,7 +527,7 @@ template <bool kPairMma>
 struct TfRing {
     static constexpr int kStages = kPairMma ? 6 : kTf32Stages;
     static constexpr uint32_t kStageBytes = kPairMma ? 2 * kTfAStage : kTfStageBytes;
-    static constexpr int kBars = 2 * kStages + 5;
+    static constexpr int kBars = 3 * kStages + 5;
     static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kTfBarBytes + kTfOutStageBytes;
     static_assert(kBars * 8 + 16 <= (int)kTfBarBytes, "barriers and the tensor-memory slot fit");
     static_assert(kSmemBytes <= 232448, "fits the 227 KiB of shared memory a block may opt in to");
@@ -534,14 +535,61 @@ struct TfRing {
 constexpr size_t kTfSmemBytes = TfRing<false>::kSmemBytes;
 constexpr size_t kTfSmemBytesPairMma = TfRing<true>::kSmemBytes;
 
+// Raw operands (split in the kernel, pair-MMA form only).  An operand stored
+// K-major (A as M x K, B as N x K) is copied by TMA straight from the
+// caller's buffer: one box of 16 K values x 128 rows (8 KiB, 64-byte rows,
+// 64-byte swizzle: the tensor core's K-major SW64 layout), rows and K past
+// the matrix read as zeros (the ghost elements).  The raw fp32 value is the
+// hi operand as it stands: kind::tf32 reads only its sign, exponent and top
+// 10 mantissa bits, i.e. hi = x truncated to tf32 (verified on this GPU).
+// Two warps of each CTA then write lo = tf32(x - trunc(x)) (x - trunc(x) is
+// exact in fp32) beside it, in the same layout 8 KiB further on, so the 16
+// KiB region of the operand in a stage holds [raw | lo] instead of the
+// pre-pass's 16 KiB hi/lo tile.  The split is elementwise, so it needs no
+// knowledge of the swizzle.
+constexpr uint32_t kRawTileBytes = kTf32BM * kTf32BK * 4;  // 8 KiB
+constexpr uint32_t kSwRowGroupBytes64 = 8 * 64;            // 8 rows of the 64-byte swizzle atom
+constexpr uint32_t kDescSwizzle64 = 4;
+static_assert(2 * kRawTileBytes == kTfAStage, "raw tile + lo fill one operand region of a stage");
+
+// lo = tf32(x - trunc_tf32(x)) of four values.
+__device__ __forceinline__ float4 split_lo4(float4 x) {
+    auto lo = [](float v) {
+        return to_tf32(v - __uint_as_float(__float_as_uint(v) & 0xffffe000u));
+    };
+    return make_float4(lo(x.x), lo(x.y), lo(x.z), lo(x.w));
+}
+
+// The 64 threads t = 0..63 of the split warps write the lo half of one raw
+// operand region (512 16-byte groups, 8 per thread; consecutive threads take
+// consecutive groups, so every warp access is conflict-free).
+__device__ __forceinline__ void split_raw_tile(uint8_t* region, int t) {
+    const float4* src = reinterpret_cast<const float4*>(region);
+    float4* dst = reinterpret_cast<float4*>(region + kRawTileBytes);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = src[t + 64 * (4 * h + u)];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[t + 64 * (4 * h + u)] = split_lo4(v[u]);
+    }
+}
+
 // kMixed: the operand tiles hold tf32 hi and bf16 hi / lo (the pre-pass's
 // kSplitBf16 layout) and each 16-wide K block takes two tf32 hi x hi products
 // and two bf16 cross products (hi x lo, lo x hi) instead of six tf32 ones.
-template <int kPair, bool kPairMma, bool kMixed = false>
+// kRawA / kRawB (pair MMA, 3xTF32): that operand is staged raw and split in
+// the kernel (see kRawTileBytes); tmA / tmB then map the caller's matrix.  A
+// split-tile operand of such a kernel comes in the pre-pass's kSplitTf32H
+// layout, so both operands are read with the 64-byte-swizzle descriptors.
+template <int kPair, bool kPairMma, bool kMixed = false, bool kRawA = false, bool kRawB = false>
 __global__ void __launch_bounds__(kTfThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        GemmArgs args) {
     static_assert(!kPairMma || kPair == 2, "the pair MMA needs a CTA pair");
+    constexpr bool kRaw = kRawA || kRawB;
+    static_assert(!kRaw || (kPairMma && !kMixed), "raw operands: pair-MMA 3xTF32 form only");
     constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK;
     constexpr int ST = TfRing<kPairMma>::kStages;
     constexpr uint32_t kStageBytes = TfRing<kPairMma>::kStageBytes;
@@ -552,7 +600,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     uint64_t* tfull = empty + ST;  // [2] chunk accumulated
     uint64_t* tempty = tfull + 2;  // [2] chunk drained by the epilogue
     uint64_t* drain = tempty + 2;  // every MMA of this CTA completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* rfull = drain + 1;   // [ST] this CTA's raw operand tiles landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + ST);
     float* out_stage = reinterpret_cast<float*>(smem + ST * kStageBytes + kTfBarBytes);  // [8 warps][32 x 32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -568,9 +617,12 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
-            mbar_init(&full[s], 1);
+            // the first CTA's copy thread, plus, with raw operands, the two
+            // split warps of each CTA of the pair
+            mbar_init(&full[s], kRaw ? 1 + 2 * kPair : 1);
             // one MMA commit: this CTA's own, or the pair MMA's (which arrives in both CTAs)
             mbar_init(&empty[s], 1);
+            mbar_init(&rfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -614,13 +666,24 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                     }
                     uint8_t* st = smem + stage * kStageBytes;
                     if (kPairMma) {
-                        // this CTA's A tile and B half into its own ring; both
-                        // CTAs' copies complete on the first CTA's "full"
-                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                        // this CTA's A tile and B half into its own ring.  Both
+                        // CTAs' split-tile copies complete on the first CTA's
+                        // "full"; a raw tile completes on this CTA's "rfull",
+                        // where the split warps pick it up
+                        constexpr uint32_t kPairTx = 2 * ((kRawA ? 0 : kTfAStage) + (kRawB ? 0 : kTfAStage));
+                        constexpr uint32_t kRawTx = (kRawA ? kRawTileBytes : 0) + (kRawB ? kRawTileBytes : 0);
+                        if (kRaw) mbar_arrive_expect_tx(&rfull[stage], kRawTx);
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], kPairTx);
                         const uint32_t bar0 = cluster_addr(&full[stage], 0);
-                        tma_load_2d_pair(st, &tmA, bar0, 0, ((t.m0 >> 7) * args.kbs + kb) * 128);
-                        tma_load_2d_pair(st + kTfAStage, &tmB, bar0, 0,
-                                         (((t.n0 >> 7) + rank) * args.kbs + kb) * 128);
+                        if (kRawA)
+                            tma_load_2d(st, &tmA, &rfull[stage], kb * BK, t.m0);
+                        else
+                            tma_load_2d_pair(st, &tmA, bar0, 0, ((t.m0 >> 7) * args.kbs + kb) * 128);
+                        if (kRawB)
+                            tma_load_2d(st + kTfAStage, &tmB, &rfull[stage], kb * BK, t.n0 + rank * BM);
+                        else
+                            tma_load_2d_pair(st + kTfAStage, &tmB, bar0, 0,
+                                             (((t.n0 >> 7) + rank) * args.kbs + kb) * 128);
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == ST) {
@@ -651,16 +714,54 @@ __global__ void __launch_bounds__(kTfThreads, 1)
             // stages ("empty" completes only after the copies landed).
             for (int s = 0; s < ST; ++s) {
                 if (!((issued >> s) & 1u)) continue;
+                if (kRaw) mbar_drain(&rfull[s], (last_par >> s) & 1u, args.timeout_ns);
                 if (issuer)
                     mbar_drain(&full[s], (last_par >> s) & 1u, args.timeout_ns);
                 else
                     mbar_drain(&empty[s], (last_par >> s) & 1u, args.timeout_ns);
+            }
+        } else if (kRaw && (warp == 2 || warp == 3)) {  // ------------- split of raw tiles
+            // per stage: wait for this CTA's raw tiles, write their lo halves,
+            // publish them to the tensor core (async proxy) and arrive on the
+            // first CTA's "full" barrier, where the MMA thread waits
+            const int t64 = threadIdx.x - 64;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            Unit t;
+            for (long long j = 0; ok && work_item<true, false>(args, first_unit, unit_stride, j, rank, BM, BN, &t); ++j) {
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    const bool got = mbar_wait(&rfull[stage], phase, wc, kSiteTfSplit);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * kStageBytes;
+                    if (kRawA) split_raw_tile(st, t64);
+                    if (kRawB) split_raw_tile(st + kTfAStage, t64);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(cluster_addr(&full[stage], 0));
+                    if (++stage == ST) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
             }
         } else if (warp == 1 && lane == 0 && issuer) {  // ---------------- MMA issuer
             constexpr uint32_t idesc = idesc_tf32(kPairMma ? 2 * BM : BM, BN);
             constexpr uint32_t idesc_x = idesc_bf16(kPairMma ? 2 * BM : BM, BN);
             static_assert(BK == 16 && kTfRowBytes == 128, "the issue loop below is written for two 8-wide slices");
             const uint64_t desc_stage0 = smem_desc_kmajor(smem_addr(smem), kSwRowGroupBytes, kDescSwizzle128);
+            // operand descriptors of stage 0 and the offset (16-byte units) of
+            // the lo halves: a kSplitTf32 tile holds hi and lo in one 128-byte
+            // swizzled row (lo +64 bytes); with raw operands every operand
+            // region holds hi (or the raw tile) in 64-byte swizzled rows and
+            // lo 8 KiB on.  The second 8-wide K slice is +32 bytes either way.
+            constexpr uint32_t kLo = kRaw ? kRawTileBytes >> 4 : 4;
+            const uint64_t desc_a0 =
+                kRaw ? smem_desc_kmajor(smem_addr(smem), kSwRowGroupBytes64, kDescSwizzle64) : desc_stage0;
+            const uint64_t desc_b0 = desc_a0 + (kTfAStage >> 4);
             int stage = 0;
             uint32_t phase = 0, chunk = 0;
             bool ok = true;
@@ -676,7 +777,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + buf * BN;
                     for (int kb = c0; kb < c1; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, wc, kSiteTfMmaSmem)) {
+                        // raw operands: the split warps of both CTAs arrive
+                        // after writing shared memory the products read
+                        if (!(kRaw ? mbar_wait_cluster(&full[stage], phase, wc, kSiteTfMmaSmem)
+                                   : mbar_wait(&full[stage], phase, wc, kSiteTfMmaSmem))) {
                             ok = false;
                             break;
                         }
@@ -710,12 +814,14 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         }
                         if (kPairMma) {  // M = 256 over the pair: each CTA's A rows and B half
                             const uint32_t acc = kb > c0 ? 1u : 0u;
-                            mma_tf32_ss_pair(d_tmem, da, db + 4, idesc, acc);
-                            mma_tf32_ss_pair(d_tmem, da, db, idesc, 1u);
-                            mma_tf32_ss_pair(d_tmem, da + 4, db, idesc, 1u);
-                            mma_tf32_ss_pair(d_tmem, da + 2, db + 6, idesc, 1u);
-                            mma_tf32_ss_pair(d_tmem, da + 2, db + 2, idesc, 1u);
-                            mma_tf32_ss_pair(d_tmem, da + 6, db + 2, idesc, 1u);
+                            const uint64_t pa = desc_a0 + (uint64_t)stage * (kStageBytes >> 4);
+                            const uint64_t pb = desc_b0 + (uint64_t)stage * (kStageBytes >> 4);
+                            mma_tf32_ss_pair(d_tmem, pa, pb + kLo, idesc, acc);
+                            mma_tf32_ss_pair(d_tmem, pa, pb, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, pa + kLo, pb, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, pa + 2, pb + kLo + 2, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, pa + 2, pb + 2, idesc, 1u);
+                            mma_tf32_ss_pair(d_tmem, pa + kLo + 2, pb + 2, idesc, 1u);
                             mma_commit_pair(&empty[stage], kPairMask);
                             if (++stage == ST) {
                                 stage = 0;
@@ -921,20 +1027,30 @@ __device__ __forceinline__ float4 load_row4(const float* src, long long ld, int 
 // Pre-pass modes: kPack copies (FFMA: op(A) -> [M][k4], op(B) -> [K][n4]);
 // kSplitTf32 writes hi = tf32(x) and lo = tf32(x - hi) (3xTF32); kSplitBf16
 // writes hi = tf32(x) and the bf16 roundings of hi and of x - hi (the
-// bf16-cross-product path).  Both split modes fill 128-byte tile rows of
-// eight 16-byte groups, group g of row r stored at position g ^ (r % 8):
+// bf16-cross-product path).  Both fill 128-byte tile rows of eight 16-byte
+// groups, group g of row r stored at position g ^ (r % 8) (128-byte swizzle):
 // kSplitTf32: groups 0-3 hi of K values 4g..4g+3, groups 4-7 their lo;
 // kSplitBf16: groups 0-3 hi (tf32), group 4 / 5 bf16(hi) of K values 0-7 /
 // 8-15, group 6 / 7 bf16(lo) of the same.
-constexpr int kPack = 0, kSplitTf32 = 1, kSplitBf16 = 2;
+// kSplitTf32H writes the same hi and lo as kSplitTf32 in the layout of a raw
+// operand region of the fused kernel: the tile's first 8 KiB hold hi, 64-byte
+// rows of 16 K values with the 64-byte swizzle (group g of row r at position
+// g ^ ((r / 2) % 4)), the second 8 KiB lo in the same places.  The pair MMA
+// reads both operands of a product in one swizzle mode (measured on GB300: an
+// A tile in the 64-byte and a B tile in the 128-byte swizzle gave wrong
+// products in the cta_group::2 form, though not with one CTA), so a product
+// whose other operand is split in the kernel takes this layout.
+constexpr int kPack = 0, kSplitTf32 = 1, kSplitBf16 = 2, kSplitTf32H = 3;
 
 // Offset of destination element (r, c): hi in its swizzled tile (split
 // modes) or the plain padded row (kPack).
 template <int MODE>
 __device__ __forceinline__ long long dst_offset(int pitch, int r, int c) {
+    const long long tile = ((long long)(r >> 7) * (pitch >> 4) + (c >> 4)) * 4096;
+    if (MODE == kSplitTf32H)
+        return tile + (r & 127) * 16 + ((((c & 15) >> 2) ^ ((r >> 1) & 3)) << 2) + (c & 3);
     if (MODE != kPack)
-        return ((long long)(r >> 7) * (pitch >> 4) + (c >> 4)) * 4096 + (r & 127) * 32 +
-               ((((c & 15) >> 2) ^ (r & 7)) << 2) + (c & 3);
+        return tile + (r & 127) * 32 + ((((c & 15) >> 2) ^ (r & 7)) << 2) + (c & 3);
     return (long long)r * pitch + c;
 }
 
@@ -974,7 +1090,10 @@ __device__ __forceinline__ void store_split4(float* d0, long long o, float4 x) {
     }
     const float4 hi = make_float4(split_hi(x.x), split_hi(x.y), split_hi(x.z), split_hi(x.w));
     *reinterpret_cast<float4*>(d0 + o) = hi;
-    if (MODE == kSplitTf32) {
+    if (MODE == kSplitTf32H) {
+        *reinterpret_cast<float4*>(d0 + o + 2048) =
+            make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
+    } else if (MODE == kSplitTf32) {
         *reinterpret_cast<float4*>(d0 + (o ^ 16)) =
             make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
     } else {
@@ -1448,19 +1567,9 @@ tg_status launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 
 // Resident 256-thread blocks per SM of the two pre-pass kernels (the grid is
 // sized to exactly fill the GPU once).
-int g_prepass_blocks_per_sm[3] = {4, 4, 4};
+int g_prepass_blocks_per_sm[4] = {4, 4, 4, 4};
 // CTA pairs of the 3xTF32 kernel resident at once (0 = unknown).
 int g_tf32_pair_clusters = 0;
-
-// CTA pairs issue one M = 256 tensor-core product over both CTAs
-// (cta_group::2), each CTA holding its A tile and its half of B, so the ring
-// has 6 stages instead of 4 (measured: 3xTF32 steps 2.8-3.5 % faster at
-// 4096^3, 8192^3 and 2048 x 2048 x 16384).  TG_TF32X3_PAIRMMA=0 keeps one
-// M = 128 product per CTA, each CTA loading the whole B tile itself.
-bool pair_mma_enabled() {
-    const char* e = std::getenv("TG_TF32X3_PAIRMMA");
-    return !(e != nullptr && e[0] == '0');
-}
 
 tg_status prepare_device_kernels() {
     int nb = 0;
@@ -1472,6 +1581,9 @@ tg_status prepare_device_kernels() {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<kSplitBf16>, 256, 0) == cudaSuccess &&
         nb > 0)
         g_prepass_blocks_per_sm[kSplitBf16] = nb;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<kSplitTf32H>, 256, 0) == cudaSuccess &&
+        nb > 0)
+        g_prepass_blocks_per_sm[kSplitTf32H] = nb;
     // The warpgroup register splits of both GEMM kernels only balance when the
     // kernels are launched with exactly the register counts they were designed
     // for; refuse to run a build that differs.
@@ -1487,6 +1599,9 @@ tg_status prepare_device_kernels() {
     } tf_kernels[] = {{tf32x3_gemm_kernel<1, false>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, false>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, true>, kTfSmemBytesPairMma},
+                      {tf32x3_gemm_kernel<2, true, false, true, false>, kTfSmemBytesPairMma},
+                      {tf32x3_gemm_kernel<2, true, false, false, true>, kTfSmemBytesPairMma},
+                      {tf32x3_gemm_kernel<2, true, false, true, true>, kTfSmemBytesPairMma},
                       {tf32x3_gemm_kernel<1, false, true>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, false, true>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, true, true>, kTfSmemBytesPairMma}};
@@ -1603,19 +1718,24 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     PrepassArgs pa{};
     // one full wave of resident blocks keeps HBM busy without a tail
     const bool mixed = p.path == TG_PATH_TF32_BF16;
-    const int mode = mixed ? kSplitBf16 : (p.path == TG_PATH_TF32X3 ? kSplitTf32 : kPack);
+    const int mode = mixed ? kSplitBf16
+                           : (p.path == TG_PATH_TF32X3 ? ((p.raw_a || p.raw_b) ? kSplitTf32H : kSplitTf32) : kPack);
     const int prepass_grid = g_prepass_blocks_per_sm[mode] * p.num_sms;
 
     if (tensor_path(p.path)) {
-        float* a_tiles = p.ext_a ? p.ext_a : reinterpret_cast<float*>(w + p.off_a0);
-        float* b_tiles = p.ext_b ? p.ext_b : reinterpret_cast<float*>(w + p.off_b0);
+        float* a_tiles = p.raw_a ? nullptr : (p.ext_a ? p.ext_a : reinterpret_cast<float*>(w + p.off_a0));
+        float* b_tiles = p.raw_b ? nullptr : (p.ext_b ? p.ext_b : reinterpret_cast<float*>(w + p.off_b0));
         // split tiles: A [a_rows/128][k16/16] from op(A); B [b_rows/128][k16/16] from op(B)^T
-        pa.op[0] = pass(A, p.lda, p.M, p.K, p.k16, p.op_a == TG_OP_T, p.a_ready ? nullptr : a_tiles, p.a_rows);
-        pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, p.b_ready ? nullptr : b_tiles, p.b_rows);
-        if (!(p.a_ready && p.b_ready)) {
+        // (none for an operand the kernel splits itself)
+        const bool need_a = !p.raw_a && !p.a_ready, need_b = !p.raw_b && !p.b_ready;
+        pa.op[0] = pass(A, p.lda, p.M, p.K, p.k16, p.op_a == TG_OP_T, need_a ? a_tiles : nullptr, p.a_rows);
+        pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, need_b ? b_tiles : nullptr, p.b_rows);
+        if (need_a || need_b) {
             NvtxRange r("tg_prepass");
             if (mixed)
                 prepass_kernel<kSplitBf16><<<prepass_grid, 256, 0, stream>>>(pa);
+            else if (mode == kSplitTf32H)
+                prepass_kernel<kSplitTf32H><<<prepass_grid, 256, 0, stream>>>(pa);
             else
                 prepass_kernel<kSplitTf32><<<prepass_grid, 256, 0, stream>>>(pa);
             if (last_launch_status() != TG_OK) return TG_ERR_CUDA;
@@ -1624,21 +1744,34 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         ga.b_tiles = b_tiles;
         ga.kbs = p.k16 / 16;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
-        // the pair-MMA form reads the tiles through 2-D tensor maps: rows of
-        // 32 floats (one tile row, hi and lo), boxes of one 128-row tile
+        // the pair-MMA form reads the split tiles through 2-D tensor maps: rows
+        // of 32 floats (one tile row, hi and lo), boxes of one 128-row tile
+        // (the plan keeps the per-CTA form when these 32-bit row coordinates
+        // would overflow); a raw operand through a map of the caller's matrix,
+        // stored K-major: boxes of 16 K values x 128 rows, 64-byte swizzle,
+        // zeros past the edges
         CUtensorMap mA{}, mB{};
-        // (tile-row coordinates are 32-bit: larger arrays keep the per-CTA form)
-        const bool pair_mma = p.pair == 2 && pair_mma_enabled() && (long long)p.a_rows * ga.kbs < (1ll << 31) &&
-                              (long long)p.b_rows * ga.kbs < (1ll << 31);
-        if (pair_mma &&
-            (!make_map(&mA, a_tiles, 32, (uint64_t)p.a_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-             !make_map(&mB, b_tiles, 32, (uint64_t)p.b_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
-            return TG_ERR_CUDA;
+        const bool pair_mma = p.pair_mma;
+        if (pair_mma) {
+            const bool ok_a =
+                p.raw_a ? make_map(&mA, A, p.K, p.M, 4ull * p.lda, kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_64B)
+                        : make_map(&mA, a_tiles, 32, (uint64_t)p.a_rows * ga.kbs, 128, 32, 128,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+            const bool ok_b =
+                p.raw_b ? make_map(&mB, B, p.K, p.N, 4ull * p.ldb, kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_64B)
+                        : make_map(&mB, b_tiles, 32, (uint64_t)p.b_rows * ga.kbs, 128, 32, 128,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (!ok_a || !ok_b) return TG_ERR_CUDA;
+        }
         int clusters = p.grid / 2;
         if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
         NvtxRange r("tg_gemm");
         void (*kern)(CUtensorMap, CUtensorMap, GemmArgs);
-        if (p.pair == 2)
+        if (p.pair == 2 && pair_mma && !mixed && (p.raw_a || p.raw_b))
+            kern = p.raw_a ? (p.raw_b ? tf32x3_gemm_kernel<2, true, false, true, true>
+                                      : tf32x3_gemm_kernel<2, true, false, true, false>)
+                           : tf32x3_gemm_kernel<2, true, false, false, true>;
+        else if (p.pair == 2)
             kern = pair_mma ? (mixed ? tf32x3_gemm_kernel<2, true, true> : tf32x3_gemm_kernel<2, true>)
                             : (mixed ? tf32x3_gemm_kernel<2, false, true> : tf32x3_gemm_kernel<2, false>);
         else

@@ -32,8 +32,9 @@ bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
     return a0 < b1 && b0 < a1;
 }
 
-// Bytes of the 3xTF32 operand copies (A_hi, A_lo rows; B_hi, B_lo columns)
-// that the last `rem` tile units of the raster read.
+// Bytes of the 3xTF32 operands (hi/lo copies: 8 bytes per element; raw
+// operands split in the kernel: 4) that the last `rem` tile units of the
+// raster read.
 long long tail_operand_bytes(const Plan& p, long long rem) {
     const int prow = (int)cdiv(p.tiles_m, p.pair);
     const long long units = (long long)prow * p.tiles_n;
@@ -51,7 +52,7 @@ long long tail_operand_bytes(const Plan& p, long long rem) {
     long long rows = 0, cols = 0;
     for (int i : rows_seen) rows += std::min<long long>((long long)p.pair * p.bm, p.M - (long long)i * p.pair * p.bm);
     for (int j : cols_seen) cols += std::min<long long>(p.bn, p.N - (long long)j * p.bn);
-    return (rows + cols) * p.k16 * 8;
+    return (rows * (p.raw_a ? 4 : 8) + cols * (p.raw_b ? 4 : 8)) * p.k16;
 }
 
 // Whether the one-launch tiled path beats the 3xTF32 path's pre-pass, GEMM
@@ -62,6 +63,11 @@ bool tiled_is_faster(int M, int N, int K, int num_sms) {
 }
 
 }  // namespace
+
+bool fused_split_enabled() {
+    const char* e = std::getenv("TG_FUSED_SPLIT");
+    return !(e != nullptr && e[0] == '0');
+}
 
 tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int lda, const void* B,
                    int ldb, const void* C, int ldc, int path, int split_k, bool need_pointers) {
@@ -97,7 +103,7 @@ tg_status validate(int op_a, int op_b, int M, int N, int K, const void* A, int l
 
 void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
                const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
-               int num_sms, Plan* p, bool external_b, bool external_a) {
+               int num_sms, Plan* p, bool external_b, bool external_a, bool allow_fuse) {
     *p = Plan{};
     p->M = M;
     p->N = N;
@@ -167,6 +173,27 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     const char* pair_env = std::getenv("TG_TF32X3_PAIR");
     const bool pair_off = pair_env != nullptr && std::strcmp(pair_env, "0") == 0;
     p->pair = (tensor_path(p->path) && p->tiles_m >= 2 && num_sms >= 2 && !pair_off) ? 2 : 1;
+    if (tensor_path(p->path)) {
+        // split tiles of 128 rows x (16 hi + 16 lo): A's rows padded to whole
+        // units (pair x 128), B^T's to whole 256-row B tiles
+        p->a_rows = (int)round_up((size_t)M, 128 * (size_t)p->pair);
+        p->b_rows = (int)round_up((size_t)N, 256);
+        // CTA pairs issue one M = 256 product over both CTAs unless
+        // TG_TF32X3_PAIRMMA=0, or the tile arrays' row coordinates (32-bit in
+        // the tensor maps) would overflow
+        const char* pm_env = std::getenv("TG_TF32X3_PAIRMMA");
+        const long long kbs = p->k16 / 16;
+        p->pair_mma = p->pair == 2 && !(pm_env != nullptr && pm_env[0] == '0') &&
+                      (long long)p->a_rows * kbs < (1ll << 31) && (long long)p->b_rows * kbs < (1ll << 31);
+        // raw operands: stored K-major (A as M x K, B as N x K), base and row
+        // pitch on 16-byte boundaries (TMA), pair-MMA 3xTF32 kernel
+        auto tma_legal = [](const void* X, int ld) {
+            return X != nullptr && reinterpret_cast<uintptr_t>(X) % 16 == 0 && ld % 4 == 0;
+        };
+        const bool fuse = allow_fuse && p->pair_mma && p->path == TG_PATH_TF32X3 && fused_split_enabled();
+        p->raw_a = fuse && op_a == TG_OP_N && tma_legal(A, lda);
+        p->raw_b = fuse && op_b == TG_OP_T && tma_legal(B, ldb);
+    }
     p->units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n * S;
     const long long cap = num_sms / p->pair;  // units in flight at once (lanes)
     p->grid = p->pair * (int)std::min<long long>(p->units, cap);
@@ -236,12 +263,10 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         return at;
     };
     if (tensor_path(p->path)) {
-        // split tiles of 128 rows x (16 hi + 16 lo): A's rows padded to whole
-        // units (pair x 128), B^T's to whole 256-row B tiles
-        p->a_rows = (int)round_up((size_t)M, 128 * (size_t)p->pair);
-        p->b_rows = (int)round_up((size_t)N, 256);
-        if (!external_a) p->off_a0 = take(8ull * p->a_rows * p->k16);  // else the caller provides them
-        if (!external_b) p->off_b0 = take(8ull * p->b_rows * p->k16);
+        // the split tiles of each operand not split in the kernel, unless the
+        // caller provides them
+        if (!external_a && !p->raw_a) p->off_a0 = take(8ull * p->a_rows * p->k16);
+        if (!external_b && !p->raw_b) p->off_b0 = take(8ull * p->b_rows * p->k16);
     } else {
         // TMA reads the operands in place when they are stored untransposed,
         // their base is 16-byte aligned and their row pitch a multiple of 16
@@ -264,7 +289,7 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->off_tail = take(4ull * slots * p->pair * p->bm * p->bn);
     }
     p->ws_bytes = off;
-    const bool prepass = tensor_path(p->path) || p->pack_a || p->pack_b;
+    const bool prepass = (tensor_path(p->path) && !(p->raw_a && p->raw_b)) || p->pack_a || p->pack_b;
     p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_lanes > 0 ? 1 : 0);
 }
 
@@ -368,8 +393,8 @@ class HostModel {
             for (int j = 0; j < nc; ++j) {
                 const int cols = nc == 1 ? N_ : std::min(hb.nb, N_ - j * hb.nb);
                 double sec = product(rows, cols);
-                if (tf32_) {
-                    if (j == 0) sec += 12.0 * rows * K_ / bw_split;
+                if (tf32_) {  // the split passes: A_i's only when the kernel does not split it
+                    if (j == 0 && !raw_a(rows, cols)) sec += 12.0 * rows * K_ / bw_split;
                     if (i == 0) sec += 12.0 * cols * K_ / bw_split;
                 }
                 prods_.push_back({i, nc == 1 ? hb.pn - 1 : j, sec, 4.0 * rows * cols + out_fixed_bytes});
@@ -379,21 +404,27 @@ class HostModel {
     }
 
   private:
-    double product(int rows, int cols) {
-        auto it = product_s_.find({rows, cols});
-        if (it != product_s_.end()) return it->second;
+    Plan plan(int rows, int cols) const {
         const void* al = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
         const int k4 = (int)round_up((size_t)std::max(K_, 1), 4), n4 = (int)round_up((size_t)std::max(N_, 1), 4);
         Plan pl;
         make_plan(TG_OP_N, TG_OP_N, rows, cols, K_, 1.0f, al, k4, al, n4, 0.0f, al, n4, path_, 0, sms_, &pl,
                   tf32_, tf32_);
-        const double t = product_seconds(pl, path_ == TG_PATH_TF32_BF16 ? 525e12 : (tf32_ ? 375e12 : 62e12));
-        product_s_[{rows, cols}] = t;
-        return t;
+        return pl;
     }
+    // (modelled seconds, whether the kernel splits A itself) of one product
+    const std::pair<double, bool>& product_info(int rows, int cols) {
+        auto it = product_s_.find({rows, cols});
+        if (it != product_s_.end()) return it->second;
+        const Plan pl = plan(rows, cols);
+        const double t = product_seconds(pl, path_ == TG_PATH_TF32_BF16 ? 525e12 : (tf32_ ? 375e12 : 62e12));
+        return product_s_[{rows, cols}] = {t, pl.raw_a};
+    }
+    double product(int rows, int cols) { return product_info(rows, cols).first; }
+    bool raw_a(int rows, int cols) { return product_info(rows, cols).second; }
     int M_, N_, K_, path_, sms_;
     bool tf32_;
-    std::map<std::pair<int, int>, double> product_s_;  // by (rows, columns)
+    std::map<std::pair<int, int>, std::pair<double, bool>> product_s_;  // by (rows, columns)
     std::vector<HostCopy> ins_;
     std::vector<HostProduct> prods_;
 };

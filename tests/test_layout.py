@@ -178,6 +178,50 @@ def test_split_tile_layouts_cover_each_slot_once(rows, pitch):
     assert all(v == 1 for v in mixed)
 
 
+def split_tile_h_offset(pitch, r, c):
+    """dst_offset of the kSplitTf32H pre-pass mode, in floats: 16 KiB tiles
+    [r / 128][c / 16]; hi in the first 8 KiB as rows of 16 floats, 16-byte
+    group (c % 16) / 4 at position group ^ ((r / 2) % 4); lo 2048 floats on."""
+    return ((r >> 7) * (pitch >> 4) + (c >> 4)) * 4096 + (r & 127) * 16 + \
+        ((((c & 15) >> 2) ^ ((r >> 1) & 3)) << 2) + (c & 3)
+
+
+def tma_swizzle_64(addr):
+    """Where a 64-byte-swizzled TMA copy puts the byte at logical offset addr
+    of its box (rows of 64 bytes, 512-byte aligned base): the 16-byte chunk
+    index (address bits 4-5) is XORed with bits 7-8."""
+    return addr ^ (((addr >> 7) & 3) << 4)
+
+
+@pytest.mark.parametrize("rows,pitch", [(300, 64), (128, 16)])
+def test_split_tile_h_matches_raw_tma_layout(rows, pitch):
+    """The fused kernel reads pre-split operands and raw TMA tiles with the
+    same descriptors, so the kSplitTf32H hi half must sit exactly where a
+    64-byte-swizzled TMA box of the same 128 x 16 block puts the raw values,
+    and hi + lo must cover each byte of the padded tiles once."""
+    padded = -(-rows // 128) * 128
+    total = padded // 128 * (pitch // 16) * 4096
+    seen = [0] * total
+    for r in range(padded):
+        for c in range(pitch):
+            o = split_tile_h_offset(pitch, r, c)
+            tile = ((r >> 7) * (pitch >> 4) + (c >> 4)) * 4096
+            assert 4 * (o - tile) == tma_swizzle_64(64 * (r & 127) + 4 * (c & 15))
+            seen[o] += 1
+            seen[o + 2048] += 1
+    assert all(v == 1 for v in seen)
+
+
+def test_fused_split_warps_access_conflict_free():
+    """The split warps of the fused kernel move a raw 8 KiB tile to its lo
+    half as 512 16-byte groups, thread t (0..63) taking t + 64u: each warp
+    access covers 512 contiguous bytes, the minimum four wavefronts."""
+    for u in range(8):
+        for warp in range(2):
+            addrs = [16 * (32 * warp + lane + 64 * u) for lane in range(32)]
+            assert wavefronts_128(addrs) == min_wavefronts_128(addrs) == 4
+
+
 # ------------------------------------------------------- transpose workload
 
 

@@ -41,20 +41,33 @@ def _noalloc(L, A, B, C, stream):
                               C.data_ptr(), C.stride(0), ctypes.c_void_p(stream.cuda_stream))
 
 
-def _scratch_bytes(M, N, K):
+def _scratch_bytes(M, N, K, a_in_kernel):
     """The hi/lo split tiles: rows padded to whole 256-row tile pairs (128 for
-    a single tile row), K to a multiple of 16, 8 bytes per element."""
+    a single tile row), K to a multiple of 16, 8 bytes per element; none for
+    A when the GEMM kernel splits it itself (A's base and row pitch 16-byte
+    aligned, more than one 128-row tile)."""
     rup = lambda x, m: -(-x // m) * m
-    return 8 * ((rup(M, 256) if M > 128 else 128) + rup(N, 256)) * rup(K, 16)
+    a_rows = 0 if a_in_kernel else (rup(M, 256) if M > 128 else 128)
+    return 8 * (a_rows + rup(N, 256)) * rup(K, 16)
 
 
-# (2048, 2048, 2048): the split tiles fill the 64 MiB exactly, so the
-# planner's balanced-tail partials do not fit and the call re-plans without them
-@pytest.mark.parametrize("M,N,K", [(777, 1029, 513), (1024, 1024, 1024), (130, 300, 2000), (2048, 2048, 2048)])
-def test_noalloc_matches_allocating_entry_and_oracle(lib, M, N, K):
+def _a_in_kernel(M, K, fused):
+    return fused and M > 128 and K % 4 == 0
+
+
+# At the 64 MiB limit exactly (the planner's balanced-tail partials then do
+# not fit, so the call re-plans without them): 2048^3 with A split by the
+# pre-pass, 2048 x 4096 x 2048 with A split in the kernel.
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("M,N,K", [(777, 1029, 513), (1024, 1024, 1024), (130, 300, 2000), (2048, 2048, 2048),
+                                   (2048, 4096, 2048)])
+def test_noalloc_matches_allocating_entry_and_oracle(lib, M, N, K, fused, monkeypatch):
     import shared_memory_tiled_fp32_gb300 as tg
 
-    assert _scratch_bytes(M, N, K) <= LIMIT
+    monkeypatch.setenv("TG_FUSED_SPLIT", "1" if fused else "0")
+    need = _scratch_bytes(M, N, K, _a_in_kernel(M, K, fused))
+    if need > LIMIT:
+        pytest.skip("does not fit this form's scratch (the rejection test covers it)")
     stream = torch.cuda.current_stream()
     for call, (dist, seed) in enumerate((("uniform", 31), ("int", 32))):  # two calls in a row
         A, B = make_inputs(M, N, K, dist, seed + M)
@@ -74,10 +87,15 @@ def test_noalloc_matches_allocating_entry_and_oracle(lib, M, N, K):
             assert_close(got, ref, K, what + " vs oracle")
 
 
-def test_noalloc_rejects_oversized_products(lib):
+@pytest.mark.parametrize("fused", [True, False])
+def test_noalloc_rejects_oversized_products(lib, fused, monkeypatch):
+    monkeypatch.setenv("TG_FUSED_SPLIT", "1" if fused else "0")
     stream = torch.cuda.current_stream()
-    for M, N, K in [(512, 8192, 2048), (2048, 2049, 2048), (2048, 2048, 2049)]:
-        assert _scratch_bytes(M, N, K) > LIMIT
+    cases = [(512, 8192, 2048), (2048, 4097, 2048), (2048, 4096, 2049), (128, 4097, 2048)]
+    if not fused:
+        cases += [(2048, 2049, 2048), (2048, 2048, 2049)]
+    for M, N, K in cases:
+        assert _scratch_bytes(M, N, K, _a_in_kernel(M, K, fused)) > LIMIT, (M, N, K)
         A = torch.empty(M, K, device="cuda")
         B = torch.empty(K, N, device="cuda")
         C = torch.empty(M, N, device="cuda")
