@@ -111,15 +111,14 @@ void fill_info(const Plan& p, tg_plan_info* out) {
     out->tiles_n = p.tiles_n;
     out->units = p.units;
     out->grid = p.grid;
-    out->prepass = (tensor_path(p.path) && !p.zero_fill && p.M > 0 && p.N > 0 && !(p.raw_a && p.raw_b)) ||
-                   p.pack_a || p.pack_b;
+    out->prepass = (tensor_path(p.path) && !p.zero_fill && p.M > 0 && p.N > 0) || p.pack_a || p.pack_b;
     out->launches = p.launches;
     out->workspace_bytes = p.ws_bytes;
     out->pair = p.pair;
     out->tail_units = p.tail_units;
     out->tail_lanes = p.tail_lanes;
     out->tail_kx = p.tail_kx;
-    out->fused_split = (p.raw_a ? 1 : 0) | (p.raw_b ? 2 : 0);
+    out->fused_split = p.raw_a ? 1 : 0;
 }
 
 }  // namespace

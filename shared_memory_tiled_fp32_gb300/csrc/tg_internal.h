@@ -86,10 +86,10 @@ struct Plan {
     int tiles_m = 0, tiles_n = 0;
     int pair = 1;        // 3xTF32: CTAs per cluster on vertically adjacent tiles
     bool pair_mma = false;  // 3xTF32 pairs: one M = 256 product over both CTAs (cta_group::2)
-    // 3xTF32 with the pair MMA: an operand stored K-major (A untransposed, B
-    // transposed) with a 16-byte-aligned base and pitch is staged raw by TMA
-    // and split into hi/lo inside the GEMM kernel (no pre-pass copy of it)
-    bool raw_a = false, raw_b = false;
+    // 3xTF32 with the pair MMA: A stored M x K with a 16-byte-aligned base
+    // and pitch is staged raw by TMA and split into hi/lo inside the GEMM
+    // kernel (no pre-pass copy of it)
+    bool raw_a = false;
     long long units = 0; // work units (a unit is `pair` vertically adjacent tiles x one K slice)
     // stream-K tail: the tile units past full_units (tail_units of them) are
     // shared out over tail_lanes lanes, each running an equal share of their
@@ -122,7 +122,7 @@ struct Plan {
     // 2*k16) live outside the workspace at ext_a (ext_b), planned with external_a
     // (external_b); a_ready (b_ready) = it already holds that operand's split,
     // so the pre-pass skips it (and is not launched if both are).  An operand
-    // the kernel splits itself (raw_a, raw_b) has no split tiles.
+    // the kernel splits itself (raw_a) has no split tiles.
     float* ext_a = nullptr;
     float* ext_b = nullptr;
     bool a_ready = false;
@@ -154,8 +154,8 @@ struct HostBlocks {
 HostBlocks choose_host_blocks(int M, int N, int K, int path, int num_sms);
 
 // Fill `p` for the given call; num_sms > 0.  Assumes validate() passed.
-// allow_fuse = false keeps every operand on the pre-pass (raw_a = raw_b =
-// false), for callers that share split tiles between products.
+// allow_fuse = false keeps every operand on the pre-pass (raw_a = false), for
+// callers that share split tiles between products.
 void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void* A, int lda,
                const void* B, int ldb, float beta, const void* C, int ldc, int path, int split_k,
                int num_sms, Plan* p, bool external_b = false, bool external_a = false, bool allow_fuse = true);

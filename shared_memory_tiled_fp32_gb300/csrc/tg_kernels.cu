@@ -579,16 +579,18 @@ __device__ __forceinline__ void split_raw_tile(uint8_t* region, int t) {
 // kMixed: the operand tiles hold tf32 hi and bf16 hi / lo (the pre-pass's
 // kSplitBf16 layout) and each 16-wide K block takes two tf32 hi x hi products
 // and two bf16 cross products (hi x lo, lo x hi) instead of six tf32 ones.
-// kRawA / kRawB (pair MMA, 3xTF32): that operand is staged raw and split in
-// the kernel (see kRawTileBytes); tmA / tmB then map the caller's matrix.  A
-// split-tile operand of such a kernel comes in the pre-pass's kSplitTf32H
-// layout, so both operands are read with the 64-byte-swizzle descriptors.
-template <int kPair, bool kPairMma, bool kMixed = false, bool kRawA = false, bool kRawB = false>
+// kRawA (pair MMA, 3xTF32): A is staged raw and split in the kernel (see
+// kRawTileBytes); tmA then maps the caller's matrix, and B's split tiles come
+// in the pre-pass's kSplitTf32H layout, so both operands are read with the
+// 64-byte-swizzle descriptors.  (B is never split here: with both operands
+// raw the two split warps held the kernel at 320-325 against 374 TFLOP/s at
+// 8192^3, more than the pre-pass of B costs.)
+template <int kPair, bool kPairMma, bool kMixed = false, bool kRawA = false>
 __global__ void __launch_bounds__(kTfThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        GemmArgs args) {
     static_assert(!kPairMma || kPair == 2, "the pair MMA needs a CTA pair");
-    constexpr bool kRaw = kRawA || kRawB;
+    constexpr bool kRaw = kRawA;
     static_assert(!kRaw || (kPairMma && !kMixed), "raw operands: pair-MMA 3xTF32 form only");
     constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK;
     constexpr int ST = TfRing<kPairMma>::kStages;
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     uint64_t* tfull = empty + ST;  // [2] chunk accumulated
     uint64_t* tempty = tfull + 2;  // [2] chunk drained by the epilogue
     uint64_t* drain = tempty + 2;  // every MMA of this CTA completed
-    uint64_t* rfull = drain + 1;   // [ST] this CTA's raw operand tiles landed
+    uint64_t* rfull = drain + 1;   // [ST] this CTA's raw A tile landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + ST);
     float* out_stage = reinterpret_cast<float*>(smem + ST * kStageBytes + kTfBarBytes);  // [8 warps][32 x 32]
 
@@ -668,22 +670,17 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                     if (kPairMma) {
                         // this CTA's A tile and B half into its own ring.  Both
                         // CTAs' split-tile copies complete on the first CTA's
-                        // "full"; a raw tile completes on this CTA's "rfull",
+                        // "full"; a raw A tile completes on this CTA's "rfull",
                         // where the split warps pick it up
-                        constexpr uint32_t kPairTx = 2 * ((kRawA ? 0 : kTfAStage) + (kRawB ? 0 : kTfAStage));
-                        constexpr uint32_t kRawTx = (kRawA ? kRawTileBytes : 0) + (kRawB ? kRawTileBytes : 0);
-                        if (kRaw) mbar_arrive_expect_tx(&rfull[stage], kRawTx);
+                        constexpr uint32_t kPairTx = 2 * ((kRawA ? 0 : kTfAStage) + kTfAStage);
+                        if (kRawA) mbar_arrive_expect_tx(&rfull[stage], kRawTileBytes);
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], kPairTx);
                         const uint32_t bar0 = cluster_addr(&full[stage], 0);
                         if (kRawA)
                             tma_load_2d(st, &tmA, &rfull[stage], kb * BK, t.m0);
                         else
                             tma_load_2d_pair(st, &tmA, bar0, 0, ((t.m0 >> 7) * args.kbs + kb) * 128);
-                        if (kRawB)
-                            tma_load_2d(st + kTfAStage, &tmB, &rfull[stage], kb * BK, t.n0 + rank * BM);
-                        else
-                            tma_load_2d_pair(st + kTfAStage, &tmB, bar0, 0,
-                                             (((t.n0 >> 7) + rank) * args.kbs + kb) * 128);
+                        tma_load_2d_pair(st + kTfAStage, &tmB, bar0, 0, (((t.n0 >> 7) + rank) * args.kbs + kb) * 128);
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == ST) {
@@ -720,8 +717,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                 else
                     mbar_drain(&empty[s], (last_par >> s) & 1u, args.timeout_ns);
             }
-        } else if (kRaw && (warp == 2 || warp == 3)) {  // ------------- split of raw tiles
-            // per stage: wait for this CTA's raw tiles, write their lo halves,
+        } else if (kRaw && (warp == 2 || warp == 3)) {  // ------------- split of raw A tiles
+            // per stage: wait for this CTA's raw A tile, write its lo half,
             // publish them to the tensor core (async proxy) and arrive on the
             // first CTA's "full" barrier, where the MMA thread waits
             const int t64 = threadIdx.x - 64;
@@ -736,9 +733,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = smem + stage * kStageBytes;
-                    if (kRawA) split_raw_tile(st, t64);
-                    if (kRawB) split_raw_tile(st + kTfAStage, t64);
+                    split_raw_tile(smem + stage * kStageBytes, t64);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(cluster_addr(&full[stage], 0));
@@ -1599,9 +1594,7 @@ tg_status prepare_device_kernels() {
     } tf_kernels[] = {{tf32x3_gemm_kernel<1, false>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, false>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, true>, kTfSmemBytesPairMma},
-                      {tf32x3_gemm_kernel<2, true, false, true, false>, kTfSmemBytesPairMma},
-                      {tf32x3_gemm_kernel<2, true, false, false, true>, kTfSmemBytesPairMma},
-                      {tf32x3_gemm_kernel<2, true, false, true, true>, kTfSmemBytesPairMma},
+                      {tf32x3_gemm_kernel<2, true, false, true>, kTfSmemBytesPairMma},
                       {tf32x3_gemm_kernel<1, false, true>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, false, true>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, true, true>, kTfSmemBytesPairMma}};
@@ -1719,15 +1712,15 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     // one full wave of resident blocks keeps HBM busy without a tail
     const bool mixed = p.path == TG_PATH_TF32_BF16;
     const int mode = mixed ? kSplitBf16
-                           : (p.path == TG_PATH_TF32X3 ? ((p.raw_a || p.raw_b) ? kSplitTf32H : kSplitTf32) : kPack);
+                           : (p.path == TG_PATH_TF32X3 ? (p.raw_a ? kSplitTf32H : kSplitTf32) : kPack);
     const int prepass_grid = g_prepass_blocks_per_sm[mode] * p.num_sms;
 
     if (tensor_path(p.path)) {
         float* a_tiles = p.raw_a ? nullptr : (p.ext_a ? p.ext_a : reinterpret_cast<float*>(w + p.off_a0));
-        float* b_tiles = p.raw_b ? nullptr : (p.ext_b ? p.ext_b : reinterpret_cast<float*>(w + p.off_b0));
+        float* b_tiles = p.ext_b ? p.ext_b : reinterpret_cast<float*>(w + p.off_b0);
         // split tiles: A [a_rows/128][k16/16] from op(A); B [b_rows/128][k16/16] from op(B)^T
         // (none for an operand the kernel splits itself)
-        const bool need_a = !p.raw_a && !p.a_ready, need_b = !p.raw_b && !p.b_ready;
+        const bool need_a = !p.raw_a && !p.a_ready, need_b = !p.b_ready;
         pa.op[0] = pass(A, p.lda, p.M, p.K, p.k16, p.op_a == TG_OP_T, need_a ? a_tiles : nullptr, p.a_rows);
         pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, need_b ? b_tiles : nullptr, p.b_rows);
         if (need_a || need_b) {
@@ -1747,9 +1740,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         // the pair-MMA form reads the split tiles through 2-D tensor maps: rows
         // of 32 floats (one tile row, hi and lo), boxes of one 128-row tile
         // (the plan keeps the per-CTA form when these 32-bit row coordinates
-        // would overflow); a raw operand through a map of the caller's matrix,
-        // stored K-major: boxes of 16 K values x 128 rows, 64-byte swizzle,
-        // zeros past the edges
+        // would overflow); a raw A through a map of the caller's matrix:
+        // boxes of 16 K values x 128 rows, 64-byte swizzle, zeros past the
+        // edges
         CUtensorMap mA{}, mB{};
         const bool pair_mma = p.pair_mma;
         if (pair_mma) {
@@ -1758,19 +1751,15 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
                         : make_map(&mA, a_tiles, 32, (uint64_t)p.a_rows * ga.kbs, 128, 32, 128,
                                    CU_TENSOR_MAP_SWIZZLE_NONE);
             const bool ok_b =
-                p.raw_b ? make_map(&mB, B, p.K, p.N, 4ull * p.ldb, kTf32BK, kTf32BM, CU_TENSOR_MAP_SWIZZLE_64B)
-                        : make_map(&mB, b_tiles, 32, (uint64_t)p.b_rows * ga.kbs, 128, 32, 128,
-                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+                make_map(&mB, b_tiles, 32, (uint64_t)p.b_rows * ga.kbs, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
             if (!ok_a || !ok_b) return TG_ERR_CUDA;
         }
         int clusters = p.grid / 2;
         if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
         NvtxRange r("tg_gemm");
         void (*kern)(CUtensorMap, CUtensorMap, GemmArgs);
-        if (p.pair == 2 && pair_mma && !mixed && (p.raw_a || p.raw_b))
-            kern = p.raw_a ? (p.raw_b ? tf32x3_gemm_kernel<2, true, false, true, true>
-                                      : tf32x3_gemm_kernel<2, true, false, true, false>)
-                           : tf32x3_gemm_kernel<2, true, false, false, true>;
+        if (p.pair == 2 && pair_mma && !mixed && p.raw_a)
+            kern = tf32x3_gemm_kernel<2, true, false, true>;
         else if (p.pair == 2)
             kern = pair_mma ? (mixed ? tf32x3_gemm_kernel<2, true, true> : tf32x3_gemm_kernel<2, true>)
                             : (mixed ? tf32x3_gemm_kernel<2, false, true> : tf32x3_gemm_kernel<2, false>);

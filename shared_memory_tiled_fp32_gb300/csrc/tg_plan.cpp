@@ -52,7 +52,7 @@ long long tail_operand_bytes(const Plan& p, long long rem) {
     long long rows = 0, cols = 0;
     for (int i : rows_seen) rows += std::min<long long>((long long)p.pair * p.bm, p.M - (long long)i * p.pair * p.bm);
     for (int j : cols_seen) cols += std::min<long long>(p.bn, p.N - (long long)j * p.bn);
-    return (rows * (p.raw_a ? 4 : 8) + cols * (p.raw_b ? 4 : 8)) * p.k16;
+    return (rows * (p.raw_a ? 4 : 8) + cols * 8) * p.k16;
 }
 
 // Whether the one-launch tiled path beats the 3xTF32 path's pre-pass, GEMM
@@ -185,14 +185,13 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         const long long kbs = p->k16 / 16;
         p->pair_mma = p->pair == 2 && !(pm_env != nullptr && pm_env[0] == '0') &&
                       (long long)p->a_rows * kbs < (1ll << 31) && (long long)p->b_rows * kbs < (1ll << 31);
-        // raw operands: stored K-major (A as M x K, B as N x K), base and row
-        // pitch on 16-byte boundaries (TMA), pair-MMA 3xTF32 kernel
-        auto tma_legal = [](const void* X, int ld) {
-            return X != nullptr && reinterpret_cast<uintptr_t>(X) % 16 == 0 && ld % 4 == 0;
-        };
+        // raw A: stored M x K (K-major), base and row pitch on 16-byte
+        // boundaries (TMA), pair-MMA 3xTF32 kernel.  B always takes the
+        // pre-pass (see tg_kernels.cu: two operands split in the kernel
+        // measured slower than the pre-pass of one)
         const bool fuse = allow_fuse && p->pair_mma && p->path == TG_PATH_TF32X3 && fused_split_enabled();
-        p->raw_a = fuse && op_a == TG_OP_N && tma_legal(A, lda);
-        p->raw_b = fuse && op_b == TG_OP_T && tma_legal(B, ldb);
+        p->raw_a = fuse && op_a == TG_OP_N && A != nullptr && reinterpret_cast<uintptr_t>(A) % 16 == 0 &&
+                   lda % 4 == 0;
     }
     p->units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n * S;
     const long long cap = num_sms / p->pair;  // units in flight at once (lanes)
@@ -266,7 +265,7 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         // the split tiles of each operand not split in the kernel, unless the
         // caller provides them
         if (!external_a && !p->raw_a) p->off_a0 = take(8ull * p->a_rows * p->k16);
-        if (!external_b && !p->raw_b) p->off_b0 = take(8ull * p->b_rows * p->k16);
+        if (!external_b) p->off_b0 = take(8ull * p->b_rows * p->k16);
     } else {
         // TMA reads the operands in place when they are stored untransposed,
         // their base is 16-byte aligned and their row pitch a multiple of 16
@@ -289,7 +288,7 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->off_tail = take(4ull * slots * p->pair * p->bm * p->bn);
     }
     p->ws_bytes = off;
-    const bool prepass = (tensor_path(p->path) && !(p->raw_a && p->raw_b)) || p->pack_a || p->pack_b;
+    const bool prepass = tensor_path(p->path) || p->pack_a || p->pack_b;
     p->launches = (prepass ? 1 : 0) + 1 + (S > 1 ? 1 : 0) + (p->tail_lanes > 0 ? 1 : 0);
 }
 
