@@ -133,9 +133,9 @@ typedef struct tg_plan_info {
     int tail_kx;          /* 0: the lanes run the units' K blocks laid end to end (stream-K) or
                              equal K slices; > 0: unit q's first tail_kx K blocks run on lane q,
                              all in step, the rest of every unit over the other lanes */
-    int fused_split;      /* 3xTF32: 1 = A is staged raw from the caller's buffer and split into
-                             hi/lo inside the GEMM kernel (no pre-pass copy of A; B always takes
-                             the pre-pass); 0 = both operands are split by the pre-pass */
+    int fused_split;      /* tensor paths: 1 = A is staged raw from the caller's buffer and split
+                             inside the GEMM kernel (no pre-pass copy of A; B always takes the
+                             pre-pass); 0 = both operands are split by the pre-pass */
 } tg_plan_info;
 
 /* C = A x B with automatic path and split choice (see the file comment for

@@ -86,9 +86,9 @@ struct Plan {
     int tiles_m = 0, tiles_n = 0;
     int pair = 1;        // 3xTF32: CTAs per cluster on vertically adjacent tiles
     bool pair_mma = false;  // 3xTF32 pairs: one M = 256 product over both CTAs (cta_group::2)
-    // 3xTF32 with the pair MMA: A stored M x K with a 16-byte-aligned base
-    // and pitch is staged raw by TMA and split into hi/lo inside the GEMM
-    // kernel (no pre-pass copy of it)
+    // tensor paths with the pair MMA: A stored M x K with a 16-byte-aligned
+    // base and pitch is staged raw by TMA and split inside the GEMM kernel
+    // (no pre-pass copy of it)
     bool raw_a = false;
     long long units = 0; // work units (a unit is `pair` vertically adjacent tiles x one K slice)
     // stream-K tail: the tile units past full_units (tail_units of them) are

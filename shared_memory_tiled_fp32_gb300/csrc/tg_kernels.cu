@@ -552,6 +552,26 @@ constexpr uint32_t kSwRowGroupBytes64 = 8 * 64;            // 8 rows of the 64-b
 constexpr uint32_t kDescSwizzle64 = 4;
 static_assert(2 * kRawTileBytes == kTfAStage, "raw tile + lo fill one operand region of a stage");
 
+// x rounded to bf16 (nearest even), truncated where that would overflow.
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return __bfloat16_as_ushort((__hisinf(b) && !isinf(x)) ? __float2bfloat16_rz(x) : b);
+}
+
+__device__ __forceinline__ uint2 to_bf16x4(float a, float b, float c, float d) {
+    return make_uint2(bf16_bits(a) | (bf16_bits(b) << 16), bf16_bits(c) | (bf16_bits(d) << 16));
+}
+
+// bf16 of four values (round to nearest even; a finite value beyond the
+// largest bf16 becomes the largest, as bf16_bits does), two per instruction:
+// the low half of each word holds the earlier value.
+__device__ __forceinline__ uint2 to_bf16x4_fast(float a, float b, float c, float d) {
+    uint32_t lo, hi;
+    asm("cvt.rn.satfinite.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(d), "f"(c));
+    return make_uint2(lo, hi);
+}
+
 // lo = tf32(x - trunc_tf32(x)) of four values.
 __device__ __forceinline__ float4 split_lo4(float4 x) {
     auto lo = [](float v) {
@@ -576,9 +596,40 @@ __device__ __forceinline__ void split_raw_tile(uint8_t* region, int t) {
     }
 }
 
+// The tf32 + bf16 variant with a raw A: the split warps write bf16(hi) and
+// bf16(lo) of the raw tile (hi = x truncated to tf32, which is how the tensor
+// core reads the raw value in the hi x hi product; lo = x - hi, exact) into
+// the region's second 8 KiB: 128 rows of 64 bytes in the 64-byte swizzle,
+// 16-byte group j of row r at position j ^ ((r / 2) % 4), groups 0 / 1 holding
+// bf16(hi) of K 0-7 / 8-15 and groups 2 / 3 bf16(lo) of the same, so that one
+// K = 16 bf16 product reads hi at +0 and lo at +32 bytes of each row.  Raw
+// group i (16 bytes) holds row i / 4, K values 4c..4c+3 with c = (i % 4) ^
+// ((row / 2) % 4).
+__device__ __forceinline__ void split_raw_tile_bf16(uint8_t* region, int t) {
+    const float4* src = reinterpret_cast<const float4*>(region);
+    uint8_t* dst = region + kRawTileBytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = src[t + 64 * (4 * h + u)];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = t + 64 * (4 * h + u), r = i >> 2, key = (r >> 1) & 3, c = (i & 3) ^ key;
+            auto trunc = [](float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); };
+            const float4 hi = make_float4(trunc(v[u].x), trunc(v[u].y), trunc(v[u].z), trunc(v[u].w));
+            const int at = 64 * r + 8 * (c & 1);
+            *reinterpret_cast<uint2*>(dst + at + 16 * ((c >> 1) ^ key)) = to_bf16x4_fast(hi.x, hi.y, hi.z, hi.w);
+            *reinterpret_cast<uint2*>(dst + at + 16 * ((2 + (c >> 1)) ^ key)) =
+                to_bf16x4_fast(v[u].x - hi.x, v[u].y - hi.y, v[u].z - hi.z, v[u].w - hi.w);
+        }
+    }
+}
+
 // kMixed: the operand tiles hold tf32 hi and bf16 hi / lo (the pre-pass's
-// kSplitBf16 layout) and each 16-wide K block takes two tf32 hi x hi products
-// and two bf16 cross products (hi x lo, lo x hi) instead of six tf32 ones.
+// kSplitBf16 layout; with a raw A, the kSplitBf16H layout and the split
+// above) and each 16-wide K block takes two tf32 hi x hi products and two
+// bf16 cross products (hi x lo, lo x hi) instead of six tf32 ones.
 // kRawA (pair MMA, 3xTF32): A is staged raw and split in the kernel (see
 // kRawTileBytes); tmA then maps the caller's matrix, and B's split tiles come
 // in the pre-pass's kSplitTf32H layout, so both operands are read with the
@@ -591,7 +642,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                        GemmArgs args) {
     static_assert(!kPairMma || kPair == 2, "the pair MMA needs a CTA pair");
     constexpr bool kRaw = kRawA;
-    static_assert(!kRaw || (kPairMma && !kMixed), "raw operands: pair-MMA 3xTF32 form only");
+    static_assert(!kRaw || kPairMma, "raw A: pair-MMA form only");
     constexpr int BM = kTf32BM, BN = kTf32BN, BK = kTf32BK;
     constexpr int ST = TfRing<kPairMma>::kStages;
     constexpr uint32_t kStageBytes = TfRing<kPairMma>::kStageBytes;
@@ -733,7 +784,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         ok = false;
                         break;
                     }
-                    split_raw_tile(smem + stage * kStageBytes, t64);
+                    if (kMixed)
+                        split_raw_tile_bf16(smem + stage * kStageBytes, t64);
+                    else
+                        split_raw_tile(smem + stage * kStageBytes, t64);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(cluster_addr(&full[stage], 0));
@@ -788,7 +842,19 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         if (kMixed) {
                             // bf16 hi at +4 (K 0-15 in one 32-byte slice), bf16 lo at +6
                             const uint32_t acc = kb > c0 ? 1u : 0u;
-                            if (kPairMma) {
+                            if (kRaw) {
+                                // every operand in 64-byte-swizzle rows: tf32 hi
+                                // (the raw A) at +0 / +32 bytes per slice, the bf16
+                                // tile 8 KiB on with hi at +0 and lo at +32 bytes
+                                constexpr uint32_t kX = kRawTileBytes >> 4;
+                                const uint64_t pa = desc_a0 + (uint64_t)stage * (kStageBytes >> 4);
+                                const uint64_t pb = desc_b0 + (uint64_t)stage * (kStageBytes >> 4);
+                                mma_f16_ss_pair(d_tmem, pa + kX, pb + kX + 2, idesc_x, acc);
+                                mma_f16_ss_pair(d_tmem, pa + kX + 2, pb + kX, idesc_x, 1u);
+                                mma_tf32_ss_pair(d_tmem, pa, pb, idesc, 1u);
+                                mma_tf32_ss_pair(d_tmem, pa + 2, pb + 2, idesc, 1u);
+                                mma_commit_pair(&empty[stage], kPairMask);
+                            } else if (kPairMma) {
                                 mma_f16_ss_pair(d_tmem, da + 4, db + 6, idesc_x, acc);
                                 mma_f16_ss_pair(d_tmem, da + 6, db + 4, idesc_x, 1u);
                                 mma_tf32_ss_pair(d_tmem, da, db, idesc, 1u);
@@ -1035,14 +1101,19 @@ __device__ __forceinline__ float4 load_row4(const float* src, long long ld, int 
 // A tile in the 64-byte and a B tile in the 128-byte swizzle gave wrong
 // products in the cta_group::2 form, though not with one CTA), so a product
 // whose other operand is split in the kernel takes this layout.
-constexpr int kPack = 0, kSplitTf32 = 1, kSplitBf16 = 2, kSplitTf32H = 3;
+// kSplitBf16H: the kSplitBf16 values for a product whose A the kernel splits:
+// tf32 hi in the first 8 KiB as in kSplitTf32H, and the second 8 KiB as 128
+// rows of 64 bytes, 16-byte group j of row r at position j ^ ((r / 2) % 4),
+// groups 0 / 1 bf16(hi) of K 0-7 / 8-15, groups 2 / 3 bf16(lo) (the layout
+// the split warps write for A, see split_raw_tile_bf16).
+constexpr int kPack = 0, kSplitTf32 = 1, kSplitBf16 = 2, kSplitTf32H = 3, kSplitBf16H = 4;
 
 // Offset of destination element (r, c): hi in its swizzled tile (split
 // modes) or the plain padded row (kPack).
 template <int MODE>
 __device__ __forceinline__ long long dst_offset(int pitch, int r, int c) {
     const long long tile = ((long long)(r >> 7) * (pitch >> 4) + (c >> 4)) * 4096;
-    if (MODE == kSplitTf32H)
+    if (MODE == kSplitTf32H || MODE == kSplitBf16H)
         return tile + (r & 127) * 16 + ((((c & 15) >> 2) ^ ((r >> 1) & 3)) << 2) + (c & 3);
     if (MODE != kPack)
         return tile + (r & 127) * 32 + ((((c & 15) >> 2) ^ (r & 7)) << 2) + (c & 3);
@@ -1065,16 +1136,6 @@ __device__ __forceinline__ float split_hi(float x) {
     return (isinf(h) && !isinf(x)) ? __uint_as_float(__float_as_uint(x) & 0xffffe000u) : h;
 }
 
-// x rounded to bf16 (nearest even), truncated where that would overflow.
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(x);
-    return __bfloat16_as_ushort((__hisinf(b) && !isinf(x)) ? __float2bfloat16_rz(x) : b);
-}
-
-__device__ __forceinline__ uint2 to_bf16x4(float a, float b, float c, float d) {
-    return make_uint2(bf16_bits(a) | (bf16_bits(b) << 16), bf16_bits(c) | (bf16_bits(d) << 16));
-}
-
 // Store destination columns c..c+3 of row r (c a multiple of 4: one 16-byte
 // group) at offset o.
 template <int MODE>
@@ -1088,6 +1149,14 @@ __device__ __forceinline__ void store_split4(float* d0, long long o, float4 x) {
     if (MODE == kSplitTf32H) {
         *reinterpret_cast<float4*>(d0 + o + 2048) =
             make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
+    } else if (MODE == kSplitBf16H) {
+        // o = tile + 16 row + 4 (c ^ key) with key = (row / 2) % 4, c = (K % 16) / 4
+        const long long tile = o & ~4095ll;
+        const int row = (int)(o >> 4) & 127, key = (row >> 1) & 3, c = ((int)(o >> 2) & 3) ^ key;
+        float* b = d0 + tile + 2048 + 16 * row + 2 * (c & 1);
+        *reinterpret_cast<uint2*>(b + 4 * ((c >> 1) ^ key)) = to_bf16x4(hi.x, hi.y, hi.z, hi.w);
+        *reinterpret_cast<uint2*>(b + 4 * ((2 + (c >> 1)) ^ key)) =
+            to_bf16x4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
     } else if (MODE == kSplitTf32) {
         *reinterpret_cast<float4*>(d0 + (o ^ 16)) =
             make_float4(to_tf32(x.x - hi.x), to_tf32(x.y - hi.y), to_tf32(x.z - hi.z), to_tf32(x.w - hi.w));
@@ -1562,7 +1631,7 @@ tg_status launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 
 // Resident 256-thread blocks per SM of the two pre-pass kernels (the grid is
 // sized to exactly fill the GPU once).
-int g_prepass_blocks_per_sm[4] = {4, 4, 4, 4};
+int g_prepass_blocks_per_sm[5] = {4, 4, 4, 4, 4};
 // CTA pairs of the 3xTF32 kernel resident at once (0 = unknown).
 int g_tf32_pair_clusters = 0;
 
@@ -1579,6 +1648,9 @@ tg_status prepare_device_kernels() {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<kSplitTf32H>, 256, 0) == cudaSuccess &&
         nb > 0)
         g_prepass_blocks_per_sm[kSplitTf32H] = nb;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prepass_kernel<kSplitBf16H>, 256, 0) == cudaSuccess &&
+        nb > 0)
+        g_prepass_blocks_per_sm[kSplitBf16H] = nb;
     // The warpgroup register splits of both GEMM kernels only balance when the
     // kernels are launched with exactly the register counts they were designed
     // for; refuse to run a build that differs.
@@ -1595,6 +1667,7 @@ tg_status prepare_device_kernels() {
                       {tf32x3_gemm_kernel<2, false>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, true>, kTfSmemBytesPairMma},
                       {tf32x3_gemm_kernel<2, true, false, true>, kTfSmemBytesPairMma},
+                      {tf32x3_gemm_kernel<2, true, true, true>, kTfSmemBytesPairMma},
                       {tf32x3_gemm_kernel<1, false, true>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, false, true>, kTfSmemBytes},
                       {tf32x3_gemm_kernel<2, true, true>, kTfSmemBytesPairMma}};
@@ -1711,7 +1784,7 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
     PrepassArgs pa{};
     // one full wave of resident blocks keeps HBM busy without a tail
     const bool mixed = p.path == TG_PATH_TF32_BF16;
-    const int mode = mixed ? kSplitBf16
+    const int mode = mixed ? (p.raw_a ? kSplitBf16H : kSplitBf16)
                            : (p.path == TG_PATH_TF32X3 ? (p.raw_a ? kSplitTf32H : kSplitTf32) : kPack);
     const int prepass_grid = g_prepass_blocks_per_sm[mode] * p.num_sms;
 
@@ -1725,7 +1798,9 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         pa.op[1] = pass(B, p.ldb, p.N, p.K, p.k16, p.op_b == TG_OP_N, need_b ? b_tiles : nullptr, p.b_rows);
         if (need_a || need_b) {
             NvtxRange r("tg_prepass");
-            if (mixed)
+            if (mode == kSplitBf16H)
+                prepass_kernel<kSplitBf16H><<<prepass_grid, 256, 0, stream>>>(pa);
+            else if (mixed)
                 prepass_kernel<kSplitBf16><<<prepass_grid, 256, 0, stream>>>(pa);
             else if (mode == kSplitTf32H)
                 prepass_kernel<kSplitTf32H><<<prepass_grid, 256, 0, stream>>>(pa);
@@ -1758,8 +1833,8 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         if (g_tf32_pair_clusters > 0 && clusters > g_tf32_pair_clusters) clusters = g_tf32_pair_clusters;
         NvtxRange r("tg_gemm");
         void (*kern)(CUtensorMap, CUtensorMap, GemmArgs);
-        if (p.pair == 2 && pair_mma && !mixed && p.raw_a)
-            kern = tf32x3_gemm_kernel<2, true, false, true>;
+        if (p.pair == 2 && pair_mma && p.raw_a)
+            kern = mixed ? tf32x3_gemm_kernel<2, true, true, true> : tf32x3_gemm_kernel<2, true, false, true>;
         else if (p.pair == 2)
             kern = pair_mma ? (mixed ? tf32x3_gemm_kernel<2, true, true> : tf32x3_gemm_kernel<2, true>)
                             : (mixed ? tf32x3_gemm_kernel<2, false, true> : tf32x3_gemm_kernel<2, false>);

@@ -186,10 +186,11 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->pair_mma = p->pair == 2 && !(pm_env != nullptr && pm_env[0] == '0') &&
                       (long long)p->a_rows * kbs < (1ll << 31) && (long long)p->b_rows * kbs < (1ll << 31);
         // raw A: stored M x K (K-major), base and row pitch on 16-byte
-        // boundaries (TMA), pair-MMA 3xTF32 kernel.  B always takes the
-        // pre-pass (see tg_kernels.cu: two operands split in the kernel
-        // measured slower than the pre-pass of one)
-        const bool fuse = allow_fuse && p->pair_mma && p->path == TG_PATH_TF32X3 && fused_split_enabled();
+        // boundaries (TMA), pair-MMA tensor kernel (3xTF32 or the tf32 +
+        // bf16 variant).  B always takes the pre-pass (see tg_kernels.cu:
+        // two operands split in the kernel measured slower than the
+        // pre-pass of one)
+        const bool fuse = allow_fuse && p->pair_mma && fused_split_enabled();
         p->raw_a = fuse && op_a == TG_OP_N && A != nullptr && reinterpret_cast<uintptr_t>(A) % 16 == 0 &&
                    lda % 4 == 0;
     }
@@ -295,8 +296,9 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
 // Modelled duration (seconds) of one planned product: its rounds of work
 // units over the lanes (whole rounds, plus the tail's share of a unit per
 // lane), each unit taking its tile's flops at the path's per-lane rate, plus
-// a fixed 25 us per product (pipeline fill and drain, reduce, launch gaps;
-// measured on GB300 for products of one to a few rounds).
+// a fixed 45 us per product (pipeline fill and drain, reduce, launch gaps
+// and the host's own issue of the product's copies and launches; fitted on
+// GB300 to 40 measured 8192^3 host-buffer layouts, RMS error 0.06 ms).
 double product_seconds(const Plan& p, double rate) {
     if (p.M == 0 || p.N == 0 || p.K == 0) return 5e-6;
     const long long lanes = std::max(1, p.grid / p.pair);
@@ -306,7 +308,7 @@ double product_seconds(const Plan& p, double rate) {
     else
         rounds = (double)cdiv(p.units, lanes);
     const double unit_flops = 2.0 * p.pair * p.bm * p.bn * ((double)p.K / p.split);
-    return rounds * unit_flops / (rate / std::max(1, p.num_sms / p.pair)) + 25e-6;
+    return rounds * unit_flops / (rate / std::max(1, p.num_sms / p.pair)) + 45e-6;
 }
 
 // Host-buffer pipeline model: a small event simulation of one call.  Copies
@@ -318,8 +320,9 @@ double product_seconds(const Plan& p, double rate) {
 // in).  Rates measured on GB300 over NVLink-C2C with pinned host memory:
 // 205 GB/s in alone, 190 GB/s out alone, about 170 GB/s each way while both
 // directions are busy, plus ~40 us per copy out; the split pre-pass about
-// 5.7 TB/s; a full round of work units 375 (3xTF32) or 62 (FFMA) useful
-// TFLOP/s.  Fitted to the measured 8192^3 layouts within ~2 %.
+// 5.7 TB/s; a full round of work units 385 (3xTF32, A split in the kernel)
+// or 62 (FFMA) useful TFLOP/s.  Fitted to the measured 8192^3 layouts
+// within ~2 %.
 namespace {
 
 struct HostCopy {
@@ -416,7 +419,7 @@ class HostModel {
         auto it = product_s_.find({rows, cols});
         if (it != product_s_.end()) return it->second;
         const Plan pl = plan(rows, cols);
-        const double t = product_seconds(pl, path_ == TG_PATH_TF32_BF16 ? 525e12 : (tf32_ ? 375e12 : 62e12));
+        const double t = product_seconds(pl, path_ == TG_PATH_TF32_BF16 ? 525e12 : (tf32_ ? 385e12 : 62e12));
         return product_s_[{rows, cols}] = {t, pl.raw_a};
     }
     double product(int rows, int cols) { return product_info(rows, cols).first; }

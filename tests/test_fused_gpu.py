@@ -35,20 +35,20 @@ def stored(X, trans):
     return np.ascontiguousarray(X.T) if trans else np.ascontiguousarray(X)
 
 
-def general(tg, As, Bs, trans_a, trans_b, M, N, alpha=1.0, beta=0.0, C0=None, **kw):
+def general(tg, As, Bs, trans_a, trans_b, M, N, alpha=1.0, beta=0.0, C0=None, path="tf32x3", **kw):
     C = torch.zeros(M, N, device="cuda") if C0 is None else torch.from_numpy(C0.copy()).cuda()
     tg.matmul_general(torch.from_numpy(As).cuda(), torch.from_numpy(Bs).cuda(), C, trans_a=trans_a,
-                      trans_b=trans_b, alpha=alpha, beta=beta, path="tf32x3", **kw)
+                      trans_b=trans_b, alpha=alpha, beta=beta, path=path, **kw)
     torch.cuda.synchronize()
     assert tg.sync_status() == 0
     return C.cpu().numpy()
 
 
-def plan_flags(tg, As, Bs, trans_a, trans_b, M, N, K):
+def plan_flags(tg, As, Bs, trans_a, trans_b, M, N, K, path="tf32x3"):
     Ad, Bd = torch.from_numpy(As).cuda(), torch.from_numpy(Bs).cuda()
     C = torch.empty(M, N, device="cuda")
     p = tg.plan_general(trans_a, trans_b, M, N, K, Ad.stride(0), Bd.stride(0), C.stride(0), A=Ad.data_ptr(),
-                        B=Bd.data_ptr(), C=C.data_ptr(), path="tf32x3")
+                        B=Bd.data_ptr(), C=C.data_ptr(), path=path)
     return p["fused_split"]
 
 
@@ -56,9 +56,10 @@ SHAPES = [(129, 300, 700), (256, 256, 16), (300, 513, 17), (383, 257, 4097), (10
           (640, 256, 2048), (2048, 2048, 4096)]
 
 
+@pytest.mark.parametrize("path", ["tf32x3", "tf32bf16"])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("trans_a,trans_b", [(False, False), (False, True), (True, True)])
-def test_fused_split_matches_oracle(tg, M, N, K, trans_a, trans_b, monkeypatch):
+def test_fused_split_matches_oracle(tg, M, N, K, trans_a, trans_b, path, monkeypatch):
     A, B = (x.numpy() for x in make_inputs(M, N, K, "uniform", 1300 + M + K))
     As, Bs = stored(A, trans_a), stored(B, trans_b)
     ref = oracle.sgemm(A, B)
@@ -66,22 +67,23 @@ def test_fused_split_matches_oracle(tg, M, N, K, trans_a, trans_b, monkeypatch):
     want = 1 if K % 4 == 0 and not trans_a else 0
     for fused in ("1", "0"):
         monkeypatch.setenv("TG_FUSED_SPLIT", fused)
-        assert plan_flags(tg, As, Bs, trans_a, trans_b, M, N, K) == (want if fused == "1" else 0)
+        assert plan_flags(tg, As, Bs, trans_a, trans_b, M, N, K, path) == (want if fused == "1" else 0)
         for split in (0, 1, 3):
-            got = general(tg, As, Bs, trans_a, trans_b, M, N, split_k=split)
-            assert_close(got, ref, K, f"fused={fused} op=({trans_a},{trans_b}) {M}x{N}x{K} s{split}")
+            got = general(tg, As, Bs, trans_a, trans_b, M, N, split_k=split, path=path)
+            assert_close(got, ref, K, f"{path} fused={fused} op=({trans_a},{trans_b}) {M}x{N}x{K} s{split}")
 
 
+@pytest.mark.parametrize("path", ["tf32x3", "tf32bf16"])
 @pytest.mark.parametrize("trans_b", [False, True])
-def test_fused_split_integers_bitexact(tg, trans_b):
+def test_fused_split_integers_bitexact(tg, trans_b, path):
     """Integer data: the raw value is its own hi (lo = 0), so the products are
     exact, on every split and tail form."""
     for i, (M, N, K) in enumerate([(129, 300, 700), (1000, 3000, 1100), (2048, 2048, 2049), (300, 513, 17)]):
         A, B = (x.numpy() for x in make_inputs(M, N, K, "int", 1400 + i))
         ref = oracle.sgemm(A, B)
         for split in (0, 2):
-            got = general(tg, A, stored(B, trans_b), False, trans_b, M, N, split_k=split)
-            assert_bitexact(got, ref, f"integers trans_b={trans_b} {M}x{N}x{K} s{split}")
+            got = general(tg, A, stored(B, trans_b), False, trans_b, M, N, split_k=split, path=path)
+            assert_bitexact(got, ref, f"{path} integers trans_b={trans_b} {M}x{N}x{K} s{split}")
 
 
 def test_fused_split_strided_and_scaled(tg):

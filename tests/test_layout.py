@@ -212,6 +212,54 @@ def test_split_tile_h_matches_raw_tma_layout(rows, pitch):
     assert all(v == 1 for v in seen)
 
 
+def bf16h_prepass_offset(pitch, r, c, part):
+    """Where the kSplitBf16H pre-pass mode puts the bf16 value of (r, c)
+    (part 0: bf16(hi), 1: bf16(lo)), in bytes: from the hi group's float
+    offset o it recovers the row and the group, then writes 8-byte runs into
+    the tile's second 8 KiB."""
+    o = split_tile_h_offset(pitch, r, c & ~3)
+    tile = o & ~4095
+    row = (o >> 4) & 127
+    key = (row >> 1) & 3
+    g = ((o >> 2) & 3) ^ key
+    base = tile + 2048 + 16 * row + 2 * (g & 1)        # floats
+    run = base + 4 * (((2 * part) + (g >> 1)) ^ key)   # floats
+    return 4 * run + 2 * (c & 3)
+
+
+def bf16h_split_warp_offset(r, c, part):
+    """Where the fused kernel's split warps put bf16 value (r, c) of a raw A
+    tile (r < 128, c < 16), in bytes from the tile's second 8 KiB, starting
+    from the raw 16-byte group that holds it (the 64-byte-swizzled TMA box)."""
+    raw_byte = tma_swizzle_64(64 * r + 4 * (c & ~3))
+    i = raw_byte // 16                  # the raw group's index, as the warps see it
+    rr, key = i >> 2, ((i >> 2) >> 1) & 3
+    g = (i & 3) ^ key
+    assert rr == r and g == c // 4
+    at = 64 * rr + 8 * (g & 1)
+    return at + 16 * (((2 * part) + (g >> 1)) ^ key) + 2 * (c & 3)
+
+
+def test_bf16h_layouts_agree_and_cover():
+    """The tf32 + bf16 variant with a raw A reads A's bf16 tile (written by the
+    split warps) and B's (written by the pre-pass) with one descriptor form,
+    so both must put bf16 value (r, c) at the same place: K 0-7 / 8-15 of
+    bf16(hi) in logical 16-byte groups 0 / 1 and bf16(lo) in 2 / 3, group j
+    of row r at position j ^ ((r / 2) % 4), and every byte written once."""
+    seen = [0] * 8192
+    for r in range(128):
+        for c in range(16):
+            for part in (0, 1):
+                pre = bf16h_prepass_offset(16, r, c, part) - 4 * 2048
+                warp = bf16h_split_warp_offset(r, c, part)
+                assert pre == warp, (r, c, part)
+                logical = ((warp - 64 * r) // 16) ^ ((r >> 1) & 3)
+                assert logical == 2 * part + (c >> 3) and (warp % 16) // 2 == c % 8
+                seen[warp] += 1
+                seen[warp + 1] += 1
+    assert all(v == 1 for v in seen)
+
+
 def test_fused_split_warps_access_conflict_free():
     """The split warps of the fused kernel move a raw 8 KiB tile to its lo
     half as 512 16-byte groups, thread t (0..63) taking t + 64u: each warp
