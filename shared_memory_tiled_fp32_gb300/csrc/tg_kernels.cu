@@ -605,18 +605,34 @@ __device__ __forceinline__ void split_raw_tile(uint8_t* region, int t) {
 // K = 16 bf16 product reads hi at +0 and lo at +32 bytes of each row.  Raw
 // group i (16 bytes) holds row i / 4, K values 4c..4c+3 with c = (i % 4) ^
 // ((row / 2) % 4).
+//
+// Thread t (warp w = t / 32, lane l) takes, in each of its 8 rounds u, the
+// 8-row group g = w + 2u: lanes 0-15 rows {0, 1, 4, 5} of the group, lanes
+// 16-31 rows {2, 3, 6, 7}, four lanes per row (16-byte position l % 4).  The
+// 8-byte stores are served per half-warp; with four consecutive rows in a
+// half-warp, rows r and r + 2 (same row parity, swizzle keys 2k and 2k + 1)
+// hit the same banks, while rows {0, 1, 4, 5} and {2, 3, 6, 7} fill all 16
+// eight-byte slots of a 128-byte bank row (measured: 13.7 M store bank
+// conflicts per 4096^3 launch with four consecutive rows per half-warp).
+// Every quarter-warp's 16-byte loads still cover 8 different bank groups.
 __device__ __forceinline__ void split_raw_tile_bf16(uint8_t* region, int t) {
     const float4* src = reinterpret_cast<const float4*>(region);
     uint8_t* dst = region + kRawTileBytes;
+    const int lane = t & 31, w = t >> 5, q = lane & 15;
+    const int rig = ((lane >> 4) << 1) + ((q >> 3) << 2) + ((q >> 2) & 1);  // {0,1,4,5} / {2,3,6,7}
+    auto trunc = [](float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); };
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         float4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = src[t + 64 * (4 * h + u)];
+        int rr[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int i = t + 64 * (4 * h + u), r = i >> 2, key = (r >> 1) & 3, c = (i & 3) ^ key;
-            auto trunc = [](float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); };
+            rr[u] = 8 * (w + 2 * (4 * h + u)) + rig;
+            v[u] = src[4 * rr[u] + (q & 3)];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = rr[u], key = (r >> 1) & 3, c = (q & 3) ^ key;
             const float4 hi = make_float4(trunc(v[u].x), trunc(v[u].y), trunc(v[u].z), trunc(v[u].w));
             const int at = 64 * r + 8 * (c & 1);
             *reinterpret_cast<uint2*>(dst + at + 16 * ((c >> 1) ^ key)) = to_bf16x4_fast(hi.x, hi.y, hi.z, hi.w);

@@ -260,6 +260,41 @@ def test_bf16h_layouts_agree_and_cover():
     assert all(v == 1 for v in seen)
 
 
+def test_bf16_split_warps_conflict_free():
+    """The tf32 + bf16 split warps (split_raw_tile_bf16): thread t = 32w + l
+    takes, in round u, row 8(w + 2u) + rig of its 8-row group, rig = {0, 1,
+    4, 5} for lanes 0-15 and {2, 3, 6, 7} for lanes 16-31, four lanes per row
+    at 16-byte position l % 4.  Every raw group is read once per stage; each
+    quarter-warp's 16-byte loads hit 8 different bank groups and each
+    half-warp's 8-byte stores (bf16 hi and bf16 lo) fill all 16 eight-byte
+    slots of a bank row.  Four consecutive rows per half-warp would not."""
+    def rig(lane):
+        q = lane & 15
+        return ((lane >> 4) << 1) + ((q >> 3) << 2) + ((q >> 2) & 1)
+
+    def slots(rows_pos, part):
+        out = []
+        for r, p in rows_pos:
+            key = (r >> 1) & 3
+            c = p ^ key
+            out.append(((64 * r + 16 * ((2 * part + (c >> 1)) ^ key) + 8 * (c & 1)) // 8) % 16)
+        return out
+
+    seen = set()
+    for w in (0, 1):
+        for u in range(8):
+            lanes = [(8 * (w + 2 * u) + rig(l), l & 3) for l in range(32)]
+            seen.update(lanes)
+            for qw in range(4):
+                assert len({(4 * r + p) % 8 for r, p in lanes[8 * qw:8 * qw + 8]}) == 8
+            for hw in range(2):
+                for part in (0, 1):
+                    assert len(set(slots(lanes[16 * hw:16 * hw + 16], part))) == 16
+    assert len(seen) == 512
+    consecutive = [(r, p) for r in range(4) for p in range(4)]
+    assert len(set(slots(consecutive, 0))) < 16
+
+
 def test_fused_split_warps_access_conflict_free():
     """The split warps of the fused kernel move a raw 8 KiB tile to its lo
     half as 512 16-byte groups, thread t (0..63) taking t + 64u: each warp
