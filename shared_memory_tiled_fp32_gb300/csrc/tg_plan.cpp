@@ -156,16 +156,6 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         return;
     }
 
-    // Split K when the tiles alone would leave most SMs idle.  Every slice
-    // keeps at least 4 K blocks, and there are at most 16 slices.
-    int S = 1;
-    if (split_k > 0) {
-        S = std::min(split_k, p->nkb);
-    } else if (tiles < num_sms / 2 && p->nkb >= 8) {
-        long long s = std::min<long long>({(long long)num_sms / tiles, (long long)p->nkb / 4, 16});
-        S = (int)std::max<long long>(1, s);
-    }
-    p->split = S;
     // 3xTF32: two CTAs of a cluster take vertically adjacent tiles; the
     // pair's first CTA issues one M = 256 product over both (cta_group::2),
     // each CTA holding its A tile and half of the shared B tile, which halves
@@ -194,7 +184,23 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
         p->raw_a = fuse && op_a == TG_OP_N && A != nullptr && reinterpret_cast<uintptr_t>(A) % 16 == 0 &&
                    lda % 4 == 0;
     }
-    p->units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n * S;
+    // Split K when the tile units alone would leave most lanes (CTAs, or CTA
+    // pairs) idle, into as many slices as keep every unit in one round of
+    // the lanes: each slice keeps at least 4 K blocks, at most 16 slices.
+    // (Counting 128 x 256 tiles against all SMs instead planned 777 x 1029 x
+    // 513 as 20 pair units x 4 slices = 80 units on 76 pairs: a second round
+    // for 4 units.)
+    const long long tile_units = cdiv(p->tiles_m, p->pair) * (long long)p->tiles_n;
+    const long long lanes = num_sms / p->pair;
+    int S = 1;
+    if (split_k > 0) {
+        S = std::min(split_k, p->nkb);
+    } else if (tile_units < lanes / 2 && p->nkb >= 8) {
+        long long s = std::min<long long>({lanes / tile_units, (long long)p->nkb / 4, 16});
+        S = (int)std::max<long long>(1, s);
+    }
+    p->split = S;
+    p->units = tile_units * S;
     const long long cap = num_sms / p->pair;  // units in flight at once (lanes)
     p->grid = p->pair * (int)std::min<long long>(p->units, cap);
     p->full_units = p->units;

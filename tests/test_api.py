@@ -99,11 +99,18 @@ def test_plan_tiles_split_and_workspace():
     assert tg.plan(128 * 2 * 70, 256, 4096, num_sms=sms)["tail_units"] == 0
     # a short K gives too little work per lane to share out
     assert tg.plan(4096, 4096, 128, num_sms=sms)["tail_units"] == 0
-    # ragged: ceil(777/128) x ceil(1029/256) tiles, split to fill the SMs
+    # ragged: ceil(777/128) x ceil(1029/256) tiles = 4 pair rows x 5 columns,
+    # K split to fill one round of the 76 pairs without a second: 3 slices
     p = tg.plan(777, 1029, 513, num_sms=sms)
     assert (p["tiles_m"], p["tiles_n"]) == (7, 5)
-    assert p["split_k"] == 4 and p["pair"] == 2 and p["units"] == 4 * 5 * 4 and p["launches"] == 3
-    assert p["grid"] == 2 * min(p["units"], sms // 2)
+    assert p["split_k"] == 3 and p["pair"] == 2 and p["units"] == 4 * 5 * 3 and p["launches"] == 3
+    assert p["units"] <= sms // 2 and p["grid"] == 2 * p["units"]
+    # every automatic K split keeps its units within one round of the lanes
+    for (M, N, K) in [(777, 1029, 513), (300, 300, 3000), (1024, 1024, 8192), (1500, 600, 2000), (129, 4000, 900)]:
+        for path in ("tf32x3", "ffma"):
+            q = tg.plan(M, N, K, num_sms=sms, path=path)
+            if q["split_k"] > 1:
+                assert q["units"] <= sms // q["pair"], (M, N, K, path, q)
     # one tile row cannot be paired; FFMA never pairs
     assert tg.plan(100, 4096, 4096, num_sms=sms)["pair"] == 1
     assert tg.plan(4096, 4096, 4096, num_sms=sms, path="ffma")["pair"] == 1
