@@ -128,7 +128,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -180,10 +180,12 @@ class ClockSampler:
 
 
 def kernel_source_fingerprint() -> str:
-    """sha256 (first 16 hex digits) of tg_kernels.cu without its comments and
-    blank lines: the counters in a profile summary stay valid while the code
-    they were taken on is unchanged."""
-    src = open(os.path.join(ROOT, "shared_memory_tiled_fp32_gb300", "csrc", "tg_kernels.cu")).read()
+    """sha256 (first 16 hex digits) of the kernels' source (tg_kernels.cu and
+    the headers it compiles with: tg_internal.h, tg_ptx.cuh) without
+    comments and blank lines: the counters in a profile summary stay valid
+    while the code they were taken on is unchanged."""
+    csrc = os.path.join(ROOT, "shared_memory_tiled_fp32_gb300", "csrc")
+    src = "".join(open(os.path.join(csrc, f)).read() for f in ("tg_kernels.cu", "tg_internal.h", "tg_ptx.cuh"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines()]
     code = "\n".join(ln for ln in lines if ln.strip())
