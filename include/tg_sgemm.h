@@ -64,14 +64,20 @@ typedef enum tg_op { TG_OP_N = 0, TG_OP_T = 1 } tg_op;
  *  - TG_PATH_TF32X3: tensor cores (tcgen05.mma kind::tf32, accumulator in
  *    tensor memory), fed through an mbarrier pipeline by a producer warp.
  *    Each float is split into hi = tf32(x) and lo = tf32(x - hi); the product
- *    is lo*hi + hi*lo + hi*hi.  A pre-pass writes hi/lo tiles of A and of B
- *    transposed.
+ *    is lo*hi + hi*lo + hi*hi.  A pre-pass writes hi/lo tiles of B
+ *    transposed; A stored untransposed with a 16-byte-aligned base and row
+ *    pitch is read in place and split inside the GEMM kernel (hi = x
+ *    truncated to tf32, as the tensor core reads it), else the pre-pass
+ *    writes A's tiles too (tg_plan_info.fused_split).
  *  - TG_PATH_FFMA: register-blocked fused multiply-add on the CUDA cores, fp32
  *    throughout, TMA-fed through the same kind of pipeline.
  *  - TG_PATH_TILED: the shared-memory tiled kernel for small products: one
- *    launch (no pre-pass, no split), 64 x 64 tiles, fp32 fused multiply-adds;
- *    operands read in place with any alignment.  A block of 256 threads
- *    handles one tile, so large products run it far below the other paths.
+ *    launch, no pre-pass and no workspace, 64 x 64 tiles, fp32 fused
+ *    multiply-adds; operands read in place with any alignment.  A block of
+ *    256 threads handles one tile (with few tiles, a cluster of up to 8
+ *    blocks handles one tile over slices of K and adds the slices in shared
+ *    memory, in a fixed order), so large products run it far below the other
+ *    paths.
  *  - TG_PATH_TF32_BF16: the TG_PATH_TF32X3 kernels and split (hi = tf32(x),
  *    lo = x - hi), with the two cross products taken in bf16: the product is
  *    hi*hi (kind::tf32) + bf16(hi)*bf16(lo) + bf16(lo)*bf16(hi) (kind::f16,

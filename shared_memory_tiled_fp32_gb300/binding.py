@@ -233,10 +233,21 @@ def matmul(A, B, out=None, *, path="auto", split_k=0, workspace=None, main_begin
     if out.dtype != torch.float32 or not out.is_cuda or tuple(out.shape) != (M, N):
         raise ValueError("out must be an (M, N) float32 CUDA tensor")
     lda, ldb, ldc = _rowmajor_ld(A, "A"), _rowmajor_ld(B, "B"), _rowmajor_ld(out, "out")
-    o = make_opts(path, split_k, workspace, main_begin, main_end)
-    with torch.cuda.device(A.device):
-        st = lib().tg_sgemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
-                               _stream_handle(stream), ctypes.byref(o))
+    # default options go as NULL (the library's defaults); the call is made on
+    # A's device, switching to it only when it is not already current (the
+    # switch costs more host time than the rest of this function)
+    default = (path == "auto" and not split_k and workspace is None and main_begin is None
+               and main_end is None)
+    opts = None if default else ctypes.byref(make_opts(path, split_k, workspace, main_begin, main_end))
+    dev = A.device.index
+    L = _lib if _lib is not None else lib()
+    if dev == torch.cuda.current_device():
+        handle = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        st = L.tg_sgemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, handle, opts)
+    else:
+        with torch.cuda.device(dev):
+            handle = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+            st = L.tg_sgemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, handle, opts)
     _check(st, "tg_sgemm_ex")
     return out
 

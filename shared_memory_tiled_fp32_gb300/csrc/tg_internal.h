@@ -25,8 +25,9 @@ constexpr int kTf32BM = 128, kTf32BN = 256, kTf32BK = 16, kTf32Stages = 4;
 // register block, K staged 32 floats at a time, 4 stages of 48 KiB.
 constexpr int kFfmaBM = 128, kFfmaBN = 256, kFfmaBK = 32, kFfmaStages = 4;
 
-// Tiled path (small products): 64 x 64 tiles, K staged 16 at a time.
-constexpr int kTiledBM = 64, kTiledBN = 64, kTiledBK = 16;
+// Tiled path (small products): 64 x 64 tiles, K staged 16 at a time; K
+// split over at most 8 blocks per tile (one cluster, the portable size).
+constexpr int kTiledBM = 64, kTiledBN = 64, kTiledBK = 16, kTiledMaxSplit = 8;
 // The automatic path takes the tiled kernel up to 2^26 multiply-adds with K
 // at most 512 (one block per tile: its time grows with K, and past that size
 // the 3xTF32 path's three launches cost less than the tiled path's math;

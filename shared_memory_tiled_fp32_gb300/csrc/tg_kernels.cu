@@ -1367,16 +1367,21 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------ tiled path
 //
-// Small products, where launch count and latency dominate: one launch, no
-// pre-pass, no split.  The shared-memory tiling of the pages ("Shared
-// Memory와 Tiling"; PMPP ch. 5 notes §5.4-§5.5) with register blocking: a
-// 64 x 64 output tile per 256-thread block, K staged 16 at a time in shared
-// memory (A transposed to [k][row], B as [k][col]), each thread accumulating
-// a 4 x 4 block in fp32 with fused multiply-adds, the next K stage loaded
-// into registers while the current one is used (double buffer).
-// Out-of-range elements load as zeros (ghost elements) and the store is
-// guarded.  Either operand may be stored transposed; alpha and beta are
-// applied at the store.  (A 4-stage cp.async version of the same tile was
+// Small products, where launch count and latency dominate: no pre-pass.  The
+// shared-memory tiling of the pages ("Shared Memory와 Tiling"; PMPP ch. 5
+// notes §5.4-§5.5) with register blocking: a 64 x 64 output tile per
+// 256-thread block, K staged 16 at a time in shared memory (A transposed to
+// [k][row], B as [k][col]), each thread accumulating a 4 x 4 block in fp32
+// with fused multiply-adds, the next K stage loaded into registers while the
+// current one is used (double buffer).  Out-of-range elements load as zeros
+// (ghost elements) and the store is guarded.  Either operand may be stored
+// transposed; alpha and beta are applied at the store.  With few tiles K is
+// split over a cluster of S blocks per tile (S <= 8): block rank s runs K
+// slice s (zeros past the slice's end) and leaves its partial tile in its
+// shared memory; after a cluster barrier each block adds its share of the
+// tile's 16-byte groups over all S partials, read from the other blocks'
+// shared memory, in slice order 0, 1, ... (deterministic), and stores them.
+// One launch, no workspace.  (A 4-stage cp.async version of the tile was
 // measured slower on small products: 18.2 vs 15.9 us at 256^3.)
 constexpr int kTiledThreads = 256;  // tile shape kTiledBM x kTiledBN, K stage kTiledBK (tg_internal.h)
 constexpr int kTiledPitch = kTiledBM + 4;  // [k][row] rows padded: 16-byte aligned, 2-way store conflicts at most
@@ -1390,13 +1395,15 @@ struct TiledArgs {
     int op_a, op_b;
     float alpha, beta;
     int scaled, vec_c;
+    int split, nkb;  // K slices (blocks of a cluster per tile); K blocks of kTiledBK
 };
 
 // This thread's 4 values of the A stage at K offset k0: op N: 4 consecutive k
 // of row r (r = tid / 4, k = 4 * (tid % 4)); op T (stored K x M): row
 // r = tid % 64 at k = 4 * (tid / 64) + q, consecutive threads reading
 // consecutive rows.
-__device__ __forceinline__ void tiled_load_a(const TiledArgs& a, int row0, int k0, float (&v)[4], int& r, int& k) {
+__device__ __forceinline__ void tiled_load_a(const TiledArgs& a, int row0, int k0, int kend, float (&v)[4], int& r,
+                                             int& k) {
     const int tid = threadIdx.x;
     if (a.op_a == TG_OP_N) {
         r = tid >> 2;
@@ -1409,7 +1416,7 @@ __device__ __forceinline__ void tiled_load_a(const TiledArgs& a, int row0, int k
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int gk = k0 + k + q;
-        const bool in = gi < a.M && gk < a.K;
+        const bool in = gi < a.M && gk < kend;
         v[q] = in ? (a.op_a == TG_OP_N ? a.A[(long long)gi * a.lda + gk] : a.A[(long long)gk * a.lda + gi]) : 0.0f;
     }
 }
@@ -1417,7 +1424,8 @@ __device__ __forceinline__ void tiled_load_a(const TiledArgs& a, int row0, int k
 // This thread's 4 values of the B stage: op N: 4 consecutive columns of row
 // k (k = tid / 16, c = 4 * (tid % 16)); op T (stored N x K): column
 // c = tid / 4, 4 consecutive k from 4 * (tid % 4).
-__device__ __forceinline__ void tiled_load_b(const TiledArgs& a, int col0, int k0, float (&v)[4], int& c, int& k) {
+__device__ __forceinline__ void tiled_load_b(const TiledArgs& a, int col0, int k0, int kend, float (&v)[4], int& c,
+                                             int& k) {
     const int tid = threadIdx.x;
     if (a.op_b == TG_OP_N) {
         k = tid >> 4;
@@ -1430,7 +1438,7 @@ __device__ __forceinline__ void tiled_load_b(const TiledArgs& a, int col0, int k
     for (int q = 0; q < 4; ++q) {
         const int gk = k0 + k + (a.op_b == TG_OP_N ? 0 : q);
         const int gj = col0 + c + (a.op_b == TG_OP_N ? q : 0);
-        const bool in = gj < a.N && gk < a.K;
+        const bool in = gj < a.N && gk < kend;
         v[q] = in ? (a.op_b == TG_OP_N ? a.B[(long long)gk * a.ldb + gj] : a.B[(long long)gj * a.ldb + gk]) : 0.0f;
     }
 }
@@ -1438,9 +1446,15 @@ __device__ __forceinline__ void tiled_load_b(const TiledArgs& a, int col0, int k
 __global__ void __launch_bounds__(kTiledThreads) tiled_gemm_kernel(TiledArgs a) {
     __shared__ __align__(16) float As[2][kTiledBK][kTiledPitch];
     __shared__ __align__(16) float Bs[2][kTiledBK][kTiledPitch];
+    __shared__ __align__(16) float part[kTiledBM][kTiledBN];  // this K slice's partial tile (split > 1)
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int tiles_n = (a.N + kTiledBN - 1) / kTiledBN;
-    const int row0 = (int)(blockIdx.x / tiles_n) * kTiledBM, col0 = (int)(blockIdx.x % tiles_n) * kTiledBN;
+    // a cluster of `split` consecutive blocks per tile, block s of it on K slice s
+    const int tile = (int)(blockIdx.x / a.split), s = (int)(blockIdx.x % a.split);
+    const int row0 = (tile / tiles_n) * kTiledBM, col0 = (tile % tiles_n) * kTiledBN;
+    // this slice's K range: whole 16-wide blocks, the last one clipped to K
+    const int kbeg = (int)((long long)s * a.nkb / a.split) * kTiledBK;
+    const int kend = min(a.K, (int)((long long)(s + 1) * a.nkb / a.split) * kTiledBK);
     grid_dep_wait();  // operands written by the previous kernel of the stream
     float acc[4][4];
 #pragma unroll
@@ -1450,10 +1464,10 @@ __global__ void __launch_bounds__(kTiledThreads) tiled_gemm_kernel(TiledArgs a) 
 
     float va[4], vb[4];
     int ar, ak, bc, bk;
-    tiled_load_a(a, row0, 0, va, ar, ak);
-    tiled_load_b(a, col0, 0, vb, bc, bk);
+    tiled_load_a(a, row0, kbeg, kend, va, ar, ak);
+    tiled_load_b(a, col0, kbeg, kend, vb, bc, bk);
     int buf = 0;
-    for (int k0 = 0; k0 < a.K; k0 += kTiledBK) {
+    for (int k0 = kbeg; k0 < kend; k0 += kTiledBK) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) As[buf][ak + q][ar] = va[q];
         if (a.op_b == TG_OP_N) {
@@ -1464,9 +1478,9 @@ __global__ void __launch_bounds__(kTiledThreads) tiled_gemm_kernel(TiledArgs a) 
             for (int q = 0; q < 4; ++q) Bs[buf][bk + q][bc] = vb[q];
         }
         __syncthreads();
-        if (k0 + kTiledBK < a.K) {  // the next stage's loads overlap this stage's math
-            tiled_load_a(a, row0, k0 + kTiledBK, va, ar, ak);
-            tiled_load_b(a, col0, k0 + kTiledBK, vb, bc, bk);
+        if (k0 + kTiledBK < kend) {  // the next stage's loads overlap this stage's math
+            tiled_load_a(a, row0, k0 + kTiledBK, kend, va, ar, ak);
+            tiled_load_b(a, col0, k0 + kTiledBK, kend, vb, bc, bk);
         }
 #pragma unroll
         for (int k = 0; k < kTiledBK; ++k) {
@@ -1483,6 +1497,46 @@ __global__ void __launch_bounds__(kTiledThreads) tiled_gemm_kernel(TiledArgs a) 
         buf ^= 1;
     }
     grid_dep_launch();
+    if (a.split > 1) {
+        // partials into shared memory; the cluster barrier (release / acquire
+        // at cluster scope) makes every block's partial visible to the others
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4*>(&part[ty * 4 + i][tx * 4]) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        cluster_sync_all();
+        // 16-byte group g of the tile (row g / 16, columns 4 (g % 16)..) for
+        // g = s, s + split, ...: the sum over the slices in order
+        for (int g = s + a.split * tid; g < kTiledBM * kTiledBN / 4; g += a.split * kTiledThreads) {
+            const int rl = g >> 4, cl = (g & 15) * 4;
+            // every slice's group first (the remote loads overlap), then the
+            // sum in slice order
+            float4 x[kTiledMaxSplit];
+#pragma unroll
+            for (int j = 0; j < kTiledMaxSplit; ++j)
+                if (j < a.split) x[j] = ld_shared_cluster_f4(cluster_addr(&part[rl][cl], (uint32_t)j));
+            float4 v = x[0];
+#pragma unroll
+            for (int j = 1; j < kTiledMaxSplit; ++j) {
+                if (j < a.split) {
+                    v.x += x[j].x;
+                    v.y += x[j].y;
+                    v.z += x[j].z;
+                    v.w += x[j].w;
+                }
+            }
+            const int r = row0 + rl;
+            if (r < a.M) {
+                float* row = a.C + (long long)r * a.ldc;
+                if (a.scaled)
+                    store_row4_scaled(row, col0 + cl, a.N, v, a.vec_c != 0, a.alpha, a.beta);
+                else
+                    store_row4(row, col0 + cl, a.N, v, a.vec_c != 0);
+            }
+        }
+        cluster_sync_all();  // no block leaves while others may still read its partial
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = row0 + ty * 4 + i;
@@ -1738,11 +1792,16 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
         ta.beta = p.beta;
         ta.scaled = (p.alpha != 1.0f || p.beta != 0.0f) ? 1 : 0;
         ta.vec_c = p.vec_c ? 1 : 0;
+        ta.split = p.split;
+        ta.nkb = p.nkb;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return TG_ERR_CUDA;
-        NvtxRange r("tg_gemm");
-        if (launch_dependent(tiled_gemm_kernel, dim3((unsigned)((long long)p.tiles_m * p.tiles_n)),
-                             dim3(kTiledThreads), 0, stream, 1, ta) != TG_OK)
-            return TG_ERR_CUDA;
+        {
+            NvtxRange r("tg_gemm");
+            // a cluster of split blocks per tile (one block each when K is not split)
+            if (launch_dependent(tiled_gemm_kernel, dim3((unsigned)((long long)p.tiles_m * p.tiles_n * p.split)),
+                                 dim3(kTiledThreads), 0, stream, (unsigned)p.split, ta) != TG_OK)
+                return TG_ERR_CUDA;
+        }
         if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return TG_ERR_CUDA;
         return TG_OK;
     }

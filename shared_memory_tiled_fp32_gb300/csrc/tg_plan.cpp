@@ -147,11 +147,24 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
     p->tiles_n = (int)cdiv(N, p->bn);
     p->nkb = (int)cdiv(K, p->bk);
     const long long tiles = (long long)p->tiles_m * p->tiles_n;
-    if (p->path == TG_PATH_TILED) {  // one block per tile, one launch, no workspace
-        p->split = 1;
-        p->units = tiles;
-        p->full_units = tiles;
-        p->grid = (int)std::min<long long>(tiles, 0x7fffffffLL);
+    if (p->path == TG_PATH_TILED) {
+        // one block per tile and K slice.  K is split when the tiles would
+        // leave more than half the SMs idle and K has at least 8 blocks of 16,
+        // into as many slices as keep one block per SM, each at least two
+        // 16-wide stages, at most 8 (256^3: 16 tiles x 8 slices).  The
+        // slices of a tile run as one cluster and add their partials in
+        // shared memory: still one launch, no workspace
+        int S = 1;
+        if (split_k > 0)
+            S = std::min(split_k, p->nkb);
+        else if (tiles < num_sms / 2 && p->nkb >= 8)
+            S = (int)std::max<long long>(1, std::min<long long>({(long long)num_sms / tiles, (long long)p->nkb / 2,
+                                                                 (long long)kTiledMaxSplit}));
+        S = std::min(S, kTiledMaxSplit);
+        p->split = S;
+        p->units = tiles * S;
+        p->full_units = p->units;
+        p->grid = (int)std::min<long long>(p->units, 0x7fffffffLL);
         p->launches = 1;
         return;
     }

@@ -131,11 +131,19 @@ def test_plan_tiles_split_and_workspace():
     # K = 0 is one fill kernel
     z = tg.plan(10, 10, 0, num_sms=sms)
     assert z["launches"] == 1 and z["workspace_bytes"] == 0
-    # small products: the one-launch tiled path (64 x 64 tiles, no workspace,
-    # operands in place), unless a K split is asked for
+    # small products: the tiled path (64 x 64 tiles, operands in place, no
+    # pre-pass, one launch, no workspace).  16 tiles would leave most SMs
+    # idle, so K is split into 8 slices of two 16-wide stages: a cluster of 8
+    # blocks per tile adds the slices in shared memory (128 blocks)
     t = tg.plan(256, 256, 256, num_sms=sms)
-    assert (t["path"], t["tiles_m"], t["tiles_n"], t["launches"], t["workspace_bytes"], t["prepass"]) == \
-        ("tiled", 4, 4, 1, 0, 0)
+    assert (t["path"], t["tiles_m"], t["tiles_n"], t["split_k"], t["grid"], t["launches"], t["prepass"],
+            t["workspace_bytes"]) == ("tiled", 4, 4, 8, 128, 1, 0, 0)
+    # a short K (fewer than 8 blocks of 16) is not split
+    assert tg.plan(100, 100, 100, num_sms=sms)["split_k"] == 1
+    # an explicit split on the tiled path is honoured, at most 8 (one cluster)
+    v = tg.plan(200, 300, 100, num_sms=sms, path="tiled", split_k=3)
+    assert (v["split_k"], v["grid"], v["launches"]) == (3, 4 * 5 * 3, 1)
+    assert tg.plan(200, 300, 1000, num_sms=sms, path="tiled", split_k=12)["split_k"] == 8
     assert tg.plan(256, 256, 256, num_sms=sms, split_k=2)["path"] == "tf32x3"
     assert tg.plan(512, 512, 512, num_sms=sms)["path"] == "tf32x3"    # 2^27 multiply-adds
     assert tg.plan(64, 64, 8192, num_sms=sms)["path"] == "tf32x3"     # long K: split instead
