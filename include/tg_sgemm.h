@@ -275,7 +275,8 @@ tg_status tg_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream)
  * allocator and does not let libraries allocate, a latency-critical loop that
  * must never enter the CUDA allocator, or code that must not be able to fail
  * with out-of-memory once it runs.  tg_sgemm needs scratch memory (the hi/lo
- * copies of A and B, and K-slice partials); here that scratch is a fixed
+ * copies of B, and of A unless the GEMM kernel splits A itself, and K-slice
+ * partials); here that scratch is a fixed
  * array of TG_SGEMM_NOALLOC_SCRATCH_BYTES in device memory that CUDA reserves
  * when it loads this library's device code on a GPU (with CUDA's default lazy
  * loading: at the first tg_sgemm_noalloc call there) and that every such GPU

@@ -1,8 +1,9 @@
 // tg_sgemm_noalloc: the 3xTF32 product for callers that cannot allocate
 // device memory at call time.
 //
-// tg_sgemm needs scratch memory (the hi/lo tf32 copies of A and B, and the
-// K-slice partials when K is split) and normally takes it from a stream-ordered
+// tg_sgemm needs scratch memory (the hi/lo tf32 copies of B, and of A when
+// the GEMM kernel cannot split A itself; the K-slice or balanced-tail
+// partials when K is shared out) and normally takes it from a stream-ordered
 // memory pool or from the caller.  Some callers can do neither: a host
 // application that owns the whole device-memory budget through its own
 // allocator and forbids libraries from allocating, a latency-critical loop
