@@ -734,6 +734,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         break;
                     }
                     uint8_t* st = smem + stage * kStageBytes;
+                    // odd work items walk K backwards: the next item of a
+                    // round usually shares its A rows with this one, and
+                    // starting where this one ended finds them still in L2
+                    const int kq = (j & 1) ? t.kb0 + t.kb1 - 1 - kb : kb;
                     if (kPairMma) {
                         // this CTA's A tile and B half into its own ring.  Both
                         // CTAs' split-tile copies complete on the first CTA's
@@ -744,10 +748,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], kPairTx);
                         const uint32_t bar0 = cluster_addr(&full[stage], 0);
                         if (kRawA)
-                            tma_load_2d(st, &tmA, &rfull[stage], kb * BK, t.m0);
+                            tma_load_2d(st, &tmA, &rfull[stage], kq * BK, t.m0);
                         else
-                            tma_load_2d_pair(st, &tmA, bar0, 0, ((t.m0 >> 7) * args.kbs + kb) * 128);
-                        tma_load_2d_pair(st + kTfAStage, &tmB, bar0, 0, (((t.n0 >> 7) + rank) * args.kbs + kb) * 128);
+                            tma_load_2d_pair(st, &tmA, bar0, 0, ((t.m0 >> 7) * args.kbs + kq) * 128);
+                        tma_load_2d_pair(st + kTfAStage, &tmB, bar0, 0, (((t.n0 >> 7) + rank) * args.kbs + kq) * 128);
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == ST) {
@@ -759,8 +763,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                     // this CTA's A tile and the whole B tile (48 KiB), each
                     // 128-row tile one bulk copy into this CTA's own ring
                     mbar_arrive_expect_tx(&full[stage], kTfStageBytes);
-                    const float* a_src = args.a_tiles + ((long long)(t.m0 >> 7) * args.kbs + kb) * kTileFloats;
-                    const float* b_src = args.b_tiles + ((long long)(t.n0 >> 7) * args.kbs + kb) * kTileFloats;
+                    const float* a_src = args.a_tiles + ((long long)(t.m0 >> 7) * args.kbs + kq) * kTileFloats;
+                    const float* b_src = args.b_tiles + ((long long)(t.n0 >> 7) * args.kbs + kq) * kTileFloats;
                     bulk_load(st, a_src, kTfAStage, &full[stage]);
                     bulk_load(st + kTfAStage, b_src, kTfAStage, &full[stage]);
                     bulk_load(st + 2 * kTfAStage, b_src + (long long)args.kbs * kTileFloats, kTfAStage, &full[stage]);
