@@ -1304,68 +1304,83 @@ __global__ void __launch_bounds__(256)
 }
 
 // Balanced last round: every tail unit that more than one lane ran is the
-// sum of its pieces' partials, added in a fixed order (deterministic), float4
-// per thread.  Stream-K runs: lane order; a unit run whole by one lane was
-// stored by the GEMM kernel.  Split point: the unit's first part, then the
-// pieces of its remainder in lane order.
+// sum of its pieces' partials, added in a fixed order (deterministic).
+// Stream-K runs: lane order; a unit run whole by one lane was stored by the
+// GEMM kernel.  Split point: the unit's first part, then the pieces of its
+// remainder in lane order.  A block takes a band of rows of one unit at a
+// time (4 rows of 16-byte groups per thread, blockDim / (BN / 4) rows per
+// pass), so the unit's lanes and slots are worked out once per band, not for
+// every element: with the 64-bit divisions they need, per element they made
+// the kernel instruction-bound (20 us for a 2048 x 2048 split-point tail).
 __global__ void __launch_bounds__(256)
     tail_reduce_kernel(GemmArgs a, float* C, long long ldc, int BM, int BN, int vec_c) {
     grid_dep_wait();  // every partial is written
+    constexpr int kRowsPerThread = 4;
     const int rows = a.pair * BM, q4 = BN / 4;
+    const int rstep = blockDim.x / q4, band = kRowsPerThread * rstep;
+    const int bands = (rows + band - 1) / band;
     const long long block = (long long)rows * BN;
-    const long long total = a.tail_units * rows * q4;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long q = i / ((long long)rows * q4);
-        const int rem = (int)(i - q * rows * q4);
-        const int r = rem / q4, c = (rem % q4) * 4;
-        long long v0, v1, T, lanes, base;
+    const long long items = a.tail_units * bands;
+    const int tr = threadIdx.x / q4, c = (threadIdx.x % q4) * 4;
+    for (long long b = blockIdx.x; b < items; b += gridDim.x) {
+        const long long q = b / bands;
+        const int r0 = (int)(b - q * bands) * band + tr;
+        long long v0, v1, T, lanes, first;
         if (a.tail_kx > 0) {
             const long long rl = a.nkb - a.tail_kx;
             T = a.tail_units * rl;
             lanes = a.tail_lanes - a.tail_units;
             v0 = tail_lane_of(q * rl, T, lanes);
             v1 = tail_lane_of((q + 1) * rl - 1, T, lanes);
-            base = q * a.tail_slots;
+            first = q * a.tail_slots;  // the unit's first part
         } else {
             T = a.tail_units * a.nkb;
             lanes = a.tail_lanes;
             v0 = tail_lane_of(q * a.nkb, T, lanes);
             v1 = tail_lane_of((q + 1) * a.nkb - 1, T, lanes);
             if (v0 == v1) continue;
-            base = 0;
+            first = 2 * v0 + (tail_run_begin(v0, T, lanes) / a.nkb == q ? 0 : 1);
         }
         int tm, tn;
         unit_tile(a.tiles_m, a.tiles_n, a.full_units + q, &tm, &tn);
-        const int m = tm * rows + r, n = tn * BN + c;
-        if (m >= a.M || n >= a.N) continue;
-        const float* tile = a.tail + (long long)r * BN + c;
-        float4 s;
-        if (a.tail_kx > 0) s = *reinterpret_cast<const float4*>(tile + base * block);
-        for (long long v = v0; v <= v1; ++v) {
+        const int n = tn * BN + c;
+        bool ok[kRowsPerThread];
+        float4 s[kRowsPerThread];
+        const float* tile = a.tail + (long long)r0 * BN + c;
+#pragma unroll
+        for (int u = 0; u < kRowsPerThread; ++u) {
+            const int r = r0 + u * rstep;
+            ok[u] = r < rows && tm * rows + r < a.M && n < a.N;
+            s[u] = ok[u] ? *reinterpret_cast<const float4*>(tile + first * block + (long long)u * rstep * BN)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (long long v = a.tail_kx > 0 ? v0 : v0 + 1; v <= v1; ++v) {
             // stream-K: slot 2v holds lane v's first piece, 2v + 1 its last;
-            // split point: slot base + 1 + (v - v0)
+            // split point: slot first + 1 + (v - v0)
             long long slot;
-            if (a.tail_kx > 0) {
-                slot = base + 1 + (v - v0);
-            } else {
-                const long long first_q = tail_run_begin(v, T, lanes) / a.nkb;
-                slot = 2 * v + (first_q == q ? 0 : 1);
-            }
-            const float4 x = *reinterpret_cast<const float4*>(tile + slot * block);
-            if (v == v0 && a.tail_kx == 0) {
-                s = x;
-            } else {
-                s.x += x.x;
-                s.y += x.y;
-                s.z += x.z;
-                s.w += x.w;
+            if (a.tail_kx > 0)
+                slot = first + 1 + (v - v0);
+            else
+                slot = 2 * v + (tail_run_begin(v, T, lanes) / a.nkb == q ? 0 : 1);
+#pragma unroll
+            for (int u = 0; u < kRowsPerThread; ++u) {
+                if (!ok[u]) continue;
+                const float4 x = *reinterpret_cast<const float4*>(tile + slot * block + (long long)u * rstep * BN);
+                s[u].x += x.x;
+                s[u].y += x.y;
+                s[u].z += x.z;
+                s[u].w += x.w;
             }
         }
-        if (a.scaled)
-            store_row4_scaled(C + (long long)m * ldc, n, a.N, s, vec_c != 0, a.alpha, a.beta);
-        else
-            store_row4(C + (long long)m * ldc, n, a.N, s, vec_c != 0);
+#pragma unroll
+        for (int u = 0; u < kRowsPerThread; ++u) {
+            if (!ok[u]) continue;
+            float* row = C + (long long)(tm * rows + r0 + u * rstep) * ldc;
+            if (a.scaled)
+                store_row4_scaled(row, n, a.N, s[u], vec_c != 0, a.alpha, a.beta);
+            else
+                store_row4(row, n, a.N, s[u], vec_c != 0);
+        }
     }
 }
 
@@ -1959,8 +1974,10 @@ tg_status launch_plan(const Plan& p, const float* A, const float* B, float* C, v
 
     NvtxRange r("tg_reduce");
     if (p.tail_lanes > 0) {
+        // bands of 4 rows x 256 threads' worth of 16-byte groups (see the kernel)
+        static_assert(256 % (kTf32BN / 4) == 0 && 256 % (kFfmaBN / 4) == 0, "a pass covers whole rows");
         const long long work = p.tail_units * p.pair * p.bm * (p.bn / 4);
-        if (launch_dependent(tail_reduce_kernel, dim3(elementwise_grid(work, 256)), dim3(256), 0, stream, 1, ga, C,
+        if (launch_dependent(tail_reduce_kernel, dim3(elementwise_grid(work, 4 * 256)), dim3(256), 0, stream, 1, ga, C,
                              (long long)p.ldc, p.bm, p.bn, p.vec_c ? 1 : 0) != TG_OK)
             return TG_ERR_CUDA;
     }
