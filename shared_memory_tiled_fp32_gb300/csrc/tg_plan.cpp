@@ -315,9 +315,9 @@ void make_plan(int op_a, int op_b, int M, int N, int K, float alpha, const void*
 // Modelled duration (seconds) of one planned product: its rounds of work
 // units over the lanes (whole rounds, plus the tail's share of a unit per
 // lane), each unit taking its tile's flops at the path's per-lane rate, plus
-// a fixed 45 us per product (pipeline fill and drain, reduce, launch gaps
+// a fixed 35 us per product (pipeline fill and drain, reduce, launch gaps
 // and the host's own issue of the product's copies and launches; fitted on
-// GB300 to 40 measured 8192^3 host-buffer layouts, RMS error 0.06 ms).
+// GB300 to 80 measured 8192^3 host-buffer layouts, RMS error 0.04 ms).
 double product_seconds(const Plan& p, double rate) {
     if (p.M == 0 || p.N == 0 || p.K == 0) return 5e-6;
     const long long lanes = std::max(1, p.grid / p.pair);
@@ -327,7 +327,7 @@ double product_seconds(const Plan& p, double rate) {
     else
         rounds = (double)cdiv(p.units, lanes);
     const double unit_flops = 2.0 * p.pair * p.bm * p.bn * ((double)p.K / p.split);
-    return rounds * unit_flops / (rate / std::max(1, p.num_sms / p.pair)) + 45e-6;
+    return rounds * unit_flops / (rate / std::max(1, p.num_sms / p.pair)) + 35e-6;
 }
 
 // Host-buffer pipeline model: a small event simulation of one call.  Copies
@@ -337,11 +337,16 @@ double product_seconds(const Plan& p, double rate) {
 // a full-width one) are in; each C block is copied out on a second copy
 // stream once its product is done (with defer_out, not before the last copy
 // in).  Rates measured on GB300 over NVLink-C2C with pinned host memory:
-// 205 GB/s in alone, 190 GB/s out alone, about 170 GB/s each way while both
-// directions are busy, plus ~40 us per copy out; the split pre-pass about
-// 5.7 TB/s; a full round of work units 385 (3xTF32, A split in the kernel)
-// or 62 (FFMA) useful TFLOP/s.  Fitted to the measured 8192^3 layouts
-// within ~2 %.
+// 205 GB/s in alone, 190 GB/s out alone, about 150 GB/s each way while both
+// directions are busy, plus ~40 us per copy out that does not start right
+// behind another (a queued copy out follows the previous one without it:
+// with this term the model ranks the layouts whose copies out wait for the
+// last copy in correctly; without it, it put them up to 0.33 ms too slow);
+// the split pre-pass about 5.7 TB/s; a full round of work units 375 (3xTF32,
+// A split in the kernel; products inside the pipeline are smaller than a
+// whole call) or 62 (FFMA) useful TFLOP/s.  Fitted to 80 measured 8192^3
+// layouts, RMS error 0.04 ms; its choice was the measured best within
+// 0.1 %.
 namespace {
 
 struct HostCopy {
@@ -355,15 +360,17 @@ struct HostProduct {
 
 double simulate_host_pipeline(const std::vector<HostCopy>& ins, const std::vector<HostProduct>& prods, int pm,
                               int pn, bool defer_out) {
-    const double r_in = 205e9, r_out = 190e9, r_both = 170e9;
+    const double r_in = 205e9, r_out = 190e9, r_both = 150e9, out_fixed_bytes = 40e-6 * 190e9;
     std::vector<char> a_in(pm, 0), b_in(pn, 0);
     size_t ik = 0, pk = 0, oh = 0;
     double t = 0.0, in_rem = ins.empty() ? 0.0 : ins[0].bytes, gpu_end = -1.0, out_rem = -1.0;
     std::vector<double> outq;
+    double out_done = -1.0;  // when the last copy out ended
     for (int iter = 0; iter < 100000; ++iter) {
         if (gpu_end < 0.0 && pk < prods.size() && a_in[prods[pk].a_block] && b_in[prods[pk].b_block])
             gpu_end = t + prods[pk].seconds;
-        if (out_rem < 0.0 && oh < outq.size() && (!defer_out || ik >= ins.size())) out_rem = outq[oh++];
+        if (out_rem < 0.0 && oh < outq.size() && (!defer_out || ik >= ins.size()))
+            out_rem = outq[oh++] + (out_done == t ? 0.0 : out_fixed_bytes);
         const bool in_busy = ik < ins.size(), out_busy = out_rem >= 0.0;
         if (!in_busy && !out_busy && gpu_end < 0.0) return pk == prods.size() ? t : 1e30;
         const double ri = in_busy ? (out_busy ? r_both : r_in) : 0.0;
@@ -384,7 +391,10 @@ double simulate_host_pipeline(const std::vector<HostCopy>& ins, const std::vecto
         }
         if (out_busy) {
             out_rem -= ro * dt;
-            if (out_rem <= 1.0) out_rem = -1.0;
+            if (out_rem <= 1.0) {
+                out_rem = -1.0;
+                out_done = t;
+            }
         }
         if (gpu_end >= 0.0 && gpu_end <= t + 1e-12) {
             outq.push_back(prods[pk++].out_bytes);
@@ -403,7 +413,7 @@ class HostModel {
         : M_(M), N_(N), K_(K), path_(path), sms_(num_sms), tf32_(path != TG_PATH_FFMA) {}
 
     double ms(const HostBlocks& hb) {
-        const double bw_split = 5.7e12, out_fixed_bytes = 40e-6 * 190e9;
+        const double bw_split = 5.7e12;
         ins_.clear();
         prods_.clear();
         ins_.push_back({4.0 * hb.rows(0, M_) * K_, 0, -1});
@@ -418,7 +428,7 @@ class HostModel {
                     if (j == 0 && !raw_a(rows, cols)) sec += 12.0 * rows * K_ / bw_split;
                     if (i == 0) sec += 12.0 * cols * K_ / bw_split;
                 }
-                prods_.push_back({i, nc == 1 ? hb.pn - 1 : j, sec, 4.0 * rows * cols + out_fixed_bytes});
+                prods_.push_back({i, nc == 1 ? hb.pn - 1 : j, sec, 4.0 * rows * cols});
             }
         }
         return simulate_host_pipeline(ins_, prods_, hb.pm, hb.pn, hb.defer_out) * 1e3;
@@ -438,7 +448,7 @@ class HostModel {
         auto it = product_s_.find({rows, cols});
         if (it != product_s_.end()) return it->second;
         const Plan pl = plan(rows, cols);
-        const double t = product_seconds(pl, path_ == TG_PATH_TF32_BF16 ? 525e12 : (tf32_ ? 385e12 : 62e12));
+        const double t = product_seconds(pl, path_ == TG_PATH_TF32_BF16 ? 525e12 : (tf32_ ? 375e12 : 62e12));
         return product_s_[{rows, cols}] = {t, pl.raw_a};
     }
     double product(int rows, int cols) { return product_info(rows, cols).first; }
