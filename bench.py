@@ -49,7 +49,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_ma
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--alpha", type=float, default=1.0)
     ap.add_argument("--beta", type=float, default=0.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--sustained-s", type=float, default=1.0,
+                    help="seconds of back-to-back steps for the sustained line (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline (profiling runs)")
@@ -521,6 +523,36 @@ def main():
     ms_per_step = elapsed_ms / args.steps
     value = job_tflops(w.flop, world, ms_per_step)
 
+    # Sustained: the same step back to back for about --sustained-s seconds,
+    # without the per-kernel events (which separate the call's launches), so
+    # the part runs into its power limit as a long job does; a short timed
+    # region (the default 20 steps, ~60 ms at 8192^3) measures the burst rate.
+    sustained_line = None
+    if args.sustained_s > 0:
+        n_sus = max(args.steps, int(args.sustained_s / max(ms_per_step * 1e-3, 1e-6)))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler2 = ClockSampler(local)
+        sampler2.start()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        w0 = time.time()
+        s0.record(stream)
+        for _ in range(n_sus):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        w1 = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        sus_clocks = sampler2.stop(w0, w1)
+        (sus_ms,) = max_over_ranks([s0.elapsed_time(s1)], dev)
+        if tg.sync_status() != 0:
+            raise RuntimeError("a kernel reported a timeout in the sustained region")
+        sustained_line = {"value": job_tflops(w.flop, world, sus_ms / n_sus), "unit": "TFLOP/s",
+                          "steps": n_sus, "ms_per_step": sus_ms / n_sus, "seconds": sus_ms * 1e-3,
+                          "clocks": sus_clocks}
+
     # end to end through the host-buffer entry point (pinned memory; the
     # untransposed product, which is what that entry point computes)
     e2e_s = None
@@ -592,6 +624,14 @@ def main():
         peak_note = "152 SMs x 128 FMA lanes x 2 FLOP x max SM clock"
         kernel_tag = "ffma_gemm"
     traffic = traffic_from_profiles(kernel_tag, w.name)
+    if sustained_line is not None and plan["path"] in ("tf32x3", "tf32bf16"):
+        # the whole step (pre-pass and reduce included) against the sustained
+        # peak of the same derivation as the roofline's
+        bf16s = peaks["bf16_tflops_sustained"]
+        tf32s = bf16s * TF32_OVER_BF16
+        ps = tf32s / 3.0 if plan["path"] == "tf32x3" else 1.0 / (1.0 / tf32s + 2.0 / bf16s)
+        sustained_line["peak_sustained"] = ps
+        sustained_line["step_frac_of_peak"] = sustained_line["value"] / world / ps
 
     # correctness and the CPU baseline on the same seeded row sample
     cpu = None
@@ -722,6 +762,7 @@ def main():
         "gpu_launches": plan["launches"] * args.steps,
         "max_rel_error": max_rel,
         "clocks": clocks,
+        "sustained": sustained_line,
         "probes": probes,
         "secondary": secondary,
         "alt_path": alt,

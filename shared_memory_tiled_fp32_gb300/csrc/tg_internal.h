@@ -47,13 +47,15 @@ constexpr size_t kWsAlign = 256;
 // Tile-unit index t (K slices aside) -> (tile-unit row, tile column).  Tiles
 // are visited in groups of kGroupM tile-unit rows, column by column inside a
 // group, so CTAs running at the same time share A rows and B columns in L2.
-// A round of 76 pair units then covers 12 pair rows x 6.3 columns: per K
-// value 12 x 256 rows of raw A (4 bytes) and 6.3 x 256 rows of split B (8
-// bytes), near the least for 76 units (rows of A twice the columns of B).
-// Measured on GB300, 8192^3: 3.14 GB DRAM read per launch against 3.41 with
-// groups of 8 pair rows, same kernel time; grouping by columns instead (8
-// tile columns, rows inside) read 3.41 GB.
-constexpr int kGroupM = 12;
+// With 76 CTA pairs a round of pair units is then a block of 19 pair rows x
+// 4 columns, and the next round (the next 4 columns) keeps the same A rows;
+// the 3xTF32 kernel walks K backwards on every second work item, so a round
+// starts on the K range of A the previous one ended with, still in L2.
+// Measured on GB300, 8192^3 DRAM read per launch (same kernel time within
+// 1 %): groups of 8 pair rows 3.30 GB, 12 2.96, 16 2.96, 19 2.80, 24 3.27,
+// 32 4.00; before K was walked backwards, 8 rows 3.41 and 12 rows 3.14;
+// grouping by columns instead (8 tile columns, rows inside) read 3.41 GB.
+constexpr int kGroupM = 19;
 
 TG_HOST_DEVICE inline void unit_tile(int tiles_m, int tiles_n, long long t, int* tm, int* tn) {
     const long long per_group = (long long)kGroupM * tiles_n;

@@ -734,8 +734,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                         break;
                     }
                     uint8_t* st = smem + stage * kStageBytes;
-                    // odd work items walk K backwards: the next item of a
-                    // round usually shares its A rows with this one, and
+                    // odd work items walk K backwards: this lane's next item
+                    // (in the next round) usually has the same A rows, and
                     // starting where this one ended finds them still in L2
                     const int kq = (j & 1) ? t.kb0 + t.kb1 - 1 - kb : kb;
                     if (kPairMma) {

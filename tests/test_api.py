@@ -73,15 +73,23 @@ def test_plan_tiles_split_and_workspace():
     assert (p["path"], p["tiles_m"], p["tiles_n"], p["split_k"]) == ("tf32x3", 64, 32, 1)
     # pairs of vertically adjacent tiles share B (cluster of 2 CTAs); 1024 pair
     # units on 76 pairs leave 36 after 13 whole rounds.  Their A and B rows
-    # (2048 rows + 1280 columns of K = 8192, hi and lo) exceed L2, so each is
-    # cut into 2 equal K slices: 72 lanes, half a round
+    # (groups of 19 pair rows: the last 36 units are 3 columns of the second
+    # group's 13 pair rows, 3328 rows + 768 columns of K = 8192, hi and lo)
+    # exceed L2, so each is cut into 2 equal K slices: 72 lanes, half a round
     assert p["pair"] == 2 and p["grid"] == sms and p["launches"] == 3
     assert (p["tail_units"], p["tail_lanes"]) == (36, 72)
     assert p["units"] == 32 * 32
     # A_hi, A_lo, B_hi^T, B_lo^T, plus two partial slots of 256 x 256 per lane
     assert p["workspace_bytes"] == 4 * 8192 * 8192 * 4 + 2 * 72 * 256 * 256 * 4
-    # 4096^3: the 28-unit tail's rows fit in L2 -> stream-K over all 76 pairs
+    # 4096^3: the 28-unit tail (the last two columns of one group of all 16
+    # pair rows) reads all 4096 rows of A and 512 columns of B.  Split by the
+    # pre-pass (no A given: 8 bytes per element) that is 150 MB, past L2 ->
+    # 2 equal K slices, 56 lanes; A split in the kernel (4 bytes) 84 MB ->
+    # stream-K over all 76 pairs
     m = tg.plan(4096, 4096, 4096, num_sms=sms)
+    assert (m["units"], m["tail_units"], m["tail_lanes"]) == (256, 28, 56)
+    m = tg.plan(4096, 4096, 4096, A=1 << 40, B=2 << 40, C=3 << 40, num_sms=sms)
+    assert m["fused_split"] == 1
     assert (m["units"], m["tail_units"], m["tail_lanes"]) == (256, 28, 76)
     # an explicit split turns the tail balancing off
     q = tg.plan(8192, 8192, 8192, num_sms=sms, split_k=1)
