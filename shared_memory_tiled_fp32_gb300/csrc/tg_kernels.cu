@@ -1009,7 +1009,30 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                                                    acc[cb * 32 + 4 * g + 2], acc[cb * 32 + 4 * g + 3]);
                 __syncwarp();
                 const int col = t.n0 + h * 128 + cb * 32 + lane;
-                if (col < args.N) {
+                // 16-byte stores (lanes 8k..8k+7 take the 8 groups of row k +
+                // 4i, four 128-byte rows per instruction) where rows start on
+                // 16 bytes and no split-point tail runs: measured against the
+                // one-row-per-instruction form below, 2048^3 83.5 vs 85.3 us,
+                // 777 x 1029 x 513 26.5 vs 27.5 us, 4096^3 kernel 373.5 vs 369.5
+                // TFLOP/s, 8192^3 equal; with a split point (2048 x 2048 x
+                // 16384) the pieces' 16-byte stores slowed the kernel ~1 %.
+                // 3xTF32 pair forms only: the mixed instantiation spilled
+                const bool vec4 = t.direct ? args.vec_out != 0 : true;
+                if (kPairMma && !kMixed && args.tail_kx == 0 && vec4 && !(scaled && args.beta != 0.0f)) {
+                    const int g = lane & 7;
+                    const int colg = t.n0 + h * 128 + cb * 32 + 4 * g;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = (lane >> 3) + 4 * i;
+                        if (r < rows) {
+                            // group g of row r sits at r*32 + 4*(g ^ (r & 7))
+                            float4 v = *reinterpret_cast<const float4*>(stg + r * 32 + 4 * (g ^ (r & 7)));
+                            if (scaled)
+                                v = make_float4(args.alpha * v.x, args.alpha * v.y, args.alpha * v.z, args.alpha * v.w);
+                            store_row4(t.out + (long long)(row0 + r) * t.ldo, colg, args.N, v, true);
+                        }
+                    }
+                } else if (col < args.N) {
                     // (r, lane) sits at r*32 + (lane ^ 4*(r & 7))
                     float* dst = t.out + (long long)row0 * t.ldo + col;
                     if (scaled && args.beta != 0.0f) {
