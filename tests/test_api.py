@@ -401,3 +401,26 @@ def test_host_blocks_pipeline_large_products():
     # below 2^33 multiply-adds: one block (bit-identical to the device entry)
     small = tg.host_blocks(777, 1029, 513, path="tf32x3", num_sms=152)
     assert (small["row_blocks"], small["col_blocks"]) == (1, 1)
+
+
+def test_host_model_queued_copies_out(monkeypatch):
+    """The host-pipeline model charges the ~40 us of a copy out only when it
+    does not start right behind another queued copy out: with the copies out
+    held until the copies in are done (they then queue), a layout with eight
+    first-row-block products costs little more than one with four, and the
+    model's choice for 8192^3 is the measured best of 80 layouts (first block
+    2560 rows in 1024-column blocks, later blocks of 1024 rows, copies out
+    held)."""
+    monkeypatch.delenv("TG_HOST_BLOCKS", raising=False)
+    h = tg.host_blocks(8192, 8192, 8192, path="tf32x3", num_sms=152)
+    assert (h["first_block_rows"], h["block_rows"], h["block_cols"], h["defer_copies_out"]) == (2560, 1024, 1024, 1)
+
+    def modelled(layout):
+        monkeypatch.setenv("TG_HOST_BLOCKS", layout)
+        return tg.host_blocks(8192, 8192, 8192, path="tf32x3", num_sms=152)["model_ms"]
+
+    held8, held4 = modelled("2560,1024,1024,1,1"), modelled("2560,1024,2048,1,1")
+    open8 = modelled("2560,1024,1024,1,0")
+    # measured: 4.26, 4.41 and 4.50 ms
+    assert held8 < held4 and held8 < open8
+    assert 4.0 < held8 < 4.6

@@ -305,6 +305,25 @@ def test_fused_split_warps_access_conflict_free():
             assert wavefronts_128(addrs) == min_wavefronts_128(addrs) == 4
 
 
+
+def test_tensor_epilogue_staging_block_conflict_free():
+    """The 3xTF32 epilogue's 32 x 32 staging block: lane r writes row r's
+    eight 16-byte groups, group g at position g ^ (r % 8); it is read back
+    either one column per lane (4-byte reads, one 128-byte row per store) or,
+    in the 16-byte store form, lanes 8k..8k+7 reading the 8 groups of row k +
+    4i.  Every access takes the minimum number of wavefronts."""
+    def at(r, g):
+        return 4 * (32 * r + 4 * (g ^ (r & 7)))  # bytes
+    for g in range(8):  # the writes: lane r, group g (one instruction per g)
+        addrs = [at(r, g) for r in range(32)]
+        assert wavefronts_128(addrs) == min_wavefronts_128(addrs) == 4
+    for r in range(32):  # 4-byte reads: lane l, column l of row r
+        assert wavefronts_32([4 * (32 * r) + 4 * (l ^ ((r & 7) << 2)) for l in range(32)]) == 1
+    for i in range(8):  # 16-byte reads: lane l, group l % 8 of row l // 8 + 4i
+        addrs = [at(l // 8 + 4 * i, l % 8) for l in range(32)]
+        assert wavefronts_128(addrs) == min_wavefronts_128(addrs) == 4
+
+
 # ------------------------------------------------------- transpose workload
 
 
