@@ -633,10 +633,12 @@ def main():
         sustained_line["peak_sustained"] = ps
         sustained_line["step_frac_of_peak"] = sustained_line["value"] / world / ps
 
-    # correctness and the CPU baseline on the same seeded row sample
+    # correctness and the CPU baseline on the same seeded row sample (one
+    # GPU only: with N ranks the others have left, and the baseline is a
+    # single-process figure)
     cpu = None
     max_rel = None
-    if not args.no_cpu and not general:
+    if not args.no_cpu and not general and world == 1:
         rows, ref, cpu = cpu_baseline(w, A.numpy(), B.numpy(), args.cpu_seconds)
         got = Cd[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
         r64 = ref.astype(np.float64)
